@@ -1,0 +1,219 @@
+"""Float64 CPU oracle -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never imports it and
+it never imports the CUDA library; the only code both sides share is the
+seeded input generator module, which holds none of the method's arithmetic.
+
+The arithmetic lives in ``oracle.c`` (plain triple loops in double precision,
+one function per definition, each citing the page and section it follows).
+This module compiles it with gcc on first use and marshals numpy arrays.
+
+Parity status per function (what pins it is in ``tests/test_oracle_*.py``):
+  plan_shards, owner          pinned (worked example + brute force vs numpy)
+  matmul                      pinned (numpy matmul, finite differences,
+                              torch float64 autograd, sharded == unsharded)
+  act, act_grad               pinned (torch gelu/tanh, closed forms, FD)
+  mlp_rows, mlp_cols          pinned (finite differences, torch autograd)
+  ce_tokens, ce_sharded_one   pinned (closed-form softmax on the worked
+                              example's logits, torch cross_entropy, FD)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ACT_GELU_ERF, ACT_GELU_TANH, ACT_TANH = 0, 1, 2
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+def compile_oracle(src: str = _SRC, out: str = _LIB_PATH, extra_flags=()) -> str:
+    """Compile ``src`` into the shared library ``out`` with gcc (-O2, OpenMP).
+
+    No fast-math and no FMA contraction, so every product and sum is the
+    IEEE double operation the source states."""
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-std=c11", src, "-o", out, "-lm", *extra_flags]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _declare(lib):
+    lib.orc_num_threads.restype = ctypes.c_int
+    lib.orc_plan_shards.argtypes = [ctypes.c_int64, ctypes.c_int32, _i64p]
+    lib.orc_plan_shards.restype = ctypes.c_int
+    lib.orc_owner.argtypes = [ctypes.c_int64, _i64p, ctypes.c_int32]
+    lib.orc_owner.restype = ctypes.c_int32
+    lib.orc_matmul.argtypes = [ctypes.c_int64] * 3 + [_dp] * 6
+    lib.orc_matmul.restype = None
+    lib.orc_act.argtypes = [ctypes.c_int, ctypes.c_double]
+    lib.orc_act.restype = ctypes.c_double
+    lib.orc_act_grad.argtypes = [ctypes.c_int, ctypes.c_double]
+    lib.orc_act_grad.restype = ctypes.c_double
+    lib.orc_mlp_rows.argtypes = [ctypes.c_int64] * 3 + [_dp] * 4 + [ctypes.c_int, ctypes.c_int64, _i64p, _dp, _dp]
+    lib.orc_mlp_rows.restype = None
+    lib.orc_mlp_cols.argtypes = [ctypes.c_int64] * 3 + [_dp] * 4 + [ctypes.c_int, ctypes.c_int64, _i64p, _dp, _dp]
+    lib.orc_mlp_cols.restype = None
+    lib.orc_ce_tokens.argtypes = ([ctypes.c_int64] * 3 + [_dp, _dp, _i64p, ctypes.c_int32, ctypes.c_int64, _i64p,
+                                  _dp, _dp, _dp, _i32p])
+    lib.orc_ce_tokens.restype = ctypes.c_int
+    lib.orc_ce_sharded_one.argtypes = [ctypes.c_int64, _dp, ctypes.c_int64, ctypes.c_int32, _dp, _dp, _dp]
+    lib.orc_ce_sharded_one.restype = ctypes.c_double
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building if needed) the oracle library.  With ``path`` given,
+    load that file instead (used by the mutation tests)."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            stale = (not os.path.exists(_LIB_PATH)
+                     or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+            if stale:
+                compile_oracle()
+            _lib = _declare(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+class Oracle:
+    """numpy-facing wrapper over one loaded copy of the oracle library."""
+
+    def __init__(self, lib=None):
+        self.lib = lib if lib is not None else load()
+
+    # -- helpers ---------------------------------------------------------
+    @staticmethod
+    def _f64(a):
+        return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+    @staticmethod
+    def _p(a, t=_dp):
+        return a.ctypes.data_as(t) if a is not None else None
+
+    def num_threads(self) -> int:
+        return int(self.lib.orc_num_threads())
+
+    # -- shard plan ------------------------------------------------------
+    def plan_shards(self, dim: int, parts: int) -> np.ndarray:
+        off = np.zeros(max(parts, 0) + 1, dtype=np.int64)
+        rc = self.lib.orc_plan_shards(dim, parts, self._p(off, _i64p))
+        if rc != 0:
+            raise ValueError("partition" if rc == 2 else "shape")
+        return off
+
+    def owner(self, y: int, off: np.ndarray) -> int:
+        off = np.ascontiguousarray(off, dtype=np.int64)
+        return int(self.lib.orc_owner(int(y), self._p(off, _i64p), len(off) - 1))
+
+    # -- GEMM ------------------------------------------------------------
+    def matmul(self, A, B, G):
+        """(Y, dA, dB) of L = <G, AB>, unsharded, float64."""
+        A, B, G = self._f64(A), self._f64(B), self._f64(G)
+        M, K = A.shape
+        K2, N = B.shape
+        if K2 != K or G.shape != (M, N):
+            raise ValueError("shape")
+        Y = np.empty((M, N))
+        dA = np.empty((M, K))
+        dB = np.empty((K, N))
+        self.lib.orc_matmul(M, K, N, self._p(A), self._p(B), self._p(G),
+                            self._p(Y), self._p(dA), self._p(dB))
+        return Y, dA, dB
+
+    # -- activations -----------------------------------------------------
+    def act(self, kind: int, x) -> np.ndarray:
+        x = np.asarray(x, dtype=np.float64)
+        return np.vectorize(lambda v: self.lib.orc_act(kind, float(v)), otypes=[np.float64])(x)
+
+    def act_grad(self, kind: int, x) -> np.ndarray:
+        x = np.asarray(x, dtype=np.float64)
+        return np.vectorize(lambda v: self.lib.orc_act_grad(kind, float(v)), otypes=[np.float64])(x)
+
+    # -- MLP (weights in (in, out) layout: W1 d x F, W2 F x d) -------------
+    def mlp_rows(self, X, W1, W2, GY, act: int, rows=None):
+        X, W1, W2, GY = map(self._f64, (X, W1, W2, GY))
+        T, d = X.shape
+        F = W1.shape[1]
+        rows = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        Y = np.empty((len(rows), d))
+        dX = np.empty((len(rows), d))
+        self.lib.orc_mlp_rows(T, d, F, self._p(X), self._p(W1), self._p(W2), self._p(GY), act,
+                              len(rows), self._p(rows, _i64p), self._p(Y), self._p(dX))
+        return Y, dX
+
+    def mlp_cols(self, X, W1, W2, GY, act: int, cols=None):
+        """Returns (dW1[:, cols] as d x ncols, dW2[cols, :] as ncols x d)."""
+        X, W1, W2, GY = map(self._f64, (X, W1, W2, GY))
+        T, d = X.shape
+        F = W1.shape[1]
+        cols = np.arange(F, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+        dW1 = np.empty((d, len(cols)))
+        dW2 = np.empty((len(cols), d))
+        self.lib.orc_mlp_cols(T, d, F, self._p(X), self._p(W1), self._p(W2), self._p(GY), act,
+                              len(cols), self._p(cols, _i64p), self._p(dW1), self._p(dW2))
+        return dW1, dW2
+
+    def mlp(self, X, W1, W2, GY, act: int):
+        """Full (Y, dX, dW1, dW2) with weights in (in, out) layout."""
+        Y, dX = self.mlp_rows(X, W1, W2, GY, act)
+        dW1, dW2 = self.mlp_cols(X, W1, W2, GY, act)
+        return Y, dX, dW1, dW2
+
+    # -- cross-entropy ---------------------------------------------------
+    def ce_tokens(self, h, W, labels, parts: int, toks=None):
+        """(loss, dlogits, dhidden, owner) for the selected tokens."""
+        h, W = self._f64(h), self._f64(W)
+        labels = np.ascontiguousarray(labels, dtype=np.int64)
+        T, d = h.shape
+        V = W.shape[1]
+        toks = np.arange(T, dtype=np.int64) if toks is None else np.ascontiguousarray(toks, dtype=np.int64)
+        n = len(toks)
+        loss = np.empty(n)
+        dlog = np.empty((n, V))
+        dh = np.empty((n, d))
+        own = np.empty(n, dtype=np.int32)
+        rc = self.lib.orc_ce_tokens(T, d, V, self._p(h), self._p(W), self._p(labels, _i64p), parts, n,
+                                    self._p(toks, _i64p), self._p(loss), self._p(dlog), self._p(dh),
+                                    self._p(own, _i32p))
+        if rc == 5:
+            raise ValueError("label")
+        if rc != 0:
+            raise ValueError("partition" if rc == 2 else "shape")
+        return loss, dlog, dh, own
+
+    def ce_sharded_one(self, z, y: int, parts: int):
+        """The pages' per-shard form for one position: (L, m_r, s_r, t_r)."""
+        z = self._f64(z)
+        m_r, s_r, t_r = np.empty(parts), np.empty(parts), np.empty(parts)
+        L = self.lib.orc_ce_sharded_one(len(z), self._p(z), int(y), parts,
+                                        self._p(m_r), self._p(s_r), self._p(t_r))
+        return float(L), m_r, s_r, t_r
+
+
+_default = None
+
+
+def get() -> Oracle:
+    """The shared oracle.  ``ORACLE_LIB`` names another build of oracle.c to
+    load instead (the mutation tests point it at deliberately broken copies)."""
+    global _default
+    if _default is None:
+        alt = os.environ.get("ORACLE_LIB")
+        _default = Oracle(load(alt) if alt else None)
+    return _default

@@ -1,0 +1,340 @@
+/*
+ * oracle.c -- plain float64 CPU oracle for the sharded GEMM forward/backward,
+ * the column-then-row tensor-parallel MLP and the vocabulary-sharded
+ * cross-entropy.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  It shares no code,
+ * header, table or helper with the CUDA library; neither side includes or
+ * links the other.
+ *
+ * Every function computes the plain, unsharded definition with triple loops
+ * in double precision, in the order the definition states, except the two
+ * functions named *_sharded*, which restate the pages' per-rank formulations
+ * so that the tests can check sharded == unsharded.  OpenMP only distributes
+ * independent output rows / columns over threads; it never splits a sum.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [SG]  "Sharded GEMM与Backprop：行、列、内维三种切分"
+ *         (interview-support-pro.com, openai-sharded-matmul-backprop)
+ *   [MC]  "多卡张量：拆开计算，再合回同一结果" (glenzli.com, distributed-execution)
+ *   [TP]  "第 6 课：张量并行 TP" (learn.payai.win, train/lesson06)
+ *
+ * Arrays are dense row-major doubles unless stated.  Labels are int64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_ERR_SHAPE 1
+#define ORC_ERR_PARTITION 2
+#define ORC_ERR_LABEL 5
+
+#define ORC_ACT_GELU_ERF 0
+#define ORC_ACT_GELU_TANH 1
+#define ORC_ACT_TANH 2
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------
+ * Shard plan.  [SG] "Python 参考实现" splits each axis with numpy's
+ * array_split; [SG] "题意与假设" allows uneven and empty shards and
+ * [SG] "手动走一遍" splits K=5 into 3/2.  array_split gives the first
+ * (dim mod parts) shards one extra element.  Written as the running sum
+ * of the shard sizes.
+ * ---------------------------------------------------------------------- */
+int orc_plan_shards(int64_t dim, int32_t parts, int64_t* off) {
+    if (parts < 1) return ORC_ERR_PARTITION;
+    if (dim < 0) return ORC_ERR_SHAPE;
+    int64_t small = dim / parts;
+    int64_t n_big = dim % parts;
+    off[0] = 0;
+    for (int32_t r = 0; r < parts; ++r) {
+        int64_t size = (r < n_big) ? small + 1 : small;
+        off[r + 1] = off[r] + size;
+    }
+    return ORC_OK;
+}
+
+/* Owner rank of index y: the r with off[r] <= y < off[r+1], by linear scan.
+ * [MC] "04 / VOCABULARY SHARDS", indicator 1[y in V_r].  -1 if none. */
+int32_t orc_owner(int64_t y, const int64_t* off, int32_t parts) {
+    for (int32_t r = 0; r < parts; ++r)
+        if (off[r] <= y && y < off[r + 1]) return r;
+    return -1;
+}
+
+/* ------------------------------------------------------------------------
+ * Unsharded GEMM forward and backward.  [SG] "题意与假设": L = <G, AB>;
+ * [SG] "解题路线" step 1: dA = G B^T, dB = A^T G.
+ * A is M x K, B is K x N, G is M x N.  Any output may be NULL.
+ * ---------------------------------------------------------------------- */
+void orc_matmul(int64_t M, int64_t K, int64_t N,
+                const double* A, const double* B, const double* G,
+                double* Y, double* dA, double* dB) {
+    if (Y) {
+        #pragma omp parallel for schedule(static)
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < N; ++n) {
+                double s = 0.0;
+                for (int64_t k = 0; k < K; ++k) s += A[m * K + k] * B[k * N + n];
+                Y[m * N + n] = s;
+            }
+    }
+    if (dA) {
+        #pragma omp parallel for schedule(static)
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t k = 0; k < K; ++k) {
+                double s = 0.0;
+                for (int64_t n = 0; n < N; ++n) s += G[m * N + n] * B[k * N + n];
+                dA[m * K + k] = s;
+            }
+    }
+    if (dB) {
+        #pragma omp parallel for schedule(static)
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t n = 0; n < N; ++n) {
+                double s = 0.0;
+                for (int64_t m = 0; m < M; ++m) s += A[m * K + k] * G[m * N + n];
+                dB[k * N + n] = s;
+            }
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * Element-wise activations and their derivatives.
+ *   GELU_ERF : x * Phi(x), Phi the standard normal CDF written with erf --
+ *              the default form of torch's gelu used by [TP] "参考答案".
+ *   GELU_TANH: the tanh approximation of GELU (Hendrycks & Gimpel 2016),
+ *              0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *   TANH     : tanh, whose derivative [MC] "02 / BACKWARD" writes as 1 - H^2.
+ * ---------------------------------------------------------------------- */
+static const double ORC_PI = 3.14159265358979323846;
+
+double orc_act(int kind, double x) {
+    if (kind == ORC_ACT_GELU_ERF) {
+        return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+    } else if (kind == ORC_ACT_GELU_TANH) {
+        double c = sqrt(2.0 / ORC_PI);
+        return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+    } else {
+        return tanh(x);
+    }
+}
+
+double orc_act_grad(int kind, double x) {
+    if (kind == ORC_ACT_GELU_ERF) {
+        /* d/dx [x Phi(x)] = Phi(x) + x phi(x), phi the normal density. */
+        double cdf = 0.5 * (1.0 + erf(x / sqrt(2.0)));
+        double pdf = exp(-0.5 * x * x) / sqrt(2.0 * ORC_PI);
+        return cdf + x * pdf;
+    } else if (kind == ORC_ACT_GELU_TANH) {
+        /* u = tanh(c (x + a x^3)); d/dx = 0.5 (1+u) + 0.5 x (1-u^2) c (1 + 3a x^2) */
+        double c = sqrt(2.0 / ORC_PI);
+        double u = tanh(c * (x + 0.044715 * x * x * x));
+        return 0.5 * (1.0 + u) + 0.5 * x * (1.0 - u * u) * c * (1.0 + 3.0 * 0.044715 * x * x);
+    } else {
+        double h = tanh(x);
+        return 1.0 - h * h;
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * Column-then-row MLP, unsharded definition.
+ * Forward  [MC] "01 / COLUMN THEN ROW"; [TP] core concept 2.A:
+ *     Hp = X W1,  Ha = phi(Hp),  Y = Ha W2.
+ * Backward [MC] "02 / BACKWARD" (upstream G_Y given, no scaling):
+ *     dHa = G_Y W2^T,  dZ = dHa * phi'(Hp),  dW2 = Ha^T G_Y,
+ *     dW1 = X^T dZ,    dX = dZ W1^T.
+ * Shapes: X T x d, W1 d x F (in,out), W2 F x d (in,out), G_Y T x d.
+ *
+ * orc_mlp_rows computes rows `rows[i]` of Y and dX (each row of Y and dX
+ * depends on one row of X and G_Y only).  Outputs are nrows x d.
+ * ---------------------------------------------------------------------- */
+void orc_mlp_rows(int64_t T, int64_t d, int64_t F,
+                  const double* X, const double* W1, const double* W2, const double* GY,
+                  int act, int64_t nrows, const int64_t* rows,
+                  double* Y, double* dX) {
+    (void)T;
+    #pragma omp parallel
+    {
+        double* hp = (double*)malloc(sizeof(double) * (size_t)(F > 0 ? F : 1));
+        double* dz = (double*)malloc(sizeof(double) * (size_t)(F > 0 ? F : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nrows; ++i) {
+            int64_t t = rows[i];
+            /* Hp[t,:] = X[t,:] W1 */
+            for (int64_t f = 0; f < F; ++f) hp[f] = 0.0;
+            for (int64_t c = 0; c < d; ++c) {
+                double x = X[t * d + c];
+                for (int64_t f = 0; f < F; ++f) hp[f] += x * W1[c * F + f];
+            }
+            /* Y[t,:] = phi(Hp[t,:]) W2 */
+            if (Y) {
+                for (int64_t c = 0; c < d; ++c) Y[i * d + c] = 0.0;
+                for (int64_t f = 0; f < F; ++f) {
+                    double ha = orc_act(act, hp[f]);
+                    for (int64_t c = 0; c < d; ++c) Y[i * d + c] += ha * W2[f * d + c];
+                }
+            }
+            if (dX) {
+                /* dZ[t,f] = (G_Y[t,:] . W2[f,:]) * phi'(Hp[t,f]) */
+                for (int64_t f = 0; f < F; ++f) {
+                    double s = 0.0;
+                    for (int64_t c = 0; c < d; ++c) s += GY[t * d + c] * W2[f * d + c];
+                    dz[f] = s * orc_act_grad(act, hp[f]);
+                }
+                /* dX[t,:] = dZ[t,:] W1^T */
+                for (int64_t c = 0; c < d; ++c) {
+                    double s = 0.0;
+                    for (int64_t f = 0; f < F; ++f) s += dz[f] * W1[c * F + f];
+                    dX[i * d + c] = s;
+                }
+            }
+        }
+        free(hp);
+        free(dz);
+    }
+}
+
+/* orc_mlp_cols computes, for each selected hidden unit f = cols[j], column f
+ * of dW1 (written to dW1[:, j], a d x ncols array) and row f of dW2 (written
+ * to dW2[j, :], an ncols x d array).  Each needs column f of Hp over all T. */
+void orc_mlp_cols(int64_t T, int64_t d, int64_t F,
+                  const double* X, const double* W1, const double* W2, const double* GY,
+                  int act, int64_t ncols, const int64_t* cols,
+                  double* dW1, double* dW2) {
+    #pragma omp parallel
+    {
+        double* ha = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        double* dz = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t j = 0; j < ncols; ++j) {
+            int64_t f = cols[j];
+            for (int64_t t = 0; t < T; ++t) {
+                double hp = 0.0;
+                for (int64_t c = 0; c < d; ++c) hp += X[t * d + c] * W1[c * F + f];
+                double dha = 0.0;
+                for (int64_t c = 0; c < d; ++c) dha += GY[t * d + c] * W2[f * d + c];
+                ha[t] = orc_act(act, hp);
+                dz[t] = dha * orc_act_grad(act, hp);
+            }
+            if (dW1)
+                for (int64_t c = 0; c < d; ++c) {
+                    double s = 0.0;
+                    for (int64_t t = 0; t < T; ++t) s += X[t * d + c] * dz[t];
+                    dW1[c * ncols + j] = s;
+                }
+            if (dW2)
+                for (int64_t c = 0; c < d; ++c) {
+                    double s = 0.0;
+                    for (int64_t t = 0; t < T; ++t) s += ha[t] * GY[t * d + c];
+                    dW2[j * d + c] = s;
+                }
+        }
+        free(ha);
+        free(dz);
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * Vocabulary cross-entropy, unsharded definition, for selected tokens.
+ * [MC] "04 / VOCABULARY SHARDS" (single supervised position, no label
+ * smoothing): per token, z = h W,  m = max_j z_j,  s = sum_j e^{z_j - m},
+ * L = log s + m - z_y,  dL/dz_j = e^{z_j - m}/s - 1[j = y];  the gradient
+ * of the shared hidden is dh = dz W^T (summed over all vocabulary shards,
+ * with no division by the shard count).
+ * h is T x d, W is d x V (in,out), labels int64 in [0, V).
+ * Outputs per selected token i: loss[i], dlogits[i, :] (V), dhidden[i, :]
+ * (d), owner[i] (shard of the label under the plan for `parts`).
+ * Returns ORC_ERR_LABEL if a selected label is outside [0, V).
+ * ---------------------------------------------------------------------- */
+int orc_ce_tokens(int64_t T, int64_t d, int64_t V,
+                  const double* h, const double* W, const int64_t* labels, int32_t parts,
+                  int64_t ntok, const int64_t* toks,
+                  double* loss, double* dlogits, double* dhidden, int32_t* owner) {
+    (void)T;
+    int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(parts + 1));
+    int rc = orc_plan_shards(V, parts, off);
+    if (rc != ORC_OK) { free(off); return rc; }
+    for (int64_t i = 0; i < ntok; ++i)
+        if (labels[toks[i]] < 0 || labels[toks[i]] >= V) { free(off); return ORC_ERR_LABEL; }
+    #pragma omp parallel
+    {
+        double* z = (double*)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+        double* dz = (double*)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < ntok; ++i) {
+            int64_t t = toks[i];
+            int64_t y = labels[t];
+            for (int64_t v = 0; v < V; ++v) z[v] = 0.0;
+            for (int64_t c = 0; c < d; ++c) {
+                double hv = h[t * d + c];
+                for (int64_t v = 0; v < V; ++v) z[v] += hv * W[c * V + v];
+            }
+            double m = -INFINITY;
+            for (int64_t v = 0; v < V; ++v) if (z[v] > m) m = z[v];
+            double s = 0.0;
+            for (int64_t v = 0; v < V; ++v) s += exp(z[v] - m);
+            if (loss) loss[i] = log(s) + m - z[y];
+            for (int64_t v = 0; v < V; ++v) dz[v] = exp(z[v] - m) / s - (v == y ? 1.0 : 0.0);
+            if (dlogits) memcpy(dlogits + i * V, dz, sizeof(double) * (size_t)V);
+            if (dhidden)
+                for (int64_t c = 0; c < d; ++c) {
+                    double acc = 0.0;
+                    for (int64_t v = 0; v < V; ++v) acc += dz[v] * W[c * V + v];
+                    dhidden[i * d + c] = acc;
+                }
+            if (owner) owner[i] = orc_owner(y, off, parts);
+        }
+        free(z);
+        free(dz);
+    }
+    free(off);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * The pages' sharded formulation of one position's cross-entropy, kept
+ * literal so that tests can check it equals the unsharded one.
+ * [MC] "04 / VOCABULARY SHARDS":
+ *   m_r = max_{j in V_r} z_j,  m = max_r m_r,
+ *   s_r = sum_{j in V_r} e^{z_j - m},  s = sum_r s_r,
+ *   t_r = 1[y in V_r] (z_y - m),  L = log s - sum_r t_r.
+ * An empty shard has m_r = -inf, s_r = 0, t_r = 0.  Outputs m_r, s_r, t_r
+ * (each `parts` long) and returns L.
+ * ---------------------------------------------------------------------- */
+double orc_ce_sharded_one(int64_t V, const double* z, int64_t y, int32_t parts,
+                          double* m_r, double* s_r, double* t_r) {
+    int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(parts + 1));
+    orc_plan_shards(V, parts, off);
+    double m = -INFINITY;
+    for (int32_t r = 0; r < parts; ++r) {
+        double mr = -INFINITY;
+        for (int64_t j = off[r]; j < off[r + 1]; ++j) if (z[j] > mr) mr = z[j];
+        m_r[r] = mr;
+        if (mr > m) m = mr;
+    }
+    double s = 0.0, tsum = 0.0;
+    for (int32_t r = 0; r < parts; ++r) {
+        double sr = 0.0;
+        for (int64_t j = off[r]; j < off[r + 1]; ++j) sr += exp(z[j] - m);
+        s_r[r] = sr;
+        s += sr;
+        t_r[r] = (off[r] <= y && y < off[r + 1]) ? (z[y] - m) : 0.0;
+        tsum += t_r[r];
+    }
+    free(off);
+    return log(s) - tsum;
+}
