@@ -1,0 +1,612 @@
+// api.cu -- the C ABI of include/tps.h: validation, shard planning, launch
+// orchestration, the device error word and the launch profiler.
+//
+// Nothing here allocates device memory: operands, results and workspace all
+// belong to the caller.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.cuh"
+#include "tps.h"
+
+namespace tps {
+
+// ------------------------------------------------------------ error detail
+static thread_local std::string t_detail;
+
+static int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_detail = buf;
+  return code;
+}
+
+// ------------------------------------------------------------ device error word
+// One word per device; kernels OR TPS_DEVERR_* bits into it.
+__device__ uint32_t g_dev_err_word;
+
+static std::mutex g_err_mu;
+static std::vector<uint32_t*> g_err_addr;  // indexed by device ordinal
+
+static uint32_t* dev_err_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (static_cast<int>(g_err_addr.size()) <= dev) g_err_addr.resize(dev + 1, nullptr);
+  if (g_err_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_err_word) != cudaSuccess) return nullptr;
+    g_err_addr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_err_addr[dev];
+}
+
+// ------------------------------------------------------------ profiler
+struct ProfRecord {
+  std::string name;  // "kind:label"
+  double flops, bytes;
+  cudaEvent_t start, stop;
+};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<ProfRecord> g_prof;
+static std::vector<cudaEvent_t> g_event_pool;
+static int64_t g_launches = 0;
+static std::vector<std::string> g_summary_names;  // storage for tps_profile_summary
+
+static cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+ProfScope::ProfScope(const char* kind, const char* label, double flops, double bytes, cudaStream_t s)
+    : slot(-1), stream(s) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return;
+  ProfRecord r{std::string(kind) + ":" + label, flops, bytes, take_event(), take_event()};
+  cudaEventRecord(r.start, s);
+  g_prof.push_back(r);
+  slot = static_cast<int>(g_prof.size()) - 1;
+}
+ProfScope::~ProfScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (slot < static_cast<int>(g_prof.size())) cudaEventRecord(g_prof[slot].stop, stream);
+}
+void note_launch() {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  ++g_launches;
+}
+
+// ------------------------------------------------------------ tensor views
+struct Mat {  // 2-D strided view
+  void* data = nullptr;
+  int dtype = 0;
+  int64_t rows = 0, cols = 0, sr = 0, sc = 0;
+};
+
+static const char* dtname(int d) {
+  switch (d) {
+    case TPS_F32: return "f32";
+    case TPS_BF16: return "bf16";
+    case TPS_I32: return "i32";
+    case TPS_I64: return "i64";
+    default: return "?";
+  }
+}
+
+// View `t` as a matrix.  flatten: leading dims (all but the last) are
+// merged into rows, which requires them to be mutually contiguous.
+// The view must have unit stride in one dimension (either one when a
+// dimension has extent <= 1).
+static int as_mat(const tps_tensor* t, const char* name, bool flatten, Mat* m) {
+  if (t == nullptr || t->data == nullptr) return fail(TPS_ERR_ARG, "%s: missing tensor", name);
+  if (t->ndim < 1 || t->ndim > 4) return fail(TPS_ERR_SHAPE, "%s: ndim %d", name, t->ndim);
+  for (int i = 0; i < t->ndim; ++i)
+    if (t->shape[i] < 0) return fail(TPS_ERR_SHAPE, "%s: negative extent", name);
+  if (!flatten && t->ndim != 2) return fail(TPS_ERR_SHAPE, "%s: expected a 2-D tensor, got %d-D", name, t->ndim);
+  if (flatten && t->ndim < 2) return fail(TPS_ERR_SHAPE, "%s: expected (..., n), got 1-D", name);
+  m->data = t->data;
+  m->dtype = t->dtype;
+  const int last = t->ndim - 1;
+  m->cols = t->shape[last];
+  m->sc = t->stride[last];
+  int64_t rows = 1;
+  for (int i = 0; i < last; ++i) rows *= t->shape[i];
+  m->rows = rows;
+  // row stride: the stride of the innermost leading dim; the others must nest
+  m->sr = t->stride[last - 1];
+  for (int i = 0; i < last - 1; ++i) {
+    if (t->shape[i] > 1 && t->stride[i] != t->stride[i + 1] * t->shape[i + 1])
+      return fail(TPS_ERR_LAYOUT, "%s: leading dimensions are not contiguous", name);
+  }
+  if (m->rows <= 1) m->sr = (m->sc == 1) ? (m->cols > 0 ? m->cols : 1) : 1;
+  if (m->cols <= 1) m->sc = (m->sr == 1) ? (m->rows > 0 ? m->rows : 1) : 1;
+  if (m->rows <= 1 && m->cols <= 1) {
+    m->sr = 1;
+    m->sc = 1;
+  }
+  if (m->sr != 1 && m->sc != 1) return fail(TPS_ERR_LAYOUT, "%s: no unit stride (strides %lld, %lld)", name,
+                                            (long long)m->sr, (long long)m->sc);
+  return TPS_OK;
+}
+
+static int expect(const Mat& m, const char* name, int64_t rows, int64_t cols) {
+  if (m.rows != rows || m.cols != cols)
+    return fail(TPS_ERR_SHAPE, "%s: shape (%lld, %lld), expected (%lld, %lld)", name, (long long)m.rows,
+                (long long)m.cols, (long long)rows, (long long)cols);
+  return TPS_OK;
+}
+
+// ------------------------------------------------------------ fill kernel
+__global__ void fill_kernel(void* base, int dtype, int64_t rows, int64_t cols, int64_t sr, int64_t sc, float v) {
+  const int64_t n = rows * cols;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / cols, c = i % cols;
+    if (dtype == TPS_F32)
+      static_cast<float*>(base)[r * sr + c * sc] = v;
+    else
+      static_cast<__nv_bfloat16*>(base)[r * sr + c * sc] = __float2bfloat16_rn(v);
+  }
+}
+
+static int launch_fill(void* base, int dtype, int64_t rows, int64_t cols, int64_t sr, int64_t sc,
+                       cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0 || base == nullptr) return TPS_OK;
+  const int64_t n = rows * cols;
+  const int blocks = static_cast<int>(n / 256 + 1 < 4096 ? n / 256 + 1 : 4096);
+  ProfScope prof("fill", "zero", 0.0, double(n) * (dtype == TPS_F32 ? 4 : 2), stream);
+  fill_kernel<<<blocks, 256, 0, stream>>>(base, dtype, rows, cols, sr, sc, 0.0f);
+  note_launch();
+  return cudaPeekAtLastError() == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ GEMM dispatch
+// Output orientation: the kernels write row-major D.  A column-major output
+// (unit stride along M) is produced as D^T = B^T A^T with the roles of the
+// operands swapped.  Epilogues other than a plain store only ever target the
+// library's own row-major workspace.
+static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream) {
+  if (g.M == 0 || g.N == 0) return TPS_OK;
+  uint32_t* err = dev_err_ptr();
+  if (err == nullptr) return fail(TPS_ERR_CUDA, "cannot resolve the device error word");
+  if (g.K == 0) {
+    // An empty contraction is the zero matrix; phi(0) = 0 and 0 * phi' = 0
+    // for every supported activation.
+    int rc = launch_fill(g.epi.d, g.epi.mode == EPI_ACT_FWD ? TPS_F32 : g.epi.d_dtype, g.M, g.N, d_sm, d_sn,
+                         stream);
+    if (rc == TPS_OK && g.epi.mode == EPI_ACT_FWD)
+      rc = launch_fill(g.epi.d2, g.epi.d2_dtype, g.M, g.N, g.epi.ldd2, 1, stream);
+    return rc;
+  }
+  if (d_sn != 1) {
+    if (d_sm != 1 || g.epi.mode != EPI_STORE) return fail(TPS_ERR_LAYOUT, "%s: unsupported output layout", g.name);
+    GemmDesc t = g;
+    t.M = g.N;
+    t.N = g.M;
+    t.a = g.b;
+    t.a_sm = g.b_sn;
+    t.a_sk = g.b_sk;
+    t.b = g.a;
+    t.b_sk = g.a_sk;
+    t.b_sn = g.a_sm;
+    t.epi.ldd = d_sn;
+    g = t;
+  } else {
+    g.epi.ldd = d_sm;
+  }
+  const int rc = gemm_tc_supported(g) ? launch_gemm_tc(g, err, stream) : launch_gemm_simt(g, err, stream);
+  if (rc == TPS_ERR_CUDA) return fail(rc, "%s: launch failed: %s", g.name, cudaGetErrorString(cudaGetLastError()));
+  return rc;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace tps
+
+using namespace tps;
+
+// ====================================================================== ABI
+
+extern "C" int tps_plan_shards(int64_t dim, int32_t parts, int64_t* offsets) {
+  if (offsets == nullptr) return fail(TPS_ERR_ARG, "offsets is NULL");
+  if (parts < 1) return fail(TPS_ERR_PARTITION, "parts must be >= 1 (got %d)", parts);
+  if (dim < 0) return fail(TPS_ERR_SHAPE, "dim must be >= 0");
+  for (int32_t i = 0; i <= parts; ++i) offsets[i] = shard_offset(dim, parts, i);
+  return TPS_OK;
+}
+
+extern "C" int tps_matmul_fwd_bwd(const tps_tensor* A, const tps_tensor* B, const tps_tensor* G, int32_t parts,
+                                  int32_t axis, const tps_tensor* Y, const tps_tensor* dA, const tps_tensor* dB,
+                                  void* cuda_stream) {
+  t_detail.clear();
+  Mat a, b, g;
+  int rc;
+  if ((rc = as_mat(A, "A", false, &a)) || (rc = as_mat(B, "B", false, &b)) || (rc = as_mat(G, "G", false, &g)))
+    return rc;
+  const int64_t M = a.rows, K = a.cols, N = b.cols;
+  if (b.rows != K) return fail(TPS_ERR_SHAPE, "A is %lld x %lld but B has %lld rows", (long long)M, (long long)K,
+                               (long long)b.rows);
+  if ((rc = expect(g, "G", M, N))) return rc;
+  if (parts < 1) return fail(TPS_ERR_PARTITION, "parts must be >= 1 (got %d)", parts);
+  if (axis != TPS_AXIS_ROWS && axis != TPS_AXIS_COLUMNS && axis != TPS_AXIS_INNER)
+    return fail(TPS_ERR_PARTITION, "unknown axis %d", axis);
+  if ((a.dtype != TPS_F32 && a.dtype != TPS_BF16) || b.dtype != a.dtype || g.dtype != a.dtype)
+    return fail(TPS_ERR_DTYPE, "A, B, G must all be f32 or all bf16 (got %s, %s, %s)", dtname(a.dtype),
+                dtname(b.dtype), dtname(g.dtype));
+  Mat y, da, db;
+  const bool want_y = Y != nullptr, want_da = dA != nullptr, want_db = dB != nullptr;
+  if (want_y && ((rc = as_mat(Y, "Y", false, &y)) || (rc = expect(y, "Y", M, N)))) return rc;
+  if (want_da && ((rc = as_mat(dA, "dA", false, &da)) || (rc = expect(da, "dA", M, K)))) return rc;
+  if (want_db && ((rc = as_mat(dB, "dB", false, &db)) || (rc = expect(db, "dB", K, N)))) return rc;
+  for (const Mat* o : {want_y ? &y : nullptr, want_da ? &da : nullptr, want_db ? &db : nullptr})
+    if (o && o->dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "outputs must be f32");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+  if (want_y) {  // Y = A B; summed over ranks for the inner split
+    GemmDesc d;
+    d.name = "gemm_Y";
+    d.M = M; d.N = N; d.K = K; d.in_dtype = a.dtype;
+    d.a = a.data; d.a_sm = a.sr; d.a_sk = a.sc;
+    d.b = b.data; d.b_sk = b.sr; d.b_sn = b.sc;
+    d.epi.d = y.data; d.epi.d_dtype = TPS_F32;
+    d.kparts = (axis == TPS_AXIS_INNER) ? parts : 1;
+    if ((rc = run_gemm(d, y.sr, y.sc, s))) return rc;
+  }
+  if (want_da) {  // dA = G B^T; summed over ranks for the column split
+    GemmDesc d;
+    d.name = "gemm_dA";
+    d.M = M; d.N = K; d.K = N; d.in_dtype = a.dtype;
+    d.a = g.data; d.a_sm = g.sr; d.a_sk = g.sc;
+    d.b = b.data; d.b_sk = b.sc; d.b_sn = b.sr;
+    d.epi.d = da.data; d.epi.d_dtype = TPS_F32;
+    d.kparts = (axis == TPS_AXIS_COLUMNS) ? parts : 1;
+    if ((rc = run_gemm(d, da.sr, da.sc, s))) return rc;
+  }
+  if (want_db) {  // dB = A^T G; summed over ranks for the row split
+    GemmDesc d;
+    d.name = "gemm_dB";
+    d.M = K; d.N = N; d.K = M; d.in_dtype = a.dtype;
+    d.a = a.data; d.a_sm = a.sc; d.a_sk = a.sr;
+    d.b = g.data; d.b_sk = g.sr; d.b_sn = g.sc;
+    d.epi.d = db.data; d.epi.d_dtype = TPS_F32;
+    d.kparts = (axis == TPS_AXIS_ROWS) ? parts : 1;
+    if ((rc = run_gemm(d, db.sr, db.sc, s))) return rc;
+  }
+  return TPS_OK;
+}
+
+extern "C" size_t tps_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int32_t dtype) {
+  (void)d;
+  (void)tp;
+  if (T < 0 || F < 0) return 0;
+  const size_t e = (dtype == TPS_F32) ? 4 : 2;
+  const size_t n = static_cast<size_t>(T) * static_cast<size_t>(F);
+  return align256(n * 4) + align256(n * e) + align256(n * e);
+}
+
+// A weight's logical (in, out) strides for either layout.
+static void weight_strides(const Mat& w, int layout, int64_t* s_in, int64_t* s_out) {
+  if (layout == TPS_W_IN_OUT) {
+    *s_in = w.sr;
+    *s_out = w.sc;
+  } else {
+    *s_in = w.sc;
+    *s_out = w.sr;
+  }
+}
+
+extern "C" int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const tps_tensor* W2,
+                               const tps_tensor* GY, int32_t tp, int32_t act, int32_t weight_layout,
+                               const tps_tensor* Y, const tps_tensor* dX, const tps_tensor* dW1,
+                               const tps_tensor* dW2, void* workspace, size_t workspace_bytes,
+                               void* cuda_stream) {
+  t_detail.clear();
+  Mat x, w1, w2, gy, y, dx, dw1, dw2;
+  int rc;
+  if ((rc = as_mat(X, "X", true, &x)) || (rc = as_mat(W1, "W1", false, &w1)) || (rc = as_mat(W2, "W2", false, &w2)) ||
+      (rc = as_mat(GY, "GY", true, &gy)))
+    return rc;
+  if (weight_layout != TPS_W_IN_OUT && weight_layout != TPS_W_OUT_IN)
+    return fail(TPS_ERR_ARG, "unknown weight layout %d", weight_layout);
+  const bool io = weight_layout == TPS_W_IN_OUT;
+  const int64_t T = x.rows, d = x.cols;
+  const int64_t F = io ? w1.cols : w1.rows;
+  if ((io ? w1.rows : w1.cols) != d) return fail(TPS_ERR_SHAPE, "W1 does not match X's width %lld", (long long)d);
+  if ((rc = expect(w2, "W2", io ? F : d, io ? d : F))) return rc;
+  if ((rc = expect(gy, "GY", T, d))) return rc;
+  if (tp < 1) return fail(TPS_ERR_PARTITION, "tp must be >= 1 (got %d)", tp);
+  if (act != TPS_ACT_GELU_ERF && act != TPS_ACT_GELU_TANH && act != TPS_ACT_TANH)
+    return fail(TPS_ERR_ARG, "unknown activation %d", act);
+  const int dt = x.dtype;
+  if ((dt != TPS_F32 && dt != TPS_BF16) || w1.dtype != dt || w2.dtype != dt || gy.dtype != dt)
+    return fail(TPS_ERR_DTYPE, "X, W1, W2, GY must all be f32 or all bf16");
+  if ((rc = as_mat(Y, "Y", true, &y)) || (rc = expect(y, "Y", T, d)) || (rc = as_mat(dX, "dX", true, &dx)) ||
+      (rc = expect(dx, "dX", T, d)) || (rc = as_mat(dW1, "dW1", false, &dw1)) ||
+      (rc = expect(dw1, "dW1", w1.rows, w1.cols)) || (rc = as_mat(dW2, "dW2", false, &dw2)) ||
+      (rc = expect(dw2, "dW2", w2.rows, w2.cols)))
+    return rc;
+  for (const Mat* o : {&y, &dx, &dw1, &dw2})
+    if (o->dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "MLP results must be f32");
+  const size_t need = tps_mlp_workspace_bytes(T, d, F, tp, dt);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255)))
+    return fail(TPS_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+  const size_t n = static_cast<size_t>(T) * static_cast<size_t>(F);
+  const size_t e = (dt == TPS_F32) ? 4 : 2;
+  char* ws = static_cast<char*>(workspace);
+  float* Hp = reinterpret_cast<float*>(ws);                 // T x F fp32 pre-activation
+  void* Ha = ws + align256(n * 4);                          // T x F activation (operand dtype)
+  void* dZ = ws + align256(n * 4) + align256(n * e);        // T x F dZ (operand dtype)
+
+  int64_t w1_in, w1_out, w2_in, w2_out, dw1_in, dw1_out, dw2_in, dw2_out;
+  weight_strides(w1, weight_layout, &w1_in, &w1_out);      // W1(dd, f)
+  weight_strides(w2, weight_layout, &w2_in, &w2_out);      // W2(f, dd)
+  weight_strides(dw1, weight_layout, &dw1_in, &dw1_out);
+  weight_strides(dw2, weight_layout, &dw2_in, &dw2_out);
+
+  {  // Hp = X W1, Ha = phi(Hp): column-parallel, each rank's columns a range of Hp
+    GemmDesc g;
+    g.name = "mlp_fc1_act";
+    g.M = T; g.N = F; g.K = d; g.in_dtype = dt;
+    g.a = x.data; g.a_sm = x.sr; g.a_sk = x.sc;
+    g.b = w1.data; g.b_sk = w1_in; g.b_sn = w1_out;
+    g.epi.mode = EPI_ACT_FWD; g.epi.act = act;
+    g.epi.d = Hp; g.epi.d_dtype = TPS_F32;
+    g.epi.d2 = Ha; g.epi.ldd2 = F; g.epi.d2_dtype = dt;
+    if ((rc = run_gemm(g, F, 1, s))) return rc;
+  }
+  {  // Y = sum_r Ha_r W2_r: row-parallel, rank sum in the K loop
+    GemmDesc g;
+    g.name = "mlp_fc2";
+    g.M = T; g.N = d; g.K = F; g.in_dtype = dt;
+    g.a = Ha; g.a_sm = F; g.a_sk = 1;
+    g.b = w2.data; g.b_sk = w2_in; g.b_sn = w2_out;
+    g.epi.d = y.data; g.epi.d_dtype = TPS_F32;
+    g.kparts = tp;
+    if ((rc = run_gemm(g, y.sr, y.sc, s))) return rc;
+  }
+  {  // dZ = (GY W2^T) * phi'(Hp), per rank on its own columns
+    GemmDesc g;
+    g.name = "mlp_dh_act";
+    g.M = T; g.N = F; g.K = d; g.in_dtype = dt;
+    g.a = gy.data; g.a_sm = gy.sr; g.a_sk = gy.sc;
+    g.b = w2.data; g.b_sk = w2_out; g.b_sn = w2_in;
+    g.epi.mode = EPI_ACT_BWD; g.epi.act = act;
+    g.epi.d = dZ; g.epi.d_dtype = dt;
+    g.epi.aux = Hp; g.epi.ld_aux = F;
+    if ((rc = run_gemm(g, F, 1, s))) return rc;
+  }
+  {  // dW2(f, dd) = sum_t Ha[t, f] GY[t, dd]
+    GemmDesc g;
+    g.name = "mlp_dW2";
+    g.M = F; g.N = d; g.K = T; g.in_dtype = dt;
+    g.a = Ha; g.a_sm = 1; g.a_sk = F;
+    g.b = gy.data; g.b_sk = gy.sr; g.b_sn = gy.sc;
+    g.epi.d = dw2.data; g.epi.d_dtype = TPS_F32;
+    if ((rc = run_gemm(g, dw2_in, dw2_out, s))) return rc;
+  }
+  {  // dW1(dd, f) = sum_t X[t, dd] dZ[t, f]
+    GemmDesc g;
+    g.name = "mlp_dW1";
+    g.M = d; g.N = F; g.K = T; g.in_dtype = dt;
+    g.a = x.data; g.a_sm = x.sc; g.a_sk = x.sr;
+    g.b = dZ; g.b_sk = F; g.b_sn = 1;
+    g.epi.d = dw1.data; g.epi.d_dtype = TPS_F32;
+    if ((rc = run_gemm(g, dw1_in, dw1_out, s))) return rc;
+  }
+  {  // dX = sum_r dZ_r W1_r^T: rank sum in the K loop
+    GemmDesc g;
+    g.name = "mlp_dX";
+    g.M = T; g.N = d; g.K = F; g.in_dtype = dt;
+    g.a = dZ; g.a_sm = F; g.a_sk = 1;
+    g.b = w1.data; g.b_sk = w1_out; g.b_sn = w1_in;
+    g.epi.d = dx.data; g.epi.d_dtype = TPS_F32;
+    g.kparts = tp;
+    if ((rc = run_gemm(g, dx.sr, dx.sc, s))) return rc;
+  }
+  return TPS_OK;
+}
+
+extern "C" size_t tps_ce_workspace_bytes(int64_t T, int64_t V, int32_t tp) {
+  if (T < 0 || V < 0 || tp < 1) return 0;
+  const size_t t = static_cast<size_t>(T);
+  return align256(t * static_cast<size_t>(V) * 4) + align256(t * static_cast<size_t>(tp) * 2 * 4) + align256(t * 4);
+}
+
+extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead, const tps_tensor* labels,
+                                    int32_t tp, int32_t weight_layout, const tps_tensor* loss,
+                                    const tps_tensor* dlogits, const tps_tensor* dHidden, const tps_tensor* owner,
+                                    void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  t_detail.clear();
+  Mat hm, w, dl, dh;
+  int rc;
+  if ((rc = as_mat(h, "h", true, &hm)) || (rc = as_mat(Whead, "Whead", false, &w))) return rc;
+  if (weight_layout != TPS_W_IN_OUT && weight_layout != TPS_W_OUT_IN)
+    return fail(TPS_ERR_ARG, "unknown weight layout %d", weight_layout);
+  const bool io = weight_layout == TPS_W_IN_OUT;
+  const int64_t T = hm.rows, d = hm.cols;
+  const int64_t V = io ? w.cols : w.rows;
+  if ((io ? w.rows : w.cols) != d) return fail(TPS_ERR_SHAPE, "Whead does not match h's width %lld", (long long)d);
+  if (tp < 1) return fail(TPS_ERR_PARTITION, "tp must be >= 1 (got %d)", tp);
+  if (V < 1) return fail(TPS_ERR_SHAPE, "empty vocabulary");
+  const int dt = hm.dtype;
+  if ((dt != TPS_F32 && dt != TPS_BF16) || w.dtype != dt) return fail(TPS_ERR_DTYPE, "h and Whead must share f32 or bf16");
+  if (labels == nullptr || labels->data == nullptr) return fail(TPS_ERR_ARG, "labels missing");
+  if (labels->ndim < 1 || (labels->dtype != TPS_I64 && labels->dtype != TPS_I32))
+    return fail(TPS_ERR_DTYPE, "labels must be i32 or i64");
+  int64_t nl = 1;
+  for (int i = 0; i < labels->ndim; ++i) nl *= labels->shape[i];
+  if (nl != T) return fail(TPS_ERR_SHAPE, "labels hold %lld entries for %lld tokens", (long long)nl, (long long)T);
+  if (labels->stride[labels->ndim - 1] != 1 && T > 1) return fail(TPS_ERR_LAYOUT, "labels must be contiguous");
+  if (loss == nullptr || loss->data == nullptr || loss->dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "loss must be f32");
+  int64_t nloss = 1;
+  for (int i = 0; i < loss->ndim; ++i) nloss *= loss->shape[i];
+  if (nloss != T || (loss->stride[loss->ndim - 1] != 1 && T > 1)) return fail(TPS_ERR_SHAPE, "loss must be T contiguous floats");
+  if ((rc = as_mat(dlogits, "dlogits", true, &dl)) || (rc = expect(dl, "dlogits", T, V))) return rc;
+  if (dl.dtype != dt) return fail(TPS_ERR_DTYPE, "dlogits must have the operand dtype (%s)", dtname(dt));
+  if (dl.sc != 1 && V > 1) return fail(TPS_ERR_LAYOUT, "dlogits rows must be contiguous");
+  if ((rc = as_mat(dHidden, "dHidden", true, &dh)) || (rc = expect(dh, "dHidden", T, d))) return rc;
+  if (dh.dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "dHidden must be f32");
+  int32_t* own = nullptr;
+  if (owner != nullptr && owner->data != nullptr) {
+    int64_t no = 1;
+    for (int i = 0; i < owner->ndim; ++i) no *= owner->shape[i];
+    if (owner->dtype != TPS_I32 || no != T || (owner->stride[owner->ndim - 1] != 1 && T > 1))
+      return fail(TPS_ERR_SHAPE, "owner must be T contiguous i32");
+    own = static_cast<int32_t*>(owner->data);
+  }
+  const size_t need = tps_ce_workspace_bytes(T, V, tp);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return fail(TPS_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  if (T == 0) return TPS_OK;
+
+  char* ws = static_cast<char*>(workspace);
+  float* z = reinterpret_cast<float*>(ws);
+  float* stats = reinterpret_cast<float*>(ws + align256(size_t(T) * size_t(V) * 4));
+  float* zy = reinterpret_cast<float*>(ws + align256(size_t(T) * size_t(V) * 4) + align256(size_t(T) * tp * 2 * 4));
+  int64_t w_in, w_out;
+  weight_strides(w, weight_layout, &w_in, &w_out);  // W(dd, v)
+
+  {  // z = h Whead: vocabulary shards are column ranges of z
+    GemmDesc g;
+    g.name = "ce_logits";
+    g.M = T; g.N = V; g.K = d; g.in_dtype = dt;
+    g.a = hm.data; g.a_sm = hm.sr; g.a_sk = hm.sc;
+    g.b = w.data; g.b_sk = w_in; g.b_sn = w_out;
+    g.epi.d = z; g.epi.d_dtype = TPS_F32;
+    if ((rc = run_gemm(g, V, 1, s))) return rc;
+  }
+  {
+    CeDesc c;
+    c.T = T; c.V = V; c.parts = tp;
+    c.logits = z; c.ldz = V;
+    c.labels = labels->data; c.label_dtype = labels->dtype;
+    c.loss = static_cast<float*>(loss->data);
+    c.dlogits = dl.data; c.ldg = dl.sr; c.dlogits_dtype = dt;
+    c.owner = own; c.stats = stats; c.zy = zy;
+    uint32_t* err = dev_err_ptr();
+    if (err == nullptr) return fail(TPS_ERR_CUDA, "cannot resolve the device error word");
+    rc = launch_ce(c, err, s, nullptr);
+    if (rc) return fail(rc, "ce launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  }
+  {  // dHidden = sum_r dlogits_r Whead_r^T: rank sum in the K loop
+    GemmDesc g;
+    g.name = "ce_dhidden";
+    g.M = T; g.N = d; g.K = V; g.in_dtype = dt;
+    g.a = dl.data; g.a_sm = dl.sr; g.a_sk = 1;
+    g.b = w.data; g.b_sk = w_out; g.b_sn = w_in;
+    g.epi.d = dh.data; g.epi.d_dtype = TPS_F32;
+    g.kparts = tp;
+    if ((rc = run_gemm(g, dh.sr, dh.sc, s))) return rc;
+  }
+  return TPS_OK;
+}
+
+extern "C" int tps_last_device_error(void* cuda_stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return fail(TPS_ERR_CUDA, "stream synchronize failed: %s", cudaGetErrorString(cudaGetLastError()));
+  uint32_t* p = dev_err_ptr();
+  if (p == nullptr) return TPS_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_dev_err_word, sizeof(v)) != cudaSuccess) return TPS_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbol(g_dev_err_word, &zero, sizeof(zero)) != cudaSuccess) return TPS_ERR_CUDA;
+  if (v & TPS_DEVERR_TIMEOUT) return TPS_ERR_TIMEOUT;
+  if (v & TPS_DEVERR_LABEL) return TPS_ERR_LABEL;
+  return TPS_OK;
+}
+
+extern "C" const char* tps_strerror(int code) {
+  switch (code) {
+    case TPS_OK: return "ok";
+    case TPS_ERR_SHAPE: return "shape";
+    case TPS_ERR_PARTITION: return "partition";
+    case TPS_ERR_DTYPE: return "dtype";
+    case TPS_ERR_LAYOUT: return "layout";
+    case TPS_ERR_LABEL: return "label out of range";
+    case TPS_ERR_WORKSPACE: return "workspace";
+    case TPS_ERR_CUDA: return "cuda";
+    case TPS_ERR_TIMEOUT: return "device wait timed out";
+    case TPS_ERR_ARG: return "argument";
+    default: return "unknown";
+  }
+}
+
+extern "C" const char* tps_last_error_detail(void) { return t_detail.c_str(); }
+
+extern "C" int tps_profile_reset(int enable) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof) {
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_prof.clear();
+  g_prof_on = enable != 0;
+  g_launches = 0;
+  return TPS_OK;
+}
+
+extern "C" int tps_profile_stop(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = false;
+  return TPS_OK;
+}
+
+extern "C" int tps_profile_summary(int cap, const char** names, int64_t* launches, double* total_ms, double* flops,
+                                   double* bytes) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  std::vector<std::string> fam;
+  std::vector<int64_t> cnt;
+  std::vector<double> ms, fl, by;
+  for (auto& r : g_prof) {
+    if (cudaEventSynchronize(r.stop) != cudaSuccess) return -TPS_ERR_CUDA;
+    float t = 0.0f;
+    if (cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess) return -TPS_ERR_CUDA;
+    size_t i = 0;
+    while (i < fam.size() && fam[i] != r.name) ++i;
+    if (i == fam.size()) {
+      fam.push_back(r.name);
+      cnt.push_back(0);
+      ms.push_back(0);
+      fl.push_back(0);
+      by.push_back(0);
+    }
+    cnt[i] += 1;
+    ms[i] += t;
+    fl[i] += r.flops;
+    by[i] += r.bytes;
+  }
+  g_summary_names = fam;
+  for (size_t i = 0; i < fam.size() && static_cast<int>(i) < cap; ++i) {
+    if (names) names[i] = g_summary_names[i].c_str();
+    if (launches) launches[i] = cnt[i];
+    if (total_ms) total_ms[i] = ms[i];
+    if (flops) flops[i] = fl[i];
+    if (bytes) bytes[i] = by[i];
+  }
+  return static_cast<int>(fam.size());
+}
+
+extern "C" int64_t tps_launch_count(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  return g_launches;
+}

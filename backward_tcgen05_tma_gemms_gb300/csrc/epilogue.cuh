@@ -1,0 +1,104 @@
+// epilogue.cuh -- per-element epilogue arithmetic shared by the tensor-core
+// and SIMT GEMM kernels: plain store, activation forward (pre-activation and
+// activation), activation backward (multiply by phi' of the pre-activation).
+#pragma once
+#include <cuda_bf16.h>
+
+#include "internal.cuh"
+
+namespace tps {
+
+__device__ __forceinline__ void store_elem(void* base, int dtype, int64_t idx, float v) {
+  if (dtype == TPS_F32)
+    static_cast<float*>(base)[idx] = v;
+  else
+    static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
+}
+
+// Store `n` (<= 32) consecutive values of one output row starting at element
+// index `idx`; uses 16-byte vector stores when the full run is aligned.
+__device__ __forceinline__ void store_run32(void* base, int dtype, int64_t idx, int n, const float (&v)[32]) {
+  if (dtype == TPS_F32) {
+    float* p = static_cast<float*>(base) + idx;
+    if (n == 32 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        reinterpret_cast<float4*>(p)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < n) p[i] = v[i];
+    }
+  } else {
+    __nv_bfloat16* p = static_cast<__nv_bfloat16*>(base) + idx;
+    if (n == 32 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 w;
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(v[8 * i + 0], v[8 * i + 1]);
+        __nv_bfloat162 b1 = __floats2bfloat162_rn(v[8 * i + 2], v[8 * i + 3]);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 4], v[8 * i + 5]);
+        __nv_bfloat162 b3 = __floats2bfloat162_rn(v[8 * i + 6], v[8 * i + 7]);
+        w.x = *reinterpret_cast<uint32_t*>(&b0);
+        w.y = *reinterpret_cast<uint32_t*>(&b1);
+        w.z = *reinterpret_cast<uint32_t*>(&b2);
+        w.w = *reinterpret_cast<uint32_t*>(&b3);
+        reinterpret_cast<uint4*>(p)[i] = w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < n) p[i] = __float2bfloat16_rn(v[i]);
+    }
+  }
+}
+
+__device__ __forceinline__ void load_run32(const float* p, int n, float (&a)[32]) {
+  if (n == 32 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(p) + i);
+      a[4 * i] = q.x;
+      a[4 * i + 1] = q.y;
+      a[4 * i + 2] = q.z;
+      a[4 * i + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a[i] = (i < n) ? __ldg(p + i) : 0.0f;
+  }
+}
+
+// Apply the epilogue to 32 consecutive accumulator values of row `row`,
+// columns [col0, col0 + n).
+__device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, int64_t col0, int n,
+                                               float (&v)[32]) {
+  if (e.mode == EPI_STORE) {
+    store_run32(e.d, e.d_dtype, row * e.ldd + col0, n, v);
+  } else if (e.mode == EPI_ACT_FWD) {
+    if (e.d != nullptr) store_run32(e.d, TPS_F32, row * e.ldd + col0, n, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = act_fwd(e.act, v[i]);
+    store_run32(e.d2, e.d2_dtype, row * e.ldd2 + col0, n, v);
+  } else {
+    float a[32];
+    load_run32(e.aux + row * e.ld_aux + col0, n, a);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= act_grad(e.act, a[i]);
+    store_run32(e.d, e.d_dtype, row * e.ldd + col0, n, v);
+  }
+}
+
+// Scalar form used by the SIMT kernel.
+__device__ __forceinline__ void epilogue_elem(const Epilogue& e, int64_t row, int64_t col, float v) {
+  if (e.mode == EPI_STORE) {
+    store_elem(e.d, e.d_dtype, row * e.ldd + col, v);
+  } else if (e.mode == EPI_ACT_FWD) {
+    if (e.d != nullptr) store_elem(e.d, TPS_F32, row * e.ldd + col, v);
+    store_elem(e.d2, e.d2_dtype, row * e.ldd2 + col, act_fwd(e.act, v));
+  } else {
+    store_elem(e.d, e.d_dtype, row * e.ldd + col, v * act_grad(e.act, e.aux[row * e.ld_aux + col]));
+  }
+}
+
+}  // namespace tps

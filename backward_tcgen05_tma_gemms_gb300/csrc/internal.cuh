@@ -1,0 +1,121 @@
+// internal.cuh -- declarations shared by the library's translation units
+// (never installed, never seen by callers; the public ABI is include/tps.h).
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "tps.h"
+
+namespace tps {
+
+// Device error word bits (read back by tps_last_device_error).
+constexpr uint32_t TPS_DEVERR_TIMEOUT = 1u;
+constexpr uint32_t TPS_DEVERR_LABEL = 2u;
+
+// ------------------------------------------------------------ epilogues
+// EPI_STORE    D = acc                                  (dtype d_dtype)
+// EPI_ACT_FWD  D = acc (fp32, may be null), D2 = phi(acc) (dtype d2_dtype)
+// EPI_ACT_BWD  D = acc * phi'(AUX), AUX the fp32 pre-activation
+enum EpiMode : int { EPI_STORE = 0, EPI_ACT_FWD = 1, EPI_ACT_BWD = 2 };
+
+struct Epilogue {
+  int mode = EPI_STORE;
+  int act = TPS_ACT_GELU_ERF;
+  void* d = nullptr;          // row-major M x N, leading dimension ldd
+  int64_t ldd = 0;
+  int d_dtype = TPS_F32;
+  void* d2 = nullptr;         // EPI_ACT_FWD activated output, row-major
+  int64_t ldd2 = 0;
+  int d2_dtype = TPS_BF16;
+  const float* aux = nullptr; // EPI_ACT_BWD pre-activation, row-major fp32
+  int64_t ld_aux = 0;
+};
+
+// One GEMM D[M x N] = sum_k A(m, k) B(k, n), operands addressed by element
+// strides: A(m, k) = a[m * a_sm + k * a_sk], B(k, n) = b[k * b_sk + n * b_sn].
+// One stride of each operand is 1 (its contiguous dimension).
+struct GemmDesc {
+  int64_t M = 0, N = 0, K = 0;
+  int in_dtype = TPS_BF16;
+  const void* a = nullptr;
+  int64_t a_sm = 0, a_sk = 0;
+  const void* b = nullptr;
+  int64_t b_sk = 0, b_sn = 0;
+  Epilogue epi;
+  // Number of logical ranks the contraction dimension K is sharded over
+  // (array_split plan).  1 when K is not sharded.
+  int32_t kparts = 1;
+  const char* name = "gemm";  // label used by the launch profiler
+};
+
+// Launchers (return a TPS_* status; asynchronous on `stream`).
+int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);
+int launch_gemm_simt(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);
+bool gemm_tc_supported(const GemmDesc& g);
+
+struct CeDesc {
+  int64_t T = 0, V = 0;
+  int32_t parts = 1;
+  const float* logits = nullptr;  // T x V fp32, leading dimension ldz
+  int64_t ldz = 0;
+  const void* labels = nullptr;   // T, int32 or int64
+  int label_dtype = TPS_I64;
+  float* loss = nullptr;          // T fp32
+  void* dlogits = nullptr;        // T x V, leading dimension ldg
+  int64_t ldg = 0;
+  int dlogits_dtype = TPS_BF16;
+  int32_t* owner = nullptr;       // T, nullable
+  float* stats = nullptr;         // workspace T x parts x 2 (two-pass path)
+  float* zy = nullptr;            // workspace T (two-pass path)
+};
+// Picks the one-read cluster kernel when the shard plan allows it, else the
+// two-pass kernels.  `used_cluster` reports the choice.
+int launch_ce(const CeDesc& c, uint32_t* dev_err, cudaStream_t stream, bool* used_cluster);
+bool ce_cluster_supported(int64_t V, int32_t parts, int dlogits_dtype);
+
+// Launch profiler hooks (api.cu).  When profiling is on, each kernel launch
+// is bracketed by CUDA events on its stream.
+struct ProfScope {
+  // `kind` names the kernel, `label` the call site (e.g. "gemm_tc", "mlp_dX").
+  ProfScope(const char* kind, const char* label, double flops, double bytes, cudaStream_t s);
+  ~ProfScope();
+  int slot;
+  cudaStream_t stream;
+};
+void note_launch();
+
+// array_split plan, closed form: offset(i) = i * (d / P) + min(i, d mod P).
+__host__ __device__ inline int64_t shard_offset(int64_t dim, int64_t parts, int64_t i) {
+  const int64_t q = dim / parts, r = dim % parts;
+  return i * q + (i < r ? i : r);
+}
+
+// ------------------------------------------------------------ activations
+// GELU (erf form) x * Phi(x); GELU tanh approximation
+// 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))); tanh.  Derivatives from
+// differentiating those definitions.  CUDA's erff / tanhf / expf are called,
+// not re-derived.
+__device__ __forceinline__ float act_fwd(int act, float x) {
+  if (act == TPS_ACT_GELU_ERF) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+  if (act == TPS_ACT_GELU_TANH) {
+    const float u = tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x));
+    return 0.5f * x * (1.0f + u);
+  }
+  return tanhf(x);
+}
+__device__ __forceinline__ float act_grad(int act, float x) {
+  if (act == TPS_ACT_GELU_ERF) {
+    const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
+    const float pdf = 0.39894228040143268f * expf(-0.5f * x * x);
+    return cdf + x * pdf;
+  }
+  if (act == TPS_ACT_GELU_TANH) {
+    const float c = 0.79788456080286536f;
+    const float u = tanhf(c * (x + 0.044715f * x * x * x));
+    return 0.5f * (1.0f + u) + 0.5f * x * (1.0f - u * u) * c * (1.0f + 3.0f * 0.044715f * x * x);
+  }
+  const float h = tanhf(x);
+  return 1.0f - h * h;
+}
+
+}  // namespace tps

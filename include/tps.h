@@ -1,0 +1,213 @@
+/*
+ * tps.h -- C ABI of the tensor-parallel sharded GEMM library for GB300
+ * (sm_103a).  Built as libtps.so from backward_tcgen05_tma_gemms_gb300/csrc.
+ *
+ * The library computes the forward and backward of a matrix product split
+ * over P logical ranks, the column-then-row tensor-parallel MLP and the
+ * vocabulary-sharded cross-entropy.  On one GPU the logical ranks are shard
+ * partitions of the same device buffers: a result the pages concatenate is a
+ * range of one output buffer, and a result the pages sum over ranks is
+ * accumulated inside the producing kernel (the contraction loop runs over
+ * the ranks' shard segments in rank order).  No communication library is
+ * used.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [SG] "Sharded GEMM与Backprop：行、列、内维三种切分"
+ *   [MC] "多卡张量：拆开计算，再合回同一结果"
+ *   [TP] "第 6 课：张量并行 TP"
+ *
+ * Conventions for every entry point:
+ *   - Memory.  Every pointer in a tps_tensor is a DEVICE pointer on the
+ *     current CUDA device, owned by the caller.  The library never allocates
+ *     or frees device memory; scratch space comes from the caller's
+ *     `workspace` (size from the *_workspace_bytes queries).
+ *   - Streams.  Work is enqueued on `cuda_stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and the call returns without waiting.
+ *   - Validation.  Shapes, dtypes, layouts and partition arguments are
+ *     checked on the host before anything is launched; on failure nothing is
+ *     enqueued and a TPS_ERR_* code is returned.  A failed CUDA launch
+ *     returns TPS_ERR_CUDA.  Conditions only the device can see (a label out
+ *     of range, a wait that exceeded its time limit) are recorded in a
+ *     device error word read by tps_last_device_error().
+ *   - Layouts.  Tensors are strided (strides in elements); a 2-D operand must
+ *     have unit stride in one of its two dimensions.  Tensors described as
+ *     "(..., n)" may have extra leading dimensions, which must be mutually
+ *     contiguous and are flattened into rows.
+ *   - Dtypes.  Operands are all TPS_F32 (true fp32 FMA arithmetic) or all
+ *     TPS_BF16 (bf16 operands, fp32 accumulation on the tcgen05 tensor
+ *     cores).  Results named "fp32" are always TPS_F32.
+ *   - Thread safety.  Entry points may be called from several host threads;
+ *     launches on one stream execute in issue order.
+ */
+#ifndef TPS_H_
+#define TPS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+enum { TPS_F32 = 0, TPS_BF16 = 1, TPS_I32 = 2, TPS_I64 = 3 };
+
+/* A strided tensor view.  `data` is a device pointer (host pointer only
+ * where an entry point says so); shape/stride entries past `ndim` are
+ * ignored.  Strides are in elements, not bytes. */
+typedef struct tps_tensor {
+  void* data;
+  int32_t dtype;
+  int32_t ndim; /* 1..4 */
+  int64_t shape[4];
+  int64_t stride[4];
+} tps_tensor;
+
+/* Status codes.  TPS_ERR_SHAPE and TPS_ERR_PARTITION are the two errors of
+ * [SG] "Python 参考实现" (ValueError('shape') / ValueError('partition')). */
+enum {
+  TPS_OK = 0,
+  TPS_ERR_SHAPE = 1,     /* wrong rank, mismatched dimensions, wrong output shape */
+  TPS_ERR_PARTITION = 2, /* parts/tp < 1, unknown axis */
+  TPS_ERR_DTYPE = 3,     /* unsupported or mixed element types */
+  TPS_ERR_LAYOUT = 4,    /* no unit stride, or leading dims not flattenable */
+  TPS_ERR_LABEL = 5,     /* a label outside [0, V) (reported by the device) */
+  TPS_ERR_WORKSPACE = 6, /* workspace missing, too small or misaligned */
+  TPS_ERR_CUDA = 7,      /* a CUDA runtime call failed */
+  TPS_ERR_TIMEOUT = 8,   /* a device-side wait exceeded its limit */
+  TPS_ERR_ARG = 9        /* NULL where a tensor is required, bad enum */
+};
+
+/* Split axes of tps_matmul_fwd_bwd ([SG] "解题路线" steps 2-4). */
+enum { TPS_AXIS_ROWS = 0, TPS_AXIS_COLUMNS = 1, TPS_AXIS_INNER = 2 };
+
+/* Element-wise activation phi of the MLP.
+ *   GELU_ERF : x * Phi(x) -- torch's default gelu used by [TP] "参考答案".
+ *   GELU_TANH: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *   TANH     : tanh, with phi' = 1 - H^2 as [MC] "02 / BACKWARD" writes. */
+enum { TPS_ACT_GELU_ERF = 0, TPS_ACT_GELU_TANH = 1, TPS_ACT_TANH = 2 };
+
+/* Weight layouts.  IN_OUT: W1 is d x F and W2 is F x d (math notation
+ * Y = phi(X W1) W2 of [MC] "01 / COLUMN THEN ROW").  OUT_IN: torch
+ * nn.Linear layout, W1 is F x d and W2 is d x F ([TP] "参考答案",
+ * x @ w.T).  For the CE head: IN_OUT is d x V, OUT_IN is V x d. */
+enum { TPS_W_IN_OUT = 0, TPS_W_OUT_IN = 1 };
+
+/* ------------------------------------------------------------------------
+ * tps_plan_shards -- array_split shard plan ([SG] "Python 参考实现";
+ * [SG] "手动走一遍": K=5, parts=2 gives 3/2; parts > dim gives empty shards).
+ * Writes offsets[0..parts] (caller-owned HOST array of parts+1 entries) with
+ * offsets[i] = i*floor(dim/parts) + min(i, dim mod parts): the first
+ * (dim mod parts) shards get one extra element.
+ * Returns TPS_ERR_PARTITION if parts < 1, TPS_ERR_SHAPE if dim < 0,
+ * TPS_ERR_ARG if offsets is NULL.  Host only, no CUDA call.
+ * ---------------------------------------------------------------------- */
+int tps_plan_shards(int64_t dim, int32_t parts, int64_t* offsets);
+
+/* ------------------------------------------------------------------------
+ * tps_matmul_fwd_bwd -- forward and backward of L = <G, AB> split over
+ * `parts` logical ranks along `axis` ([SG] "题意与假设", "解题路线" 1-4):
+ *   Y = A B,  dA = G B^T,  dB = A^T G.
+ *   ROWS    : A and G split by rows; Y and dA are row-concatenated layouts,
+ *             dB = sum_r A_r^T G_r is reduced inside the dB kernel.
+ *   COLUMNS : B and G split by columns; Y and dB are column-concatenated,
+ *             dA = sum_r G_r B_r^T is reduced in-kernel.
+ *   INNER   : A split by columns, B by rows; Y = sum_r A_r B_r is reduced
+ *             in-kernel, dA and dB are concatenated along K.
+ * A (M x K), B (K x N), G (M x N): all TPS_F32 or all TPS_BF16.
+ * Y (M x N), dA (M x K), dB (K x N): TPS_F32; any may be NULL to skip it.
+ * Uneven and empty shards are legal.  No division by `parts` anywhere.
+ * Errors: TPS_ERR_SHAPE (non-2-D, K or G mismatch, wrong output shape),
+ * TPS_ERR_PARTITION (parts < 1, unknown axis), TPS_ERR_DTYPE, TPS_ERR_LAYOUT.
+ * ---------------------------------------------------------------------- */
+int tps_matmul_fwd_bwd(const tps_tensor* A, const tps_tensor* B, const tps_tensor* G, int32_t parts,
+                       int32_t axis, const tps_tensor* Y, const tps_tensor* dA, const tps_tensor* dB,
+                       void* cuda_stream);
+
+/* ------------------------------------------------------------------------
+ * tps_mlp_fwd_bwd -- column-then-row tensor-parallel MLP, forward and
+ * backward, over `tp` logical ranks that split the hidden width F
+ * ([MC] "01 / COLUMN THEN ROW" and "02 / BACKWARD"; [TP] core concept 2.A):
+ *   rank r owns columns F_r of W1 and rows F_r of W2 (array_split of F);
+ *   H_r = phi(X W1_r) stays local, Y = sum_r H_r W2_r (one in-kernel sum);
+ *   dZ_r = (G_Y W2_r^T) * phi'(X W1_r), dW2_r = H_r^T G_Y, dW1_r = X^T dZ_r,
+ *   dX = sum_r dZ_r W1_r^T (in-kernel sum).  The replicated G_Y is used
+ *   once per rank and never summed again.
+ * X (..., d) and GY (..., d): same dtype (F32 or BF16), rows T.
+ * W1, W2: layout `weight_layout` (TPS_W_IN_OUT or TPS_W_OUT_IN), same dtype.
+ * Y, dX (..., d) fp32; dW1, dW2 fp32 with the shapes of W1, W2.
+ * `workspace` (device, 256-byte aligned, >= tps_mlp_workspace_bytes) holds
+ * the pre-activation (fp32), the activation and dZ (operand dtype).
+ * Errors as tps_matmul_fwd_bwd, plus TPS_ERR_WORKSPACE, TPS_ERR_ARG (act).
+ * ---------------------------------------------------------------------- */
+int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const tps_tensor* W2, const tps_tensor* GY,
+                    int32_t tp, int32_t act, int32_t weight_layout, const tps_tensor* Y, const tps_tensor* dX,
+                    const tps_tensor* dW1, const tps_tensor* dW2, void* workspace, size_t workspace_bytes,
+                    void* cuda_stream);
+
+/* Workspace bytes tps_mlp_fwd_bwd needs for T tokens, model width d, hidden
+ * width F and operand dtype `dtype` (tp does not change it). */
+size_t tps_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int32_t dtype);
+
+/* ------------------------------------------------------------------------
+ * tps_vocab_ce_fwd_bwd -- cross-entropy over a vocabulary split into `tp`
+ * contiguous shards (array_split of V), forward and backward
+ * ([MC] "04 / VOCABULARY SHARDS"; single supervised position per token, no
+ * label smoothing, no ignore index):
+ *   z = h Whead (T x V fp32, kept in the workspace);
+ *   per token and shard r: m_r = max_{j in V_r} z_j, s_r = sum e^{z_j - m_r};
+ *   combined: m = max_r m_r, s = sum_r s_r e^{m_r - m},
+ *   loss = log s + m - z_y;  dlogits_j = e^{z_j - m}/s - 1[j = y];
+ *   dHidden = dlogits Whead^T, summed over all shards (no division by tp).
+ * h (..., d): F32 or BF16.  Whead: d x V (TPS_W_IN_OUT) or V x d
+ * (TPS_W_OUT_IN), same dtype.  labels (T): TPS_I64 or TPS_I32 in [0, V).
+ * loss (T) fp32.  dlogits (T x V): the operand dtype (bf16 for bf16 runs).
+ * dHidden (..., d) fp32.  owner (T) TPS_I32 or NULL: the rank whose shard
+ * holds the label.  `workspace` >= tps_ce_workspace_bytes, 256-B aligned.
+ * A label outside [0, V) makes that token's loss NaN and its owner -1, and
+ * sets TPS_ERR_LABEL in the device error word.
+ * ---------------------------------------------------------------------- */
+int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead, const tps_tensor* labels, int32_t tp,
+                         int32_t weight_layout, const tps_tensor* loss, const tps_tensor* dlogits,
+                         const tps_tensor* dHidden, const tps_tensor* owner, void* workspace,
+                         size_t workspace_bytes, void* cuda_stream);
+
+/* Workspace bytes tps_vocab_ce_fwd_bwd needs for T tokens, vocabulary V and
+ * `tp` shards. */
+size_t tps_ce_workspace_bytes(int64_t T, int64_t V, int32_t tp);
+
+/* ------------------------------------------------------------------------
+ * tps_last_device_error -- synchronizes `cuda_stream`, then reads and clears
+ * the current device's error word.  Returns TPS_OK, TPS_ERR_TIMEOUT (a
+ * kernel gave up waiting and exited early; its outputs are invalid),
+ * TPS_ERR_LABEL, or TPS_ERR_CUDA if the synchronization itself failed.
+ * ---------------------------------------------------------------------- */
+int tps_last_device_error(void* cuda_stream);
+
+/* Static description of a status code. */
+const char* tps_strerror(int code);
+
+/* Detail of the last failure on the calling host thread ("" if none). */
+const char* tps_last_error_detail(void);
+
+/* ------------------------------------------------------------------------
+ * Launch profiler.  While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on its own stream.
+ * tps_profile_reset clears the records and enables recording;
+ * tps_profile_stop disables it.  tps_profile_summary synchronizes the
+ * recorded events and writes, for kernel family i < n (host arrays of
+ * `cap` entries, NULL to skip): its name, number of launches, total device
+ * milliseconds, total algorithmic FLOPs and bytes.  Returns n, or a
+ * negative TPS_ERR_* code.  tps_launch_count returns the number of kernels
+ * launched since the last reset, whether or not profiling is enabled.
+ * ---------------------------------------------------------------------- */
+int tps_profile_reset(int enable);
+int tps_profile_stop(void);
+int tps_profile_summary(int cap, const char** names, int64_t* launches, double* total_ms, double* flops,
+                        double* bytes);
+int64_t tps_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TPS_H_ */

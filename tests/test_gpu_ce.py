@@ -1,0 +1,114 @@
+"""GPU parity of tps_vocab_ce_fwd_bwd against the float64 oracle.
+
+"多卡张量：拆开计算，再合回同一结果", section 04 / VOCABULARY SHARDS: per-shard
+max and sum-exp combined into one log-sum-exp, loss, dlogits = softmax -
+onehot, dHidden summed over the vocabulary shards; the owner rank of each
+label is compared bit-exactly."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from backward_tcgen05_tma_gemms_gb300 import api, inputs
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def run(h, W, labels, tp, layout="in_out"):
+    out = api.vocab_ce_fwd_bwd(h.cuda(), W.cuda(), labels.cuda(), tp, layout)
+    rc = api.last_device_error()
+    return [t.cpu() for t in out], rc
+
+
+def check(orc, h, W, labels, tp, bf16, layout="in_out", what=""):
+    (loss, dlog, dh, own), rc = run(h, W, labels, tp, layout)
+    assert rc == 0
+    w = inputs.as_f64(W) if layout == "in_out" else inputs.as_f64(W).T
+    rl, rdl, rdh, rown = orc.ce_tokens(inputs.as_f64(h), w, labels.numpy(), tp)
+    assert_close(loss, rl, bf16, f"{what} loss")
+    assert_close(dlog, rdl, bf16, f"{what} dlogits")
+    assert_close(dh, rdh, bf16, f"{what} dHidden")
+    assert np.array_equal(own.numpy(), rown), f"{what} owner"
+
+
+def test_worked_logits(orc):
+    z = json.load(open(os.path.join(GOLDEN, "ce_worked_logits.json")))["logits"]
+    h = torch.tensor([z] * 6, dtype=torch.float32)
+    W = torch.eye(6)
+    labels = torch.arange(6)
+    for tp in (1, 2, 3, 7):
+        (loss, dlog, dh, own), rc = run(h, W, labels, tp)
+        assert rc == 0
+        den = sum(math.exp(v) for v in z)
+        for y in range(6):
+            assert abs(loss[y].item() - (math.log(den) - z[y])) < 1e-5
+            p = np.array([math.exp(v) / den for v in z])
+            assert np.abs(dlog[y].numpy() - (p - np.eye(6)[y])).max() < 1e-6
+        off = api.plan_shards(6, tp)
+        assert [int(v) for v in own] == [next(r for r in range(tp) if off[r] <= y < off[r + 1]) for y in range(6)]
+
+
+@pytest.mark.parametrize("tp", [1, 3, 7, 8])
+def test_fp32_cluster_path(orc, tp):
+    h, W, labels = inputs.ce_case(tp, 37, 48, 1000, torch.float32, w_std=0.5)
+    check(orc, h, W, labels, tp, False, what=f"tp{tp}")
+
+
+@pytest.mark.parametrize("tp,V", [(9, 1000), (16, 5003), (1, 100000)])
+def test_fp32_two_pass_path(orc, tp, V):
+    """More ranks than a cluster holds, or a shard larger than shared memory."""
+    h, W, labels = inputs.ce_case(tp + V, 5, 16, V, torch.float32, w_std=0.5)
+    check(orc, h, W, labels, tp, False, what=f"tp{tp} V{V}")
+
+
+def test_fp32_empty_shards(orc):
+    h, W, labels = inputs.ce_case(3, 6, 8, 5, torch.float32, w_std=1.0)
+    check(orc, h, W, labels, 8, False, what="tp8 V5")       # three empty shards
+
+
+@pytest.mark.parametrize("tp", [8, 7])
+@pytest.mark.parametrize("layout", ["in_out", "out_in"])
+def test_bf16_tensor_core(orc, tp, layout):
+    h, W, labels = inputs.ce_case(40 + tp, 200, 256, 32000, torch.bfloat16)
+    if layout == "out_in":
+        W = W.t().contiguous()
+    with api.profile() as p:
+        check(orc, h, W, labels, tp, True, layout, what=f"bf16 tp{tp} {layout}")
+    kinds = {k.split(":")[0] for k in p.summary}
+    assert kinds == {"gemm_tc", "ce_cluster"}, p.summary
+
+
+def test_label_out_of_range_sets_error():
+    h, W, labels = inputs.ce_case(1, 4, 16, 64, torch.float32)
+    labels[2] = 64
+    (loss, dlog, dh, own), rc = run(h, W, labels, 4)
+    assert rc == api.ERR_LABEL
+    assert torch.isnan(loss[2]) and own[2] == -1
+    assert torch.isfinite(loss[[0, 1, 3]]).all()
+    assert api.last_device_error() == 0     # the word was cleared
+
+
+def test_llama_vocab_sampled(orc):
+    """h 8192 x 4096, head 4096 x 128256, tp=8 (16032 per shard), bf16, at
+    full size in the benchmark's launch configuration; 8 tokens spread over
+    the batch are recomputed by the oracle (loss, full dlogits row, dHidden
+    row) and every owner rank is checked against a host scan."""
+    cfg = inputs.LLAMA_CE
+    h, W, labels = inputs.ce_case(0, cfg["T"], cfg["d"], cfg["V"], torch.bfloat16)
+    (loss, dlog, dh, own), rc = run(h, W, labels, cfg["tp"])
+    assert rc == 0
+    toks = np.array([0, 1, 1000, 2047, 4096, 5555, 8000, 8191])
+    rl, rdl, rdh, rown = orc.ce_tokens(inputs.as_f64(h), inputs.as_f64(W), labels.numpy(), cfg["tp"], toks)
+    assert_close(loss[toks], rl, True, "loss")
+    assert_close(dlog[toks], rdl, True, "dlogits")
+    assert_close(dh[toks], rdh, True, "dHidden")
+    off = np.array(api.plan_shards(cfg["V"], cfg["tp"]))
+    assert np.array_equal(own.numpy(), np.searchsorted(off, labels.numpy(), side="right") - 1)
+    assert torch.isfinite(loss).all()
+    # mean loss near log V + var(z)/2 with var(z) = d * 0.02^2
+    assert abs(loss.mean().item() - (math.log(cfg["V"]) + cfg["d"] * 0.02 ** 2 / 2)) < 0.1
