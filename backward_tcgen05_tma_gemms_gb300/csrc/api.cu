@@ -116,10 +116,15 @@ static const char* dtname(int d) {
 // The view must have unit stride in one dimension (either one when a
 // dimension has extent <= 1).
 static int as_mat(const tps_tensor* t, const char* name, bool flatten, Mat* m) {
-  if (t == nullptr || t->data == nullptr) return fail(TPS_ERR_ARG, "%s: missing tensor", name);
+  if (t == nullptr) return fail(TPS_ERR_ARG, "%s: missing tensor", name);
   if (t->ndim < 1 || t->ndim > 4) return fail(TPS_ERR_SHAPE, "%s: ndim %d", name, t->ndim);
-  for (int i = 0; i < t->ndim; ++i)
+  int64_t numel = 1;
+  for (int i = 0; i < t->ndim; ++i) {
     if (t->shape[i] < 0) return fail(TPS_ERR_SHAPE, "%s: negative extent", name);
+    numel *= t->shape[i];
+  }
+  // An empty tensor may have no storage (NULL data); nothing reads it.
+  if (t->data == nullptr && numel > 0) return fail(TPS_ERR_ARG, "%s: missing data", name);
   if (!flatten && t->ndim != 2) return fail(TPS_ERR_SHAPE, "%s: expected a 2-D tensor, got %d-D", name, t->ndim);
   if (flatten && t->ndim < 2) return fail(TPS_ERR_SHAPE, "%s: expected (..., n), got 1-D", name);
   m->data = t->data;

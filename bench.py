@@ -69,7 +69,7 @@ def peak_value(peaks, *keys):
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -77,11 +77,24 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.windows = []   # (t0, t1) host wall-clock bounds of the timed regions
+
+    def window(self):
+        sampler = self
+
+        class _W:
+            def __enter__(self):
+                self.t0 = time.time()
+
+            def __exit__(self, *exc):
+                sampler.windows.append((self.t0, time.time()))
+                return False
+        return _W()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
                  "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -104,18 +117,23 @@ class ClockSampler:
         return False
 
     def summary(self):
+        import datetime
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, clk_max = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for name, v in zip(names, parts[5:9]):
+            if self.windows and not any(t0 - 0.05 <= ts <= t1 + 0.05 for t0, t1 in self.windows):
+                continue
+            sm.append(clk)
+            smax.append(clk_max)
+            for name, v in zip(names, parts[6:10]):
                 if v.lower() == "active":
                     reasons.add(name)
         if not sm:
@@ -168,13 +186,14 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        with api.profile() as prof:
-            ev0.record(stream)
-            for _ in range(args.steps):
-                step(d)
-            ev1.record(stream)
-            torch.cuda.synchronize(dev)
+    clk = ClockSampler(dev.index if dev.index is not None else 0).__enter__()
+    time.sleep(0.3)   # let the sampler start before the timed region
+    with clk.window(), api.profile() as prof:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(d)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
     barrier()
     ms = ev0.elapsed_time(ev1) / args.steps
     rc = api.last_device_error()
@@ -201,11 +220,14 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    with clk.window():
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    time.sleep(0.2)
+    clk.__exit__(None, None, None)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
     assert torch.isfinite(host_out[4]).all(), "non-finite loss"
@@ -220,7 +242,7 @@ def run_gpu(args, rank, world, local_rank):
 
 
 # ----------------------------------------------------------------- oracle (CPU) arm
-def oracle_sample(n_rows=16, n_cols=16, n_tok=16, seed=0, host=None):
+def oracle_sample(n_rows=192, n_cols=192, n_tok=192, seed=0, host=None):
     """Time the float64 oracle on a bounded sample of one step: n_rows rows of
     the MLP's Y/dX, n_cols columns of dW1 / rows of dW2 and n_tok tokens of
     the cross-entropy (loss, dlogits row, dHidden row).  Returns (flops done,
@@ -252,7 +274,7 @@ def oracle_sample(n_rows=16, n_cols=16, n_tok=16, seed=0, host=None):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["tps", "reference"], default="tps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -271,7 +293,7 @@ def main():
         for _ in range(args.warmup):
             oracle_sample(1, 1, 1, host=host)
         for i in range(args.steps):
-            f, s, threads, desc = oracle_sample(4, 4, 4, seed=i, host=host)
+            f, s, threads, desc = oracle_sample(16, 16, 16, seed=i, host=host)
             flops_all += f
             secs_all += s
         tflops = flops_all / secs_all / 1e12
