@@ -197,6 +197,145 @@ __global__ void __launch_bounds__(CE_THREADS) ce_cluster_kernel(const CeParams p
   cluster_sync();  // no CTA leaves while another may still read its `stat`
 }
 
+// Register-resident variant of the one-read path for shards of up to
+// CE_THREADS * 4 * VPT4 elements (plus an unaligned head and tail of at most
+// three each): every thread issues all of its 16-byte loads before using
+// any, so a CTA keeps its whole shard (64 KB at V=128256, P=8) in flight,
+// and the slice never touches shared memory.
+template <typename TOut, int VPT4>
+__global__ void __launch_bounds__(CE_THREADS) ce_cluster_reg_kernel(const CeParams p) {
+  __shared__ float red[32];
+  __shared__ float stat[2];
+  __shared__ float comb[2];
+
+  const uint32_t r = cluster_ctarank();
+  const int64_t t = blockIdx.y;
+  const int64_t beg = shard_offset(p.V, p.parts, r);
+  const int64_t len = shard_offset(p.V, p.parts, r + 1) - beg;
+  const float* zrow = p.z + t * p.ldz + beg;
+  const int tid = threadIdx.x;
+
+  const int64_t head = imin64(len, (4 - ((reinterpret_cast<uintptr_t>(zrow) >> 2) & 3)) & 3);
+  const int64_t body4 = (len - head) / 4;
+  const int64_t tail0 = head + 4 * body4;  // first tail element
+  const float4* z4 = reinterpret_cast<const float4*>(zrow + head);
+
+  float4 v[VPT4];
+#pragma unroll
+  for (int k = 0; k < VPT4; ++k) {
+    const int64_t j = tid + static_cast<int64_t>(k) * CE_THREADS;
+    v[k] = (j < body4) ? __ldcs(z4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  }
+  // at most 3 head and 3 tail scalars, held by threads 0..5
+  float e = -INFINITY;
+  int64_t e_idx = -1;
+  if (tid < head) {
+    e_idx = tid;
+  } else if (tid >= 3 && tid - 3 < len - tail0) {
+    e_idx = tail0 + (tid - 3);
+  }
+  if (e_idx >= 0) e = __ldcs(zrow + e_idx);
+
+  float mx = e;
+#pragma unroll
+  for (int k = 0; k < VPT4; ++k) mx = fmaxf(mx, fmaxf(fmaxf(v[k].x, v[k].y), fmaxf(v[k].z, v[k].w)));
+  const float m_r = block_max(mx, red);
+  float se = 0.0f;
+  if (len > 0) {
+    // exp(-inf - m_r) = 0 for the padding slots
+#pragma unroll
+    for (int k = 0; k < VPT4; ++k)
+      se += __expf(v[k].x - m_r) + __expf(v[k].y - m_r) + __expf(v[k].z - m_r) + __expf(v[k].w - m_r);
+    if (e_idx >= 0) se += __expf(e - m_r);
+  }
+  const float s_r = block_sum(se, red);
+  if (tid == 0) {
+    stat[0] = m_r;
+    stat[1] = s_r;
+  }
+  cluster_sync();
+
+  const int64_t y = load_label(p, t);
+  const bool valid = (y >= 0 && y < p.V);
+  const int64_t yl = (valid && y >= beg && y < beg + len) ? (y - beg) : -1;
+  if (tid == 0) {
+    float m = -INFINITY;
+    for (int q = 0; q < p.parts; ++q) m = fmaxf(m, ld_cluster_f32(cluster_map(smem_u32(&stat[0]), q)));
+    float s = 0.0f;
+    for (int q = 0; q < p.parts; ++q) {
+      const float mq = ld_cluster_f32(cluster_map(smem_u32(&stat[0]), q));
+      const float sq = ld_cluster_f32(cluster_map(smem_u32(&stat[1]), q));
+      if (sq > 0.0f) s += sq * __expf(mq - m);
+    }
+    comb[0] = m;
+    comb[1] = s;
+    if (!valid && r == 0) {
+      p.loss[t] = __int_as_float(0x7fc00000);  // NaN
+      if (p.owner) p.owner[t] = -1;
+      atomicOr(p.err, TPS_DEVERR_LABEL);
+    }
+  }
+  __syncthreads();
+  const float m = comb[0];
+  const float s = comb[1];
+  const float inv_s = 1.0f / s;
+  // the owner rank's thread holding z_y writes the loss
+  if (yl >= 0) {
+    float zy = 0.0f;
+    bool mine = false;
+    if (yl == e_idx) {
+      zy = e;
+      mine = true;
+    } else if (yl >= head && yl < tail0) {
+      const int64_t q4 = (yl - head) >> 2;
+      if (q4 % CE_THREADS == tid) {
+        const int64_t slot = q4 / CE_THREADS;
+        float4 w = v[0];
+#pragma unroll
+        for (int k = 1; k < VPT4; ++k)
+          if (k == slot) w = v[k];  // static register indexing
+        const int c = static_cast<int>((yl - head) & 3);
+        zy = c == 0 ? w.x : (c == 1 ? w.y : (c == 2 ? w.z : w.w));
+        mine = true;
+      }
+    }
+    if (mine) {
+      p.loss[t] = logf(s) + m - zy;
+      if (p.owner) p.owner[t] = static_cast<int32_t>(r);
+    }
+  }
+
+  TOut* grow = static_cast<TOut*>(p.dlog) + t * p.ldg + beg;
+  auto g = [&](float x, int64_t idx) { return __expf(x - m) * inv_s - (idx == yl ? 1.0f : 0.0f); };
+  if (e_idx >= 0) store_grad(grow + e_idx, g(e, e_idx));
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(grow + head) & (4 * sizeof(TOut) - 1)) == 0;
+#pragma unroll
+  for (int k = 0; k < VPT4; ++k) {
+    const int64_t j = tid + static_cast<int64_t>(k) * CE_THREADS;
+    if (j < body4) {
+      const int64_t i0 = head + 4 * j;
+      const float g0 = g(v[k].x, i0), g1 = g(v[k].y, i0 + 1), g2 = g(v[k].z, i0 + 2), g3 = g(v[k].w, i0 + 3);
+      if (vec_ok) {
+        if constexpr (sizeof(TOut) == 2) {
+          __nv_bfloat162 a = __floats2bfloat162_rn(g0, g1), b = __floats2bfloat162_rn(g2, g3);
+          uint2 w;
+          w.x = *reinterpret_cast<uint32_t*>(&a);
+          w.y = *reinterpret_cast<uint32_t*>(&b);
+          __stcs(reinterpret_cast<uint2*>(grow + i0), w);
+        } else {
+          __stcs(reinterpret_cast<float4*>(grow + i0), make_float4(g0, g1, g2, g3));
+        }
+      } else {
+        store_grad(grow + i0, g0);
+        store_grad(grow + i0 + 1, g1);
+        store_grad(grow + i0 + 2, g2);
+        store_grad(grow + i0 + 3, g3);
+      }
+    }
+  }
+  cluster_sync();  // no CTA leaves while another may still read its `stat`
+}
+
 // ------------------------------------------------------------ two-pass path
 // Grid (parts, T): rank r's (m_r, s_r) for token t with an online max/sum
 // (one read of the shard), the label's logit and owner.
@@ -291,21 +430,18 @@ bool ce_cluster_supported(int64_t V, int32_t parts, int /*dlogits_dtype*/) {
   return max_len <= CE_MAX_SHARD;
 }
 
+template <typename TOut, int VPT4>
+static cudaError_t launch_cluster_reg(const CeParams& p, cudaLaunchConfig_t cfg) {
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, ce_cluster_reg_kernel<TOut, VPT4>, p);
+}
+
 template <typename TOut>
 static int launch_cluster(const CeParams& p, cudaStream_t stream) {
   const int64_t max_len = (p.V + p.parts - 1) / p.parts;
-  const size_t smem = static_cast<size_t>(max_len + 4) * sizeof(float);
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(ce_cluster_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>((CE_MAX_SHARD + 4) * sizeof(float)));
-  });
-  if (attr_err != cudaSuccess) return TPS_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.parts), static_cast<unsigned>(p.T), 1);
   cfg.blockDim = dim3(CE_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -316,7 +452,25 @@ static int launch_cluster(const CeParams& p, cudaStream_t stream) {
   cfg.numAttrs = 1;
   const double bytes = double(p.T) * double(p.V) * (4.0 + sizeof(TOut)) + double(p.T) * (8.0 + 4.0);
   ProfScope prof("ce_cluster", "ce_core", 0.0, bytes, stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, ce_cluster_kernel<TOut>, p);
+  cudaError_t e;
+  // body capacity of the register kernel: CE_THREADS * 4 * VPT4 elements
+  if (max_len <= CE_THREADS * 4 * 2) {
+    e = launch_cluster_reg<TOut, 2>(p, cfg);
+  } else if (max_len <= CE_THREADS * 4 * 4) {
+    e = launch_cluster_reg<TOut, 4>(p, cfg);
+  } else if (max_len <= CE_THREADS * 4 * 8) {
+    e = launch_cluster_reg<TOut, 8>(p, cfg);
+  } else {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+      attr_err = cudaFuncSetAttribute(ce_cluster_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>((CE_MAX_SHARD + 4) * sizeof(float)));
+    });
+    if (attr_err != cudaSuccess) return TPS_ERR_CUDA;
+    cfg.dynamicSmemBytes = static_cast<size_t>(max_len + 4) * sizeof(float);
+    e = cudaLaunchKernelEx(&cfg, ce_cluster_kernel<TOut>, p);
+  }
   note_launch();
   return e == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
 }

@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "epilogue.cuh"
@@ -41,6 +42,11 @@ constexpr uint32_t TC_TMEM_COLS = 2 * TC_BN;  // two fp32 accumulators of BN col
 constexpr int TC_GROUP_M = 16;                // tile raster: groups of 16 M-tiles
 // A box of an MN-major operand: 64 MN elements (128 B) x 64 K rows.
 constexpr int TC_MN_BOX_BYTES = 64 * TC_BK * 2;  // 8 KB
+// Epilogue staging for TMA stores, per epilogue warp: a 32 x 32 fp32 box
+// (128-byte swizzle) and a 32 x 32 bf16 box (64-byte swizzle).
+constexpr int TC_STG_F32_BYTES = 32 * 32 * 4;
+constexpr int TC_STG_BF16_BYTES = 32 * 32 * 2;
+constexpr int TC_STAGING_BYTES = 4 * (TC_STG_F32_BYTES + TC_STG_BF16_BYTES);
 
 struct TcBarriers {
   uint64_t full[TC_STAGES];
@@ -52,14 +58,42 @@ struct TcBarriers {
   uint32_t abort;
 };
 
-constexpr size_t TC_SMEM_BYTES = 1024 /*alignment slack*/ + TC_STAGES * TC_STAGE_BYTES + sizeof(TcBarriers);
+constexpr size_t TC_SMEM_BYTES =
+    1024 /*alignment slack*/ + TC_STAGES * TC_STAGE_BYTES + TC_STAGING_BYTES + sizeof(TcBarriers);
 
 struct TcParams {
   int M, N, K;
   int m_tiles, n_tiles, k_tiles, num_tiles;
+  int tma_store;  // 1: outputs leave through swizzled staging + TMA stores
   Epilogue epi;
   uint32_t* err;
 };
+
+// Row `r` of a warp's staging box, in the layout the TMA unit expects for
+// 128-byte (fp32, 8 chunks of 16 B per row) and 64-byte (bf16, 4 chunks per
+// row) swizzling: chunk i of row r sits at chunk i ^ f(r).  Consecutive rows
+// land in different bank groups, so the per-lane row writes do not conflict.
+__device__ __forceinline__ void stage_f32_sw128(uint8_t* buf, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    *reinterpret_cast<float4*>(buf + r * 128 + ((i ^ (r & 7)) << 4)) =
+        make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+__device__ __forceinline__ void stage_bf16_sw64(uint8_t* buf, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b0 = __floats2bfloat162_rn(v[8 * i + 0], v[8 * i + 1]);
+    __nv_bfloat162 b1 = __floats2bfloat162_rn(v[8 * i + 2], v[8 * i + 3]);
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 4], v[8 * i + 5]);
+    __nv_bfloat162 b3 = __floats2bfloat162_rn(v[8 * i + 6], v[8 * i + 7]);
+    uint4 w;
+    w.x = *reinterpret_cast<uint32_t*>(&b0);
+    w.y = *reinterpret_cast<uint32_t*>(&b1);
+    w.z = *reinterpret_cast<uint32_t*>(&b2);
+    w.w = *reinterpret_cast<uint32_t*>(&b3);
+    *reinterpret_cast<uint4*>(buf + r * 64 + ((i ^ ((r >> 1) & 3)) << 4)) = w;
+  }
+}
 
 __device__ __forceinline__ void tc_tile_coords(int tile, int m_tiles, int n_tiles, int& mt, int& nt) {
   const int group_size = TC_GROUP_M * n_tiles;
@@ -86,12 +120,14 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzling repeats every 1024 bytes: align the stage buffers.
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  TcBarriers* bars = reinterpret_cast<TcBarriers*>(smem + TC_STAGES * TC_STAGE_BYTES);
+  uint8_t* staging = smem + TC_STAGES * TC_STAGE_BYTES;  // 1024-aligned
+  TcBarriers* bars = reinterpret_cast<TcBarriers*>(staging + TC_STAGING_BYTES);
   volatile uint32_t* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -215,6 +251,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else {
     // -------------------------------------------------- epilogue warps
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    uint8_t* stg_f32 = staging + (warp - 2) * TC_STG_F32_BYTES;
+    uint8_t* stg_bf16 = staging + 4 * TC_STG_F32_BYTES + (warp - 2) * TC_STG_BF16_BYTES;
+    const Epilogue& e = p.epi;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mt, nt;
@@ -222,7 +261,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int m0 = mt * TC_BM, n0 = nt * TC_BN;
       if (!mbar_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
-      const int64_t row = m0 + q * 32 + lane;
+      const int row0 = m0 + q * 32;
+      const int64_t row = row0 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC_BN;
       for (int c = 0; c < TC_BN / 32; ++c) {
         const int col0 = n0 + c * 32;
@@ -230,11 +270,53 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tmem_ld_wait();
-        if (row < p.M) {
-          float v[32];
+        float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          epilogue_run32(p.epi, row, col0, min(32, p.N - col0), v);
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        const int n = min(32, p.N - col0);
+        if (!p.tma_store) {
+          if (row < p.M) epilogue_run32(e, row, col0, n, v);
+          continue;
+        }
+        // TMA store path: the box (32 rows x 32 columns) is clipped to the
+        // tensor by the TMA unit, so rows >= M and columns >= N are dropped.
+        if (lane == 0) bulk_wait_read0();  // previous boxes have left staging
+        __syncwarp();
+        if (e.mode == EPI_STORE) {
+          if (e.d_dtype == TPS_F32)
+            stage_f32_sw128(stg_f32, lane, v);
+          else
+            stage_bf16_sw64(stg_bf16, lane, v);
+        } else if (e.mode == EPI_ACT_FWD) {
+          if (e.d != nullptr) stage_f32_sw128(stg_f32, lane, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = act_fwd(e.act, v[i]);
+          stage_bf16_sw64(stg_bf16, lane, v);
+        } else {
+          float a[32];
+          if (row < p.M) {
+            load_run32(e.aux + row * e.ld_aux + col0, n, a);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= act_grad(e.act, a[i]);
+          if (e.d_dtype == TPS_F32)
+            stage_f32_sw128(stg_f32, lane, v);
+          else
+            stage_bf16_sw64(stg_bf16, lane, v);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (e.mode == EPI_ACT_FWD) {
+            if (e.d != nullptr) tma_store_2d(&tmD, stg_f32, col0, row0);
+            tma_store_2d(&tmD2, stg_bf16, col0, row0);
+          } else {
+            tma_store_2d(&tmD, e.d_dtype == TPS_F32 ? stg_f32 : stg_bf16, col0, row0);
+          }
+          bulk_commit();
         }
       }
       tc_fence_before();
@@ -242,6 +324,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (p.tma_store && lane == 0) bulk_wait0();  // stores complete before exit
   }
 
   __syncthreads();
@@ -283,6 +366,25 @@ static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
   return r == CUDA_SUCCESS;
 }
 
+// Output view for TMA stores: rows x cols row-major with pitch `ld`
+// elements, box 32 x 32, swizzle matching the staging layout.
+static bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int dtype) {
+  auto fn = encode_fn();
+  if (fn == nullptr || base == nullptr) return false;
+  const int es = (dtype == TPS_F32) ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (ld * es) % 16 != 0 || ld < cols) return false;
+  if (rows >= (1ll << 31) || cols >= (1ll << 31)) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * es)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype == TPS_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  dtype == TPS_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // The tensor-core path needs bf16 operands that TMA can describe: 16-byte
 // aligned base, unit stride in one dimension and a pitch that is a multiple
 // of 16 bytes.
@@ -302,8 +404,8 @@ bool gemm_tc_supported(const GemmDesc& g) {
 }
 
 template <bool A_MN, bool B_MN>
-static int launch_typed(const GemmDesc& g, const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
-                        int grid, cudaStream_t stream) {
+static int launch_typed(const GemmDesc& g, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                        const CUtensorMap& td2, const TcParams& p, int grid, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -312,7 +414,7 @@ static int launch_typed(const GemmDesc& g, const CUtensorMap& ta, const CUtensor
   });
   if (attr_err != cudaSuccess) return TPS_ERR_CUDA;
   ProfScope prof("gemm_tc", g.name, 2.0 * double(g.M) * double(g.N) * double(g.K), 0.0, stream);
-  gemm_tc_kernel<A_MN, B_MN><<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(ta, tb, p);
+  gemm_tc_kernel<A_MN, B_MN><<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(ta, tb, td, td2, p);
   note_launch();
   return cudaPeekAtLastError() == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
 }
@@ -344,12 +446,24 @@ int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   p.num_tiles = p.m_tiles * p.n_tiles;
   p.epi = g.epi;
   p.err = dev_err;
+  // TMA stores when every output can be described (else direct stores).
+  CUtensorMap td, td2;
+  memset(&td, 0, sizeof(td));
+  memset(&td2, 0, sizeof(td2));
+  bool tma = true;
+  if (g.epi.mode == EPI_ACT_FWD) {
+    if (g.epi.d != nullptr) tma = make_out_map(&td, g.epi.d, g.M, g.N, g.epi.ldd, TPS_F32);
+    tma = tma && g.epi.d2_dtype == TPS_BF16 && make_out_map(&td2, g.epi.d2, g.M, g.N, g.epi.ldd2, TPS_BF16);
+  } else {
+    tma = make_out_map(&td, g.epi.d, g.M, g.N, g.epi.ldd, g.epi.d_dtype);
+  }
+  p.tma_store = tma ? 1 : 0;
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
 
-  if (!a_mn && !b_mn) return launch_typed<false, false>(g, ta, tb, p, grid, stream);
-  if (!a_mn && b_mn) return launch_typed<false, true>(g, ta, tb, p, grid, stream);
-  if (a_mn && !b_mn) return launch_typed<true, false>(g, ta, tb, p, grid, stream);
-  return launch_typed<true, true>(g, ta, tb, p, grid, stream);
+  if (!a_mn && !b_mn) return launch_typed<false, false>(g, ta, tb, td, td2, p, grid, stream);
+  if (!a_mn && b_mn) return launch_typed<false, true>(g, ta, tb, td, td2, p, grid, stream);
+  if (a_mn && !b_mn) return launch_typed<true, false>(g, ta, tb, td, td2, p, grid, stream);
+  return launch_typed<true, true>(g, ta, tb, td, td2, p, grid, stream);
 }
 
 }  // namespace tps

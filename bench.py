@@ -201,36 +201,80 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device error {rc} in the timed region")
     launches = prof.launches
 
-    # ---- end-to-end: pinned host inputs in, results out, every step
+    # ---- end-to-end: pinned host inputs in, results out, every step.
+    # Three streams pipeline consecutive steps: host->device copies of step
+    # i+1's inputs and device->host copies of step i-1's results overlap the
+    # kernels of step i.  Inputs and copied-out results are double buffered;
+    # events order every reuse of a buffer.
     pinned = {k: v.pin_memory() for k, v in host.items()}
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for t in (mlp_out[0], mlp_out[1], mlp_out[2], mlp_out[3], ce_out[0], ce_out[2])]
+    in_bufs = [d, {k: torch.empty_like(v) for k, v in d.items()}]
+    out_names = ("Y", "dX", "dW1", "dW2", "loss", "dHidden")
+
+    def new_outs():
+        return dict(Y=torch.empty(T, dm, **f32), dX=torch.empty(T, dm, **f32), dW1=torch.empty(dm, F, **f32),
+                    dW2=torch.empty(F, dm, **f32), loss=torch.empty(T, **f32), dHidden=torch.empty(T, dm, **f32))
+    out_bufs = [new_outs(), new_outs()]
+    host_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out_bufs[0].items()}
+                for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    d2h = sum(out_bufs[0][k].numel() * out_bufs[0][k].element_size() for k in out_names)
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    ev_in_free, ev_out_free = [ev(), ev()], [ev(), ev()]
+    for e_ in ev_in_free + ev_out_free:
+        e_.record(stream)
 
-    def e2e_step():
-        for k, v in pinned.items():
-            d[k].copy_(v, non_blocking=True)
-        step(d)
-        for dst, src in zip(host_out, (mlp_out[0], mlp_out[1], mlp_out[2], mlp_out[3], ce_out[0], ce_out[2])):
-            dst.copy_(src, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        src, out, hout = in_bufs[b], out_bufs[b], host_out[b]
+        ev_mlp_in, ev_ce_in, ev_mlp_done, ev_ce_done = ev(), ev(), ev(), ev()
+        with torch.cuda.stream(s_h2d):
+            s_h2d.wait_event(ev_in_free[b])
+            for k in ("X", "W1", "W2", "GY"):
+                src[k].copy_(pinned[k], non_blocking=True)
+            ev_mlp_in.record(s_h2d)
+            for k in ("h", "W", "labels"):
+                src[k].copy_(pinned[k], non_blocking=True)
+            ev_ce_in.record(s_h2d)
+        stream.wait_event(ev_mlp_in)
+        stream.wait_event(ev_out_free[b])
+        api.mlp_fwd_bwd(src["X"], src["W1"], src["W2"], src["GY"], MLP["tp"], "gelu_tanh", "in_out",
+                        workspace=mlp_ws, out=(out["Y"], out["dX"], out["dW1"], out["dW2"]))
+        ev_mlp_done.record(stream)
+        stream.wait_event(ev_ce_in)
+        api.vocab_ce_fwd_bwd(src["h"], src["W"], src["labels"], CE["tp"], "in_out", workspace=ce_ws,
+                             out=(out["loss"], ce_out[1], out["dHidden"], ce_out[3]))
+        ev_ce_done.record(stream)
+        ev_in_free[b].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev_mlp_done)
+            for k in ("Y", "dX", "dW1", "dW2"):
+                hout[k].copy_(out[k], non_blocking=True)
+            s_d2h.wait_event(ev_ce_done)
+            for k in ("loss", "dHidden"):
+                hout[k].copy_(out[k], non_blocking=True)
+            ev_out_free[b].record(s_d2h)
 
-    e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with clk.window():
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_h2d)
+        for i in range(args.steps):
+            e2e_step(i)
+        e1.record(s_d2h)
         torch.cuda.synchronize(dev)
     time.sleep(0.2)
     clk.__exit__(None, None, None)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    assert torch.isfinite(host_out[4]).all(), "non-finite loss"
+    assert torch.isfinite(host_out[(args.steps - 1) % 2]["loss"]).all(), "non-finite loss"
+    rc = api.last_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} in the end-to-end region")
 
     # max over ranks
     if world > 1:
