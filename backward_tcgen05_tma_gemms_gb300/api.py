@@ -54,6 +54,7 @@ def library():
     lib.tps_plan_shards.argtypes = [i64, i32, ctypes.POINTER(i64)]
     lib.tps_matmul_fwd_bwd.argtypes = [P, P, P, i32, i32, P, P, P, vp]
     lib.tps_mlp_fwd_bwd.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, vp, sz, vp]
+    lib.tps_mlp_fwd_bwd_noalloc.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, vp]
     lib.tps_mlp_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     lib.tps_mlp_workspace_bytes.restype = sz
     lib.tps_vocab_ce_fwd_bwd.argtypes = [P, P, P, i32, i32, P, P, P, P, vp, sz, vp]
@@ -181,6 +182,32 @@ def mlp_fwd_bwd(X: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, GY: torch.T
                                      *[_ref(a) for a in args[4:]], ctypes.c_void_p(workspace.data_ptr()),
                                      workspace.numel() * workspace.element_size(), _stream(X.device)))
     return Y, dX, dW1, dW2
+
+
+# Size of the static scratch of tps_mlp_fwd_bwd_noalloc (TPS_MLP_NOALLOC_SCRATCH_BYTES).
+MLP_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def mlp_fwd_bwd_noalloc(X: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, GY: torch.Tensor, tp: int,
+                        act: str = "gelu_tanh", weight_layout: str = "in_out",
+                        out: Optional[Sequence[torch.Tensor]] = None):
+    """mlp_fwd_bwd without a workspace, for callers that cannot allocate
+    device memory (an allocator owned by a hosting framework, or a path that
+    must not call cudaMalloc): the library's static 32 MiB device scratch is
+    used instead.  Larger problems are rejected; calls that overlap on the
+    GPU race on the shared scratch.  Outputs still come from `out` (or are
+    allocated here by torch when `out` is None)."""
+    _parts(tp, "tp")
+    if act not in ACTS or weight_layout not in LAYOUTS:
+        raise ValueError("argument")
+    if out is None:
+        kw = dict(device=X.device, dtype=torch.float32)
+        out = (torch.empty(X.shape, **kw), torch.empty(X.shape, **kw), torch.empty(W1.shape, **kw),
+               torch.empty(W2.shape, **kw))
+    args = [_tt(t) for t in (X, W1, W2, GY, *out)]
+    _check(library().tps_mlp_fwd_bwd_noalloc(*[_ref(a) for a in args[:4]], tp, ACTS[act], LAYOUTS[weight_layout],
+                                             *[_ref(a) for a in args[4:]], _stream(X.device)))
+    return tuple(out)
 
 
 def ce_workspace_bytes(T: int, V: int, tp: int) -> int:

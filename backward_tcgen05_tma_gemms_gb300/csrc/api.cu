@@ -31,6 +31,8 @@ static int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+void set_error_detail(const char* msg) { t_detail = msg; }
+
 // ------------------------------------------------------------ device error word
 // One word per device; kernels OR TPS_DEVERR_* bits into it.
 __device__ uint32_t g_dev_err_word;

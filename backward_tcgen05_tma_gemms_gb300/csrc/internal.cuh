@@ -83,6 +83,8 @@ struct ProfScope {
   cudaStream_t stream;
 };
 void note_launch();
+// Sets the text tps_last_error_detail returns on this host thread.
+void set_error_detail(const char* msg);
 
 // array_split plan, closed form: offset(i) = i * (d / P) + min(i, d mod P).
 __host__ __device__ inline int64_t shard_offset(int64_t dim, int64_t parts, int64_t i) {

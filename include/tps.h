@@ -150,6 +150,34 @@ int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const tps_tensor*
 size_t tps_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int32_t dtype);
 
 /* ------------------------------------------------------------------------
+ * tps_mlp_fwd_bwd_noalloc -- tps_mlp_fwd_bwd for callers that cannot
+ * allocate device memory.  No counterpart on the source pages: this is a
+ * deployment variant.  Some callers cannot obtain a workspace: code running
+ * under a framework or server that owns all device memory through its own
+ * allocator and forbids side allocations, or code on a latency-critical path
+ * that must not call cudaMalloc (which synchronizes the device).  This entry
+ * point takes the same arguments minus the workspace and allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library call): its scratch is
+ * a static device array of TPS_MLP_NOALLOC_SCRATCH_BYTES (32 MiB), which
+ * every device that loads the library holds until the process exits.
+ *   - Sizes whose scratch (tps_mlp_workspace_bytes) exceeds the array are
+ *     rejected with TPS_ERR_WORKSPACE before anything is launched; for bf16
+ *     operands that is T x F > 4,194,304.
+ *   - The first call on a device resolves the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (every byte is written before it is read, so nothing needs
+ *     clearing).  Calls that overlap on the GPU race on the array: the
+ *     caller must serialise them (one stream, or events between streams).
+ * Results are the same as tps_mlp_fwd_bwd's for the same inputs.
+ * ---------------------------------------------------------------------- */
+#define TPS_MLP_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int tps_mlp_fwd_bwd_noalloc(const tps_tensor* X, const tps_tensor* W1, const tps_tensor* W2, const tps_tensor* GY,
+                            int32_t tp, int32_t act, int32_t weight_layout, const tps_tensor* Y,
+                            const tps_tensor* dX, const tps_tensor* dW1, const tps_tensor* dW2, void* cuda_stream);
+
+/* ------------------------------------------------------------------------
  * tps_vocab_ce_fwd_bwd -- cross-entropy over a vocabulary split into `tp`
  * contiguous shards (array_split of V), forward and backward
  * ([MC] "04 / VOCABULARY SHARDS"; single supervised position per token, no
