@@ -61,6 +61,7 @@ def library():
     lib.tps_ce_workspace_bytes.argtypes = [i64, i64, i32]
     lib.tps_ce_workspace_bytes.restype = sz
     lib.tps_last_device_error.argtypes = [vp]
+    lib.tps_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.tps_strerror.argtypes = [ctypes.c_int]
     lib.tps_strerror.restype = ctypes.c_char_p
     lib.tps_last_error_detail.restype = ctypes.c_char_p
@@ -240,6 +241,12 @@ def vocab_ce_fwd_bwd(h: torch.Tensor, Whead: torch.Tensor, labels: torch.Tensor,
                                           *[_ref(a) for a in args[3:]], ctypes.c_void_p(workspace.data_ptr()),
                                           workspace.numel() * workspace.element_size(), _stream(h.device)))
     return loss, dlog, dh, owner
+
+
+def selftest_wait_timeout(limit_ns: int = 50_000_000) -> None:
+    """Enqueue the bounded-wait self test (a wait nothing satisfies, given up
+    after `limit_ns`); read the outcome with last_device_error()."""
+    _check(library().tps_selftest_wait_timeout(int(limit_ns), _stream(None)))
 
 
 def last_device_error(device=None) -> int:

@@ -53,6 +53,8 @@ static uint32_t* dev_err_ptr() {
   return g_err_addr[dev];
 }
 
+uint32_t* device_error_word() { return dev_err_ptr(); }
+
 // ------------------------------------------------------------ profiler
 struct ProfRecord {
   std::string name;  // "kind:label"

@@ -336,6 +336,309 @@ __global__ void __launch_bounds__(CE_THREADS) ce_cluster_reg_kernel(const CePara
   cluster_sync();  // no CTA leaves while another may still read its `stat`
 }
 
+// ------------------------------------------------------------ persistent path
+// Persistent clusters fed by a ring of bulk copies.  Cluster c handles
+// tokens c, c + C, c + 2C, ...; CTA r of the cluster owns shard r.  Thread
+// 0 keeps CEP_NBUF bulk copies (cp.async.bulk, one token's shard each) in
+// flight, so HBM reads continue while the CTA reduces, exchanges and writes
+// the previous token.  The shard goes from shared memory to registers once;
+// the exponentials e_j = exp(z_j - m_r) computed for s_r are reused for the
+// gradient, which is e_j * exp(m_r - m) / s - 1[j = y].
+constexpr int CEP_THREADS = 512;
+constexpr int CEP_NBUF = 3;
+constexpr int CEP_VPT4 = 8;                                  // float4 slots per thread
+constexpr int CEP_BUF_FLOATS = CEP_THREADS * 4 * CEP_VPT4;  // 16384 floats = 64 KB
+constexpr int CEP_CHUNK_BYTES = 16384;                       // bulk copy granule
+
+struct CepGeom {  // one rank's slice, identical for every token
+  int64_t beg, end;  // shard columns [beg, end)
+  int64_t a0;        // beg rounded down to 4: first column copied to smem
+  int64_t a1;        // end rounded down to 4: end of the bulk copy
+  int64_t tail0;     // first column loaded from global by threads (< 4 of them)
+};
+
+__device__ __forceinline__ CepGeom cep_geom(int64_t V, int32_t parts, int64_t r) {
+  CepGeom g;
+  g.beg = shard_offset(V, parts, r);
+  g.end = shard_offset(V, parts, r + 1);
+  g.a0 = g.beg & ~int64_t(3);
+  g.a1 = g.end & ~int64_t(3);
+  if (g.a1 < g.a0) g.a1 = g.a0;
+  g.tail0 = g.beg > g.a1 ? g.beg : g.a1;
+  return g;
+}
+
+__device__ __forceinline__ void cep_issue(const CeParams& p, const CepGeom& g, int64_t t, float* buf,
+                                          uint64_t* bar) {
+  const uint32_t bytes = static_cast<uint32_t>((g.a1 - g.a0) * 4);
+  mbar_expect_tx(bar, bytes);
+  const char* src = reinterpret_cast<const char*>(p.z + t * p.ldz + g.a0);
+  char* dst = reinterpret_cast<char*>(buf);
+  for (uint32_t off = 0; off < bytes; off += CEP_CHUNK_BYTES) {
+    const uint32_t n = bytes - off < CEP_CHUNK_BYTES ? bytes - off : CEP_CHUNK_BYTES;
+    bulk_load(dst + off, src + off, n, bar);
+  }
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// e^{x - m} as 2^{x log2(e) - m log2(e)}: one FMA and one ex2.
+__device__ __forceinline__ float exp_shift(float x, float m_l2e) { return ex2_approx(fmaf(x, kLog2e, -m_l2e)); }
+
+// Combine per-thread (max, sum of e^{z - max}) pairs over the block: first
+// the maximum, then the sums rescaled to it.  One __syncthreads: every warp
+// then reduces the per-warp partials itself.  `red` holds 64 floats and must
+// not be reused before every thread has returned (callers alternate two).
+// Returns the block's (m, s); an empty block gives (-inf, 0).
+__device__ __forceinline__ float2 block_ms(float mt, float st, float* red) {
+  float m = mt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sl = (mt == -INFINITY) ? 0.0f : st * ex2_approx((mt - m) * kLog2e);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (l == 0) {
+    red[w] = m;
+    red[32 + w] = sl;
+  }
+  __syncthreads();
+  const float m2 = (l < nw) ? red[l] : -INFINITY;
+  float M = m2;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float s2 = (m2 == -INFINITY) ? 0.0f : red[32 + l] * ex2_approx((m2 - M) * kLog2e);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+  return make_float2(M, s2);
+}
+
+// One token's shard in registers: e_j = exp(z_j - mt) with the thread's own
+// maximum mt (0 for padding), and the CTA's (m_r, s_r).
+struct CepTok {
+  float4 v[CEP_VPT4];
+  float tail;
+  float mt;
+  float m_r, s_r;
+};
+
+struct CepCtx {  // per-CTA constants of the persistent CE kernel
+  int64_t c, C, n_iter;
+  CepGeom g;
+  int h0, h1, ntail, q_first, q_last;
+  bool has_body, vec_store;
+  uint32_t r;
+};
+
+struct CepSmem {
+  uint64_t full[CEP_NBUF];
+  float red[2][64];                     // block_ms partials, alternating per token
+  __align__(8) float stat_in[2][8][2];  // [token parity][rank] (m_q, s_q), written by rank q
+  uint32_t abort_flag;
+};
+
+// Load token i (ring buffer i % NBUF) into registers, compute the
+// statistics, and refill the buffer with token i + NBUF.
+__device__ __forceinline__ void cep_load_stats(const CeParams& p, const CepCtx& x, int64_t i, CepTok& k, float* ring,
+                                               CepSmem& sm) {
+  const int tid = threadIdx.x;
+  const int64_t t = x.c + i * x.C;
+  const int b = static_cast<int>(i % CEP_NBUF);
+  float tail_v = -INFINITY;
+  if (tid < x.ntail) tail_v = __ldcs(p.z + t * p.ldz + x.g.tail0 + tid);
+  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  if (x.has_body) {
+    mbar_wait(&sm.full[b], static_cast<uint32_t>((i / CEP_NBUF) & 1), &sm.abort_flag, p.err);
+    const float4* buf4 = reinterpret_cast<const float4*>(ring + b * CEP_BUF_FLOATS);
+#pragma unroll
+    for (int j = 0; j < CEP_VPT4; ++j) {
+      const int q = tid + j * CEP_THREADS;
+      float4 w = (q <= x.q_last) ? buf4[q] : ninf;
+      if (q == x.q_first) {  // the slot holding the shard's first element
+        const int e0 = 4 * q;
+        if (e0 + 0 < x.h0) w.x = -INFINITY;
+        if (e0 + 1 < x.h0) w.y = -INFINITY;
+        if (e0 + 2 < x.h0) w.z = -INFINITY;
+        if (e0 + 3 < x.h0) w.w = -INFINITY;
+      }
+      k.v[j] = w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < CEP_VPT4; ++j) k.v[j] = ninf;
+  }
+  float mt = tail_v;
+#pragma unroll
+  for (int j = 0; j < CEP_VPT4; ++j) mt = fmaxf(fmaxf(mt, fmaxf(k.v[j].x, k.v[j].y)), fmaxf(k.v[j].z, k.v[j].w));
+  float st = 0.0f;
+  if (mt != -INFINITY) {
+    const float ml = mt * kLog2e;
+#pragma unroll
+    for (int j = 0; j < CEP_VPT4; ++j) {
+      k.v[j].x = exp_shift(k.v[j].x, ml);
+      k.v[j].y = exp_shift(k.v[j].y, ml);
+      k.v[j].z = exp_shift(k.v[j].z, ml);
+      k.v[j].w = exp_shift(k.v[j].w, ml);
+      st += (k.v[j].x + k.v[j].y) + (k.v[j].z + k.v[j].w);
+    }
+    k.tail = exp_shift(tail_v, ml);
+    st += k.tail;
+  } else {
+#pragma unroll
+    for (int j = 0; j < CEP_VPT4; ++j) k.v[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    k.tail = 0.0f;
+  }
+  k.mt = mt;
+  // block_ms's barrier also certifies that buffer b has been read by all
+  const float2 ms = block_ms(mt, st, sm.red[i & 1]);
+  k.m_r = ms.x;
+  k.s_r = ms.y;
+  if (tid == 0 && x.has_body && i + CEP_NBUF < x.n_iter) {
+    fence_async_smem();
+    cep_issue(p, x.g, x.c + (i + CEP_NBUF) * x.C, ring + b * CEP_BUF_FLOATS, &sm.full[b]);
+  }
+}
+
+// Push the CTA's (m_r, s_r) for token parity `par` into every rank's
+// stat_in[par][r] (remote shared-memory stores), then arrive on the
+// cluster barrier; the stores are ordered before the arrive by a fence.
+__device__ __forceinline__ void cep_publish(const CeParams& p, const CepCtx& x, int par, const CepTok& k,
+                                            CepSmem& sm) {
+  if (threadIdx.x < p.parts) {
+    st_cluster_f32x2(cluster_map(smem_u32(&sm.stat_in[par][x.r][0]), threadIdx.x), k.m_r, k.s_r);
+    fence_cluster();
+  }
+  cluster_arrive_relaxed();
+}
+
+// One pipeline step: statistics of token i+1 (overlapping the barrier of
+// token i), then the combine, loss and gradient of token i.
+template <typename TOut>
+__device__ __forceinline__ void cep_step(const CeParams& p, const CepCtx& x, int64_t i, CepTok& cur, CepTok& nxt,
+                                         float* ring, CepSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t t = x.c + i * x.C;
+  const int64_t y = load_label(p, t);
+  const bool valid = (y >= 0 && y < p.V);
+  const bool owner = valid && y >= x.g.beg && y < x.g.end;
+  float zy = 0.0f;
+  if (tid == 0 && owner) zy = p.z[t * p.ldz + y];
+  const bool has_next = i + 1 < x.n_iter;
+  if (has_next) cep_load_stats(p, x, i + 1, nxt, ring, sm);
+  cluster_wait();  // every rank's statistics of token t are in stat_in
+  const int par = static_cast<int>(i & 1);
+  // every warp combines the ranks' (m_q, s_q) itself: no block barrier
+  const float mq = (lane < p.parts) ? sm.stat_in[par][lane][0] : -INFINITY;
+  const float sq = (lane < p.parts) ? sm.stat_in[par][lane][1] : 0.0f;
+  float m = mq;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = (mq == -INFINITY) ? 0.0f : sq * ex2_approx((mq - m) * kLog2e);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (tid == 0) {
+    if (owner) {
+      p.loss[t] = logf(s) + m - zy;
+      if (p.owner) p.owner[t] = static_cast<int32_t>(x.r);
+    } else if (!valid && x.r == 0) {
+      p.loss[t] = __int_as_float(0x7fc00000);  // NaN
+      if (p.owner) p.owner[t] = -1;
+      atomicOr(p.err, TPS_DEVERR_LABEL);
+    }
+  }
+  // dlogits_j = e^{z_j - m}/s - 1[j = y] = e_j * e^{mt - m}/s - 1[j = y]
+  const float f = (cur.mt != -INFINITY) ? ex2_approx((cur.mt - m) * kLog2e) / s : 0.0f;
+  const int yl = owner ? static_cast<int>(y - x.g.a0) : -1;  // smem-local index of the label
+  const int qy = (yl >= 0 && yl < x.h1) ? (yl >> 2) : -1;
+  TOut* gbase = static_cast<TOut*>(p.dlog) + t * p.ldg + x.g.a0;  // element 0 = smem index 0
+  if (tid < x.ntail) {
+    const int il = x.h1 + tid;  // tail elements follow the body
+    store_grad(gbase + il, cur.tail * f - (il == yl ? 1.0f : 0.0f));
+  }
+#pragma unroll
+  for (int j = 0; j < CEP_VPT4; ++j) {
+    const int q = tid + j * CEP_THREADS;
+    if (q > x.q_last) continue;
+    float g0 = cur.v[j].x * f, g1 = cur.v[j].y * f, g2 = cur.v[j].z * f, g3 = cur.v[j].w * f;
+    if (q == qy) {
+      const int cpt = yl & 3;
+      g0 -= (cpt == 0) ? 1.0f : 0.0f;
+      g1 -= (cpt == 1) ? 1.0f : 0.0f;
+      g2 -= (cpt == 2) ? 1.0f : 0.0f;
+      g3 -= (cpt == 3) ? 1.0f : 0.0f;
+    }
+    const int i0 = 4 * q;
+    if (x.vec_store && q != x.q_first) {
+      if constexpr (sizeof(TOut) == 2) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(g0, g1), bb = __floats2bfloat162_rn(g2, g3);
+        uint2 w;
+        w.x = *reinterpret_cast<uint32_t*>(&a);
+        w.y = *reinterpret_cast<uint32_t*>(&bb);
+        __stcs(reinterpret_cast<uint2*>(gbase + i0), w);
+      } else {
+        __stcs(reinterpret_cast<float4*>(gbase + i0), make_float4(g0, g1, g2, g3));
+      }
+    } else {
+      if (i0 + 0 >= x.h0) store_grad(gbase + i0, g0);
+      if (i0 + 1 >= x.h0) store_grad(gbase + i0 + 1, g1);
+      if (i0 + 2 >= x.h0) store_grad(gbase + i0 + 2, g2);
+      if (i0 + 3 >= x.h0) store_grad(gbase + i0 + 3, g3);
+    }
+  }
+  // Every rank read stat_in[par ^ 1] (token i-1) before arriving at the
+  // barrier just waited on, so the next token's values may land there now.
+  if (has_next) cep_publish(p, x, par ^ 1, nxt, sm);
+}
+
+template <typename TOut>
+__global__ void __launch_bounds__(CEP_THREADS, 1) ce_persistent_kernel(const CeParams p) {
+  extern __shared__ float4 cep_smem4[];
+  float* ring = reinterpret_cast<float*>(cep_smem4);
+  __shared__ CepSmem sm;
+
+  CepCtx x;
+  x.r = cluster_ctarank();
+  x.c = blockIdx.y;
+  x.C = gridDim.y;
+  x.g = cep_geom(p.V, p.parts, x.r);
+  x.h0 = static_cast<int>(x.g.beg - x.g.a0);
+  x.h1 = static_cast<int>(x.g.tail0 - x.g.a0);
+  x.ntail = static_cast<int>(x.g.end - x.g.tail0);
+  x.has_body = x.g.a1 > x.g.a0;
+  x.q_first = x.has_body ? (x.h0 >> 2) : -1;
+  x.q_last = x.has_body ? ((x.h1 - 1) >> 2) : -1;
+  x.n_iter = (p.T - x.c + x.C - 1) / x.C;
+  x.vec_store = ((p.ldg & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.dlog) & (4 * sizeof(TOut) - 1)) == 0);
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    for (int b = 0; b < CEP_NBUF; ++b) mbar_init(&sm.full[b], 1);
+    sm.abort_flag = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  cluster_sync();  // every CTA of the cluster is running before any DSMEM access
+  if (tid == 0 && x.has_body)
+    for (int64_t i = 0; i < CEP_NBUF && i < x.n_iter; ++i)
+      cep_issue(p, x.g, x.c + i * x.C, ring + i * CEP_BUF_FLOATS, &sm.full[i]);
+
+  CepTok A, B;  // two register sets, alternating roles without copies
+  if (x.n_iter > 0) {
+    cep_load_stats(p, x, 0, A, ring, sm);
+    cep_publish(p, x, 0, A, sm);  // phase 0
+  }
+  for (int64_t i = 0; i < x.n_iter; i += 2) {
+    cep_step<TOut>(p, x, i, A, B, ring, sm);
+    if (i + 1 < x.n_iter) cep_step<TOut>(p, x, i + 1, B, A, ring, sm);
+  }
+  // Every issued copy was waited for above; after a timed-out wait, make
+  // sure none is still landing before shared memory is released.
+  if (tid == 0 && x.has_body)
+    for (int64_t j = x.n_iter > CEP_NBUF ? x.n_iter - CEP_NBUF : 0; j < x.n_iter; ++j)
+      mbar_wait_drain(&sm.full[j % CEP_NBUF], static_cast<uint32_t>((j / CEP_NBUF) & 1), p.err);
+  cluster_sync();  // no CTA leaves while another may still write into its stat_in
+}
+
 // ------------------------------------------------------------ two-pass path
 // Grid (parts, T): rank r's (m_r, s_r) for token t with an online max/sum
 // (one read of the shard), the label's logit and owner.
@@ -453,8 +756,27 @@ static int launch_cluster(const CeParams& p, cudaStream_t stream) {
   const double bytes = double(p.T) * double(p.V) * (4.0 + sizeof(TOut)) + double(p.T) * (8.0 + 4.0);
   ProfScope prof("ce_cluster", "ce_core", 0.0, bytes, stream);
   cudaError_t e;
-  // body capacity of the register kernel: CE_THREADS * 4 * VPT4 elements
-  if (max_len <= CE_THREADS * 4 * 2) {
+  const bool z_aligned = ((reinterpret_cast<uintptr_t>(p.z) & 15u) == 0) && ((p.ldz & 3) == 0);
+  if (z_aligned && max_len + 3 <= CEP_BUF_FLOATS) {
+    // persistent clusters, as many as can be resident at once
+    const size_t smem = size_t(CEP_NBUF) * CEP_BUF_FLOATS * sizeof(float);
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [smem] {
+      attr_err = cudaFuncSetAttribute(ce_persistent_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem));
+    });
+    if (attr_err != cudaSuccess) return TPS_ERR_CUDA;
+    cfg.blockDim = dim3(CEP_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int clusters = 0;
+    cfg.gridDim = dim3(static_cast<unsigned>(p.parts), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&clusters, ce_persistent_kernel<TOut>, &cfg) != cudaSuccess || clusters < 1)
+      clusters = 1;
+    const int64_t C = p.T < clusters ? p.T : clusters;
+    cfg.gridDim = dim3(static_cast<unsigned>(p.parts), static_cast<unsigned>(C), 1);
+    e = cudaLaunchKernelEx(&cfg, ce_persistent_kernel<TOut>, p);
+  } else if (max_len <= CE_THREADS * 4 * 2) {
     e = launch_cluster_reg<TOut, 2>(p, cfg);
   } else if (max_len <= CE_THREADS * 4 * 4) {
     e = launch_cluster_reg<TOut, 4>(p, cfg);

@@ -105,18 +105,6 @@ __device__ __forceinline__ void tc_tile_coords(int tile, int m_tiles, int n_tile
   nt = in_group / gm;
 }
 
-// Wait without honouring the abort flag (used to drain in-flight work
-// before exit); still bounded in time.
-__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* err) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, TPS_DEVERR_TIMEOUT);
-      return;
-    }
-  }
-}
-
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -264,11 +252,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int row0 = m0 + q * 32;
       const int64_t row = row0 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC_BN;
+      // act-bwd: the pre-activation of the next 32 columns is loaded while
+      // the current ones are processed
+      float a_next[32];
+      const bool bwd = p.tma_store && e.mode == EPI_ACT_BWD;
+      if (bwd) {
+        if (row < p.M) {
+          load_run32(e.aux + row * e.ld_aux + n0, min(32, p.N - n0), a_next);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a_next[i] = 0.0f;
+        }
+      }
       for (int c = 0; c < TC_BN / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= p.N) break;  // warp-uniform
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
+        float a[32];
+        if (bwd) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = a_next[i];
+          if (row < p.M && col0 + 32 < p.N && c + 1 < TC_BN / 32)
+            load_run32(e.aux + row * e.ld_aux + col0 + 32, min(32, p.N - col0 - 32), a_next);
+        }
         tmem_ld_wait();
         float v[32];
 #pragma unroll
@@ -293,13 +300,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int i = 0; i < 32; ++i) v[i] = act_fwd(e.act, v[i]);
           stage_bf16_sw64(stg_bf16, lane, v);
         } else {
-          float a[32];
-          if (row < p.M) {
-            load_run32(e.aux + row * e.ld_aux + col0, n, a);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = 0.0f;
-          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= act_grad(e.act, a[i]);
           if (e.d_dtype == TPS_F32)

@@ -83,6 +83,8 @@ struct ProfScope {
   cudaStream_t stream;
 };
 void note_launch();
+// Device address of the current device's error word (nullptr on failure).
+uint32_t* device_error_word();
 // Sets the text tps_last_error_detail returns on this host thread.
 void set_error_detail(const char* msg);
 
@@ -93,16 +95,20 @@ __host__ __device__ inline int64_t shard_offset(int64_t dim, int64_t parts, int6
 }
 
 // ------------------------------------------------------------ activations
-// GELU (erf form) x * Phi(x); GELU tanh approximation
-// 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))); tanh.  Derivatives from
-// differentiating those definitions.  CUDA's erff / tanhf / expf are called,
-// not re-derived.
+// GELU (erf form) x * Phi(x), with CUDA's erff; tanh with CUDA's tanhf.
+// GELU tanh approximation 0.5 x (1 + tanh(z)), z = sqrt(2/pi) (x + 0.044715
+// x^3), evaluated through the identity 0.5 (1 + tanh(z)) = 1 / (1 + e^{-2z})
+// (one exponential and one division instead of a tanh); the exponent is
+// clamped at 80, where the sigmoid is already 0 in fp32.  Derivatives are
+// those of the definitions: for the tanh form, with s = 1/(1 + e^{-2z}),
+// d/dx = s + 2 x s (1 - s) sqrt(2/pi) (1 + 3 * 0.044715 x^2).
+__device__ __forceinline__ float gelu_tanh_sigmoid(float x) {
+  const float z = 0.79788456080286536f * (x + 0.044715f * x * x * x);
+  return __fdividef(1.0f, 1.0f + __expf(fminf(-2.0f * z, 80.0f)));
+}
 __device__ __forceinline__ float act_fwd(int act, float x) {
   if (act == TPS_ACT_GELU_ERF) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
-  if (act == TPS_ACT_GELU_TANH) {
-    const float u = tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x));
-    return 0.5f * x * (1.0f + u);
-  }
+  if (act == TPS_ACT_GELU_TANH) return x * gelu_tanh_sigmoid(x);
   return tanhf(x);
 }
 __device__ __forceinline__ float act_grad(int act, float x) {
@@ -112,9 +118,8 @@ __device__ __forceinline__ float act_grad(int act, float x) {
     return cdf + x * pdf;
   }
   if (act == TPS_ACT_GELU_TANH) {
-    const float c = 0.79788456080286536f;
-    const float u = tanhf(c * (x + 0.044715f * x * x * x));
-    return 0.5f * (1.0f + u) + 0.5f * x * (1.0f - u * u) * c * (1.0f + 3.0f * 0.044715f * x * x);
+    const float s = gelu_tanh_sigmoid(x);
+    return s + 2.0f * x * s * (1.0f - s) * 0.79788456080286536f * (1.0f + 3.0f * 0.044715f * x * x);
   }
   const float h = tanhf(x);
   return 1.0f - h * h;

@@ -40,8 +40,54 @@ STEP_FLOPS = MLP_FLOPS + CE_GEMM_FLOPS
 # CE core (per-shard stats, combine, dlogits): one fp32 read of the logits,
 # one bf16 write of dlogits, the label (int64) and the loss (fp32) per token.
 CE_CORE_BYTES_PER_TOKEN = CE["V"] * (4 + 2) + 8 + 4
+# Algorithmic DRAM bytes of the step's eight GEMM launches, averaged per
+# launch: every operand read once and every output written once (bf16
+# operands, fp32 results; the column GEMM also writes the fp32
+# pre-activation, the dZ GEMM also reads it).
+def _gemm_algo_bytes():
+    T, d, F, V = MLP["T"], MLP["d"], MLP["F"], CE["V"]
+    b = 0
+    b += 2 * T * d + 2 * d * F + 4 * T * F + 2 * T * F      # fc1: X, W1 -> Hp (f32), Ha (bf16)
+    b += 2 * T * F + 2 * F * d + 4 * T * d                  # fc2: Ha, W2 -> Y
+    b += 2 * T * d + 2 * F * d + 4 * T * F + 2 * T * F      # dh: GY, W2, Hp -> dZ (bf16)
+    b += 2 * T * F + 2 * T * d + 4 * F * d                  # dW2: Ha, GY -> dW2
+    b += 2 * T * d + 2 * T * F + 4 * d * F                  # dW1: X, dZ -> dW1
+    b += 2 * T * F + 2 * d * F + 4 * T * d                  # dX: dZ, W1 -> dX
+    b += 2 * T * d + 2 * d * V + 4 * T * V                  # logits: h, W -> z (f32)
+    b += 2 * T * V + 2 * d * V + 4 * T * d                  # dHidden: dlogits, W -> dh
+    return b / 8
+
+
+GEMM_ALGO_BYTES_PER_LAUNCH = _gemm_algo_bytes()
 WORKLOAD = ("TP-MLP fwd+bwd (T=8192, d=4096, F=14336, tp=8, tanh-GELU) + vocab-parallel CE fwd+bwd "
             "(T=8192, d=4096, V=128256, tp=8), bf16 operands / fp32 accumulation")
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+GEMM_SOURCES = ["gemm_tc.cu", "ptx.cuh", "epilogue.cuh", "internal.cuh"]
+
+
+def kernel_source_hash(names):
+    """sha256 over the CUDA sources a kernel is built from, to tell whether
+    recorded ncu counters still describe the current kernel."""
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "backward_tcgen05_tma_gemms_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel, sources):
+    """DRAM bytes per launch recorded by ncu for `kernel`, or None when no
+    record exists or the kernel's sources changed since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("source_sha256") != kernel_source_hash(sources):
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def load_peaks():
@@ -140,6 +186,14 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over all ranks of the default process
+    group (the slowest replica sets the job's time)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -278,9 +332,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # max over ranks
     if world > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+        ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
     return dict(ms=ms, e2e_ms=e2e_ms, prof=prof.summary, launches=launches, clocks=clk.summary(), h2d=h2d, d2h=d2h,
                 host=host)
 
@@ -377,7 +429,9 @@ def main():
                    "l2": "no flush; the per-step working set (~9.7 GB) is far larger than the 129 MB L2"},
         "roofline": {"kernel": "gemm_tc (tcgen05 bf16 GEMM, all launches of the step)", "bound": "tensor",
                      "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
-                     "frac": (achieved / bf16_peak) if achieved and bf16_peak else None, "traffic": None,
+                     "frac": (achieved / bf16_peak) if achieved and bf16_peak else None,
+                     "traffic": recorded_traffic("gemm_tc", GEMM_SOURCES),
+                     "algorithmic_bytes_per_launch": GEMM_ALGO_BYTES_PER_LAUNCH,
                      "peak_source": f"{peak_src} bf16 (sustained)", "launches_per_step": tc_launches / args.steps},
         "mlp": {"ms_per_step": mlp_ms, "tflops": MLP_FLOPS / (mlp_ms * 1e-3) / 1e12 if mlp_ms else None},
         "ce": {"tokens_per_s": CE["T"] * world / (r["ms"] * 1e-3),

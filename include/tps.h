@@ -212,6 +212,16 @@ size_t tps_ce_workspace_bytes(int64_t T, int64_t V, int32_t tp);
  * ---------------------------------------------------------------------- */
 int tps_last_device_error(void* cuda_stream);
 
+/* ------------------------------------------------------------------------
+ * tps_selftest_wait_timeout -- failure-detection self test.  Launches one
+ * thread that waits on a barrier nothing arrives on, with the same bounded
+ * wait the pipelined kernels use, giving up after `limit_ns` (1 ns .. 2 s).
+ * The kernel then returns normally and the next tps_last_device_error()
+ * reports TPS_ERR_TIMEOUT; the CUDA context stays usable.  Returns
+ * TPS_ERR_ARG for a limit outside that range.
+ * ---------------------------------------------------------------------- */
+int tps_selftest_wait_timeout(uint64_t limit_ns, void* cuda_stream);
+
 /* Static description of a status code. */
 const char* tps_strerror(int code);
 

@@ -59,6 +59,15 @@ def test_fp32_cluster_path(orc, tp):
     check(orc, h, W, labels, tp, False, what=f"tp{tp}")
 
 
+@pytest.mark.parametrize("tp,V,T", [(3, 1001, 23), (2, 40000, 9), (8, 1000, 300), (5, 16380 * 5, 11)])
+def test_fp32_cluster_variants(orc, tp, V, T):
+    """Logits rows not 16-byte aligned (register kernel), shards above the
+    register capacity (shared-memory kernel), many tokens per persistent
+    cluster (ring wrap-around), shards at the persistent kernel's limit."""
+    h, W, labels = inputs.ce_case(tp * 31 + V, T, 12, V, torch.float32, w_std=0.5)
+    check(orc, h, W, labels, tp, False, what=f"tp{tp} V{V} T{T}")
+
+
 @pytest.mark.parametrize("tp,V", [(9, 1000), (16, 5003), (1, 100000)])
 def test_fp32_two_pass_path(orc, tp, V):
     """More ranks than a cluster holds, or a shard larger than shared memory."""
