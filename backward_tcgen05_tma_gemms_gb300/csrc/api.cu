@@ -434,10 +434,28 @@ extern "C" int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const 
   return TPS_OK;
 }
 
+// CE workspace: logits (T x V fp32) | per-shard stats of the two-pass path
+// (T x tp x 2) | label logits (T) | per-tile stats (T x ceil(V/256) x 4) |
+// combined (m, 1/s) per token (T x 2).
+struct CeWs {
+  size_t z, stats, zy, tiles, ms, total;
+};
+static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp) {
+  const size_t t = static_cast<size_t>(T);
+  const size_t n_tiles = static_cast<size_t>((V + kTileN - 1) / kTileN);
+  CeWs w;
+  w.z = 0;
+  w.stats = w.z + align256(t * static_cast<size_t>(V) * 4);
+  w.zy = w.stats + align256(t * static_cast<size_t>(tp) * 2 * 4);
+  w.tiles = w.zy + align256(t * 4);
+  w.ms = w.tiles + align256(t * n_tiles * 4 * 4);
+  w.total = w.ms + align256(t * 2 * 4);
+  return w;
+}
+
 extern "C" size_t tps_ce_workspace_bytes(int64_t T, int64_t V, int32_t tp) {
   if (T < 0 || V < 0 || tp < 1) return 0;
-  const size_t t = static_cast<size_t>(T);
-  return align256(t * static_cast<size_t>(V) * 4) + align256(t * static_cast<size_t>(tp) * 2 * 4) + align256(t * 4);
+  return ce_ws_layout(T, V, tp).total;
 }
 
 extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead, const tps_tensor* labels,
@@ -489,21 +507,33 @@ extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead
   if (T == 0) return TPS_OK;
 
   char* ws = static_cast<char*>(workspace);
-  float* z = reinterpret_cast<float*>(ws);
-  float* stats = reinterpret_cast<float*>(ws + align256(size_t(T) * size_t(V) * 4));
-  float* zy = reinterpret_cast<float*>(ws + align256(size_t(T) * size_t(V) * 4) + align256(size_t(T) * tp * 2 * 4));
+  const CeWs lay = ce_ws_layout(T, V, tp);
+  float* z = reinterpret_cast<float*>(ws + lay.z);
+  float* stats = reinterpret_cast<float*>(ws + lay.stats);
+  float* zy = reinterpret_cast<float*>(ws + lay.zy);
+  float* tile_stats = reinterpret_cast<float*>(ws + lay.tiles);
+  float* ms = reinterpret_cast<float*>(ws + lay.ms);
+  const int64_t n_tiles = (V + kTileN - 1) / kTileN;
   int64_t w_in, w_out;
   weight_strides(w, weight_layout, &w_in, &w_out);  // W(dd, v)
 
-  {  // z = h Whead: vocabulary shards are column ranges of z
-    GemmDesc g;
-    g.name = "ce_logits";
-    g.M = T; g.N = V; g.K = d; g.in_dtype = dt;
-    g.a = hm.data; g.a_sm = hm.sr; g.a_sk = hm.sc;
-    g.b = w.data; g.b_sk = w_in; g.b_sn = w_out;
-    g.epi.d = z; g.epi.d_dtype = TPS_F32;
-    if ((rc = run_gemm(g, V, 1, s))) return rc;
+  // z = h Whead: vocabulary shards are column ranges of z.  On the tensor
+  // cores (shards of at least one 256-column tile) the epilogue also leaves
+  // each shard's partial softmax statistics per tile.
+  GemmDesc g;
+  g.name = "ce_logits";
+  g.M = T; g.N = V; g.K = d; g.in_dtype = dt;
+  g.a = hm.data; g.a_sm = hm.sr; g.a_sk = hm.sc;
+  g.b = w.data; g.b_sk = w_in; g.b_sn = w_out;
+  g.epi.d = z; g.epi.d_dtype = TPS_F32; g.epi.ldd = V;
+  const bool fused = gemm_tc_supported(g) && ce_tile_stats_supported(V, tp);
+  if (fused) {
+    g.epi.mode = EPI_CE_STATS;
+    g.epi.stats = tile_stats;
+    g.epi.n_tiles = n_tiles;
+    g.epi.ce_parts = tp;
   }
+  if ((rc = run_gemm(g, V, 1, s))) return rc;
   {
     CeDesc c;
     c.T = T; c.V = V; c.parts = tp;
@@ -514,7 +544,7 @@ extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead
     c.owner = own; c.stats = stats; c.zy = zy;
     uint32_t* err = dev_err_ptr();
     if (err == nullptr) return fail(TPS_ERR_CUDA, "cannot resolve the device error word");
-    rc = launch_ce(c, err, s, nullptr);
+    rc = fused ? launch_ce_from_tile_stats(c, tile_stats, n_tiles, ms, err, s) : launch_ce(c, err, s, nullptr);
     if (rc) return fail(rc, "ce launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   }
   {  // dHidden = sum_r dlogits_r Whead_r^T: rank sum in the K loop

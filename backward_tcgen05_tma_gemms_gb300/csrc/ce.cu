@@ -385,6 +385,16 @@ constexpr float kLog2e = 1.4426950408889634f;
 // e^{x - m} as 2^{x log2(e) - m log2(e)}: one FMA and one ex2.
 __device__ __forceinline__ float exp_shift(float x, float m_l2e) { return ex2_approx(fmaf(x, kLog2e, -m_l2e)); }
 
+// (m, s) <- statistics of the union of (m, s) and (m2, s2), each a (max,
+// sum of e^{z - max}) pair; (-inf, 0) is the empty set.
+__device__ __forceinline__ void ms_combine_acc(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  s = (m == -INFINITY ? 0.0f : s * ex2_approx((m - M) * kLog2e)) +
+      (m2 == -INFINITY ? 0.0f : s2 * ex2_approx((m2 - M) * kLog2e));
+  m = M;
+}
+
 // Combine per-thread (max, sum of e^{z - max}) pairs over the block: first
 // the maximum, then the sums rescaled to it.  One __syncthreads: every warp
 // then reduces the per-warp partials itself.  `red` holds 64 floats and must
@@ -724,6 +734,159 @@ __global__ void __launch_bounds__(256) ce_grad_kernel(const CeParams p) {
   TOut* grow = static_cast<TOut*>(p.dlog) + t * p.ldg;
   for (int64_t j = c0 + threadIdx.x; j < c1; j += blockDim.x)
     store_grad(grow + j, __expf(zrow[j] - m) * inv_s - (j == y ? 1.0f : 0.0f));
+}
+
+// ------------------------------------------------------------ from tile statistics
+// The logits GEMM's epilogue left, per (token, 256-column tile), the
+// statistics of the tile's columns split at the shard boundary.  Shard r's
+// (m_r, s_r) combines the tiles whose first column lies in r (their first
+// part) and, when r starts inside a tile, that tile's second part.
+
+constexpr int CEF_TOK_PER_BLOCK = 8;  // one warp per token
+
+__global__ void __launch_bounds__(32 * CEF_TOK_PER_BLOCK) ce_combine_kernel(const CeParams p, const float* ts,
+                                                                          int64_t n_tiles, float* ms) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * CEF_TOK_PER_BLOCK + w;
+  if (t >= p.T) return;
+  const float4* row = reinterpret_cast<const float4*>(ts) + t * n_tiles;
+  float m = -INFINITY, s = 0.0f;  // running global combine (identical in all lanes)
+  for (int32_t r = 0; r < p.parts; ++r) {
+    const int64_t beg = shard_offset(p.V, p.parts, r), end = shard_offset(p.V, p.parts, r + 1);
+    const int64_t t0 = beg / kTileN, t1 = (end - 1) / kTileN;
+    float mr = -INFINITY, sr = 0.0f;
+    for (int64_t tt = t0 + lane; tt <= t1; tt += 32) {
+      const float4 e = row[tt];
+      const bool second = (tt == t0) && (beg % kTileN != 0);
+      ms_combine_acc(mr, sr, second ? e.z : e.x, second ? e.w : e.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      ms_combine_acc(mr, sr, __shfl_xor_sync(0xffffffffu, mr, o), __shfl_xor_sync(0xffffffffu, sr, o));
+    ms_combine_acc(m, s, mr, sr);  // the pages' combine across shards
+  }
+  if (lane == 0) {
+    const int64_t y = load_label(p, t);
+    const bool valid = (y >= 0 && y < p.V);
+    reinterpret_cast<float2*>(ms)[t] = make_float2(m, 1.0f / s);
+    if (valid) {
+      p.loss[t] = logf(s) + m - p.z[t * p.ldz + y];
+      if (p.owner) {
+        int32_t r = 0;
+        while (r + 1 < p.parts && shard_offset(p.V, p.parts, r + 1) <= y) ++r;
+        p.owner[t] = r;
+      }
+    } else {
+      p.loss[t] = __int_as_float(0x7fc00000);  // NaN
+      if (p.owner) p.owner[t] = -1;
+      atomicOr(p.err, TPS_DEVERR_LABEL);
+    }
+  }
+}
+
+constexpr int CEF_THREADS = 256;
+constexpr int CEF_VEC = 4;                                 // float4 loads per thread per item
+constexpr int64_t CEF_ITEM = CEF_THREADS * 4 * CEF_VEC;   // 4096 elements
+
+// dlogits = e^{z - m}/s - 1[j = y], streamed over (token, 4096-column item)
+// work items by a persistent grid; all loads of an item are issued first.
+template <typename TOut>
+__global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CeParams p, const float* ms) {
+  const int64_t per_row = (p.V + CEF_ITEM - 1) / CEF_ITEM;
+  const int64_t items = p.T * per_row;
+  const bool vec = ((p.ldz & 3) == 0) && ((p.ldg & 3) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(p.z) & 15u) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(p.dlog) & (4 * sizeof(TOut) - 1)) == 0);
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const int64_t t = it / per_row;
+    const int64_t c0 = (it - t * per_row) * CEF_ITEM;
+    const float2 mi = reinterpret_cast<const float2*>(ms)[t];
+    const float ml = mi.x * kLog2e;
+    const int64_t y = load_label(p, t);
+    const float* zrow = p.z + t * p.ldz;
+    TOut* grow = static_cast<TOut*>(p.dlog) + t * p.ldg;
+    float4 v[CEF_VEC];
+#pragma unroll
+    for (int k = 0; k < CEF_VEC; ++k) {
+      const int64_t e = c0 + 4 * (threadIdx.x + k * CEF_THREADS);
+      if (vec && e + 3 < p.V) v[k] = __ldcs(reinterpret_cast<const float4*>(zrow + e));
+      else {
+        v[k].x = (e + 0 < p.V) ? zrow[e + 0] : 0.0f;
+        v[k].y = (e + 1 < p.V) ? zrow[e + 1] : 0.0f;
+        v[k].z = (e + 2 < p.V) ? zrow[e + 2] : 0.0f;
+        v[k].w = (e + 3 < p.V) ? zrow[e + 3] : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < CEF_VEC; ++k) {
+      const int64_t e = c0 + 4 * (threadIdx.x + k * CEF_THREADS);
+      float g0 = exp_shift(v[k].x, ml) * mi.y, g1 = exp_shift(v[k].y, ml) * mi.y;
+      float g2 = exp_shift(v[k].z, ml) * mi.y, g3 = exp_shift(v[k].w, ml) * mi.y;
+      if (y >= e && y < e + 4) {
+        const int64_t d = y - e;
+        g0 -= (d == 0) ? 1.0f : 0.0f;
+        g1 -= (d == 1) ? 1.0f : 0.0f;
+        g2 -= (d == 2) ? 1.0f : 0.0f;
+        g3 -= (d == 3) ? 1.0f : 0.0f;
+      }
+      if (vec && e + 3 < p.V) {
+        if constexpr (sizeof(TOut) == 2) {
+          __nv_bfloat162 a = __floats2bfloat162_rn(g0, g1), b = __floats2bfloat162_rn(g2, g3);
+          uint2 w;
+          w.x = *reinterpret_cast<uint32_t*>(&a);
+          w.y = *reinterpret_cast<uint32_t*>(&b);
+          __stcs(reinterpret_cast<uint2*>(grow + e), w);
+        } else {
+          __stcs(reinterpret_cast<float4*>(grow + e), make_float4(g0, g1, g2, g3));
+        }
+      } else {
+        if (e + 0 < p.V) store_grad(grow + e + 0, g0);
+        if (e + 1 < p.V) store_grad(grow + e + 1, g1);
+        if (e + 2 < p.V) store_grad(grow + e + 2, g2);
+        if (e + 3 < p.V) store_grad(grow + e + 3, g3);
+      }
+    }
+  }
+}
+
+bool ce_tile_stats_supported(int64_t V, int32_t parts) { return parts >= 1 && V / parts >= kTileN; }
+
+int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,
+                              uint32_t* dev_err, cudaStream_t stream) {
+  if (c.T == 0) return TPS_OK;
+  CeParams p;
+  p.T = c.T;
+  p.V = c.V;
+  p.parts = c.parts;
+  p.z = c.logits;
+  p.ldz = c.ldz;
+  p.labels = c.labels;
+  p.label_is_i64 = (c.label_dtype == TPS_I64);
+  p.loss = c.loss;
+  p.dlog = c.dlogits;
+  p.ldg = c.ldg;
+  p.owner = c.owner;
+  p.stats = nullptr;
+  p.zy = nullptr;
+  p.err = dev_err;
+  const int64_t gsize = c.dlogits_dtype == TPS_F32 ? 4 : 2;
+  const double bytes = double(c.T) * double(c.V) * (4.0 + gsize) + double(c.T) * (8.0 + 4.0);
+  ProfScope prof("ce_stream", "ce_core", 0.0, bytes, stream);
+  const int64_t nb = (c.T + CEF_TOK_PER_BLOCK - 1) / CEF_TOK_PER_BLOCK;
+  if (nb > 0x7FFFFFFF) return TPS_ERR_SHAPE;
+  ce_combine_kernel<<<static_cast<unsigned>(nb), 32 * CEF_TOK_PER_BLOCK, 0, stream>>>(p, tile_stats, n_tiles, ms);
+  note_launch();
+  if (cudaPeekAtLastError() != cudaSuccess) return TPS_ERR_CUDA;
+  int dev = 0, sms = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const unsigned grid = static_cast<unsigned>(sms * 8);
+  if (c.dlogits_dtype == TPS_F32)
+    ce_grad_stream_kernel<float><<<grid, CEF_THREADS, 0, stream>>>(p, ms);
+  else
+    ce_grad_stream_kernel<__nv_bfloat16><<<grid, CEF_THREADS, 0, stream>>>(p, ms);
+  note_launch();
+  return cudaPeekAtLastError() == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
 }
 
 // ------------------------------------------------------------ host

@@ -73,7 +73,7 @@ __device__ __forceinline__ void load_run32(const float* p, int n, float (&a)[32]
 // columns [col0, col0 + n).
 __device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, int64_t col0, int n,
                                                float (&v)[32]) {
-  if (e.mode == EPI_STORE) {
+  if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
     store_run32(e.d, e.d_dtype, row * e.ldd + col0, n, v);
   } else if (e.mode == EPI_ACT_FWD) {
     if (e.d != nullptr) store_run32(e.d, TPS_F32, row * e.ldd + col0, n, v);
@@ -91,7 +91,7 @@ __device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, i
 
 // Scalar form used by the SIMT kernel.
 __device__ __forceinline__ void epilogue_elem(const Epilogue& e, int64_t row, int64_t col, float v) {
-  if (e.mode == EPI_STORE) {
+  if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
     store_elem(e.d, e.d_dtype, row * e.ldd + col, v);
   } else if (e.mode == EPI_ACT_FWD) {
     if (e.d != nullptr) store_elem(e.d, TPS_F32, row * e.ldd + col, v);

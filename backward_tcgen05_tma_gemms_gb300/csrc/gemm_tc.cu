@@ -31,6 +31,7 @@ namespace tps {
 
 constexpr int TC_BM = 128;
 constexpr int TC_BN = 256;
+static_assert(TC_BN == kTileN, "CE tile statistics assume the GEMM's N tile");
 constexpr int TC_BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int TC_STAGES = 4;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
@@ -103,6 +104,40 @@ __device__ __forceinline__ void tc_tile_coords(int tile, int m_tiles, int n_tile
   const int in_group = tile - group * group_size;
   mt = first_m + in_group % gm;
   nt = in_group / gm;
+}
+
+// ---- vocabulary-CE statistics in the logits epilogue --------------------
+// Each epilogue thread owns one output row of the tile, so the statistics
+// of the tile's 256 columns need no cross-thread reduction: the thread folds
+// its 8 chunks of 32 columns into (max, sum of e^{z - max}) for the part of
+// the tile in shard a (the shard of the tile's first column) and the part in
+// shard b (the next one).
+constexpr float kTcLog2e = 1.4426950408889634f;
+
+// Fold elements [i0, i1) of v into (m, s); the range is a compile-time-free
+// runtime interval, so each element is predicated.
+__device__ __forceinline__ void ce_fold(const float (&v)[32], int i0, int i1, float& m, float& s) {
+  float cm = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i >= i0 && i < i1) cm = fmaxf(cm, v[i]);
+  if (cm == -INFINITY) return;
+  if (cm > m) {
+    s = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - cm) * kTcLog2e);
+    m = cm;
+  }
+  const float ml = m * kTcLog2e;
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i >= i0 && i < i1) acc += ex2_approx(fmaf(v[i], kTcLog2e, -ml));
+  s += acc;
+}
+
+// The shard owning column c under the array_split of n into p parts.
+__device__ __forceinline__ int64_t shard_of(int64_t c, int64_t n, int64_t p) {
+  const int64_t q = n / p, r = n % p, big = r * (q + 1);
+  return c < big ? c / (q + 1) : r + (c - big) / q;
 }
 
 template <bool A_MN, bool B_MN>
@@ -264,6 +299,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int i = 0; i < 32; ++i) a_next[i] = 0.0f;
         }
       }
+      // CE statistics: columns < split belong to shard a, the rest to b
+      const bool ce = (e.mode == EPI_CE_STATS);
+      int64_t split = 0;
+      float ma = -INFINITY, sa = 0.0f, mb = -INFINITY, sb = 0.0f;
+      if (ce) split = shard_offset(p.N, e.ce_parts, shard_of(n0, p.N, e.ce_parts) + 1);
       for (int c = 0; c < TC_BN / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= p.N) break;  // warp-uniform
@@ -281,6 +321,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         const int n = min(32, p.N - col0);
+        if (ce) {
+          const int na = static_cast<int>(split - col0 < 0 ? 0 : (split - col0 > n ? n : split - col0));
+          ce_fold(v, 0, na, ma, sa);
+          if (na < n) ce_fold(v, na, n, mb, sb);
+        }
         if (!p.tma_store) {
           if (row < p.M) epilogue_run32(e, row, col0, n, v);
           continue;
@@ -289,7 +334,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // tensor by the TMA unit, so rows >= M and columns >= N are dropped.
         if (lane == 0) bulk_wait_read0();  // previous boxes have left staging
         __syncwarp();
-        if (e.mode == EPI_STORE) {
+        if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
           if (e.d_dtype == TPS_F32)
             stage_f32_sw128(stg_f32, lane, v);
           else
@@ -319,6 +364,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           bulk_commit();
         }
       }
+      if (ce && row < p.M)
+        *reinterpret_cast<float4*>(e.stats + (row * e.n_tiles + nt) * 4) = make_float4(ma, sa, mb, sb);
       tc_fence_before();
       mbar_arrive(&bars->tmem_empty[acc]);
       acc ^= 1u;

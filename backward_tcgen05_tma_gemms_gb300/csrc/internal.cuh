@@ -16,7 +16,14 @@ constexpr uint32_t TPS_DEVERR_LABEL = 2u;
 // EPI_STORE    D = acc                                  (dtype d_dtype)
 // EPI_ACT_FWD  D = acc (fp32, may be null), D2 = phi(acc) (dtype d2_dtype)
 // EPI_ACT_BWD  D = acc * phi'(AUX), AUX the fp32 pre-activation
-enum EpiMode : int { EPI_STORE = 0, EPI_ACT_FWD = 1, EPI_ACT_BWD = 2 };
+// EPI_CE_STATS D = acc (fp32 logits), and per (row, 256-column tile) the
+//              softmax statistics of the tile's columns, split at the
+//              vocabulary-shard boundary (see CeTileStats)
+enum EpiMode : int { EPI_STORE = 0, EPI_ACT_FWD = 1, EPI_ACT_BWD = 2, EPI_CE_STATS = 3 };
+
+// Width of the N tiles of the tensor-core GEMM (the CE statistics are kept
+// per tile of this width).
+constexpr int kTileN = 256;
 
 struct Epilogue {
   int mode = EPI_STORE;
@@ -29,6 +36,15 @@ struct Epilogue {
   int d2_dtype = TPS_BF16;
   const float* aux = nullptr; // EPI_ACT_BWD pre-activation, row-major fp32
   int64_t ld_aux = 0;
+  // EPI_CE_STATS: stats[(row * n_tiles + tile) * 4 + {0,1,2,3}] =
+  // (m_a, s_a, m_b, s_b): max and sum of e^{z - max} over the tile's columns
+  // in the shard that owns the tile's first column (a) and in the next shard
+  // (b, empty = (-inf, 0) unless a shard boundary falls inside the tile).
+  // Shards are the array_split of N into ce_parts; every shard must be at
+  // least kTileN wide so that a tile meets at most two.
+  float* stats = nullptr;
+  int64_t n_tiles = 0;
+  int32_t ce_parts = 1;
 };
 
 // One GEMM D[M x N] = sum_k A(m, k) B(k, n), operands addressed by element
@@ -68,6 +84,14 @@ struct CeDesc {
   float* stats = nullptr;         // workspace T x parts x 2 (two-pass path)
   float* zy = nullptr;            // workspace T (two-pass path)
 };
+// Vocabulary CE when the logits GEMM already produced per-tile statistics
+// (EPI_CE_STATS): a combine kernel forms each shard's (m_r, s_r), the global
+// log-sum-exp, the loss and the owner; a streaming kernel writes dlogits.
+// `tile_stats` is T x n_tiles x 4 floats, `ms` is T x 2 floats of scratch.
+int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,
+                              uint32_t* dev_err, cudaStream_t stream);
+bool ce_tile_stats_supported(int64_t V, int32_t parts);
+
 // Picks the one-read cluster kernel when the shard plan allows it, else the
 // two-pass kernels.  `used_cluster` reports the choice.
 int launch_ce(const CeDesc& c, uint32_t* dev_err, cudaStream_t stream, bool* used_cluster);

@@ -415,7 +415,11 @@ def main():
     tc_flops = sum(v["flops"] for v in tc.values())
     tc_launches = sum(v["launches"] for v in tc.values())
     achieved = tc_flops / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
-    ce = r["prof"].get("ce_cluster:ce_core") or r["prof"].get("ce_stats:ce_core")
+    ce_parts = [v for k, v in r["prof"].items() if k.endswith(":ce_core")]
+    ce = None
+    if ce_parts:
+        ce = dict(ms=sum(v["ms"] for v in ce_parts), launches=ce_parts[0]["launches"],
+                  bytes=max(v["bytes"] for v in ce_parts))
     ce_gbs = ce["bytes"] / (ce["ms"] * 1e-3) / 1e9 if ce else None
     mlp_ms = sum(v["ms"] for k, v in tc.items() if ":mlp_" in k) / args.steps
 

@@ -89,7 +89,20 @@ def test_bf16_tensor_core(orc, tp, layout):
     with api.profile() as p:
         check(orc, h, W, labels, tp, True, layout, what=f"bf16 tp{tp} {layout}")
     kinds = {k.split(":")[0] for k in p.summary}
-    assert kinds == {"gemm_tc", "ce_cluster"}, p.summary
+    assert kinds == {"gemm_tc", "ce_stream"}, p.summary   # statistics from the logits epilogue
+
+
+@pytest.mark.parametrize("tp,V,T", [(8, 4096, 130), (3, 2048 + 768, 64), (2, 520, 33), (8, 1000, 50), (1, 32768, 17)])
+def test_bf16_shard_layouts(orc, tp, V, T):
+    """Shard boundaries on and off the 256-column tile edges, shards of
+    exactly one tile, a ragged last tile, and shards narrower than a tile
+    (which take the cluster kernel instead of the epilogue statistics)."""
+    h, W, labels = inputs.ce_case(tp * 7 + V, T, 64, V, torch.bfloat16, w_std=0.1)
+    with api.profile() as p:
+        check(orc, h, W, labels, tp, True, what=f"bf16 tp{tp} V{V}")
+    kinds = {k.split(":")[0] for k in p.summary}
+    expect = "ce_stream" if V // tp >= 256 else "ce_cluster"
+    assert expect in kinds, p.summary
 
 
 def test_label_out_of_range_sets_error():
