@@ -442,7 +442,7 @@ struct CeWs {
 };
 static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp) {
   const size_t t = static_cast<size_t>(T);
-  const size_t n_tiles = static_cast<size_t>((V + kTileN - 1) / kTileN);
+  const size_t n_tiles = static_cast<size_t>((V + kStatsTileN - 1) / kStatsTileN);
   CeWs w;
   w.z = 0;
   w.stats = w.z + align256(t * static_cast<size_t>(V) * 4);
@@ -513,7 +513,7 @@ extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead
   float* zy = reinterpret_cast<float*>(ws + lay.zy);
   float* tile_stats = reinterpret_cast<float*>(ws + lay.tiles);
   float* ms = reinterpret_cast<float*>(ws + lay.ms);
-  const int64_t n_tiles = (V + kTileN - 1) / kTileN;
+  const int64_t n_tiles = (V + kStatsTileN - 1) / kStatsTileN;
   int64_t w_in, w_out;
   weight_strides(w, weight_layout, &w_in, &w_out);  // W(dd, v)
 

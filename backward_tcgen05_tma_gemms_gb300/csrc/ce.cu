@@ -753,11 +753,11 @@ __global__ void __launch_bounds__(32 * CEF_TOK_PER_BLOCK) ce_combine_kernel(cons
   float m = -INFINITY, s = 0.0f;  // running global combine (identical in all lanes)
   for (int32_t r = 0; r < p.parts; ++r) {
     const int64_t beg = shard_offset(p.V, p.parts, r), end = shard_offset(p.V, p.parts, r + 1);
-    const int64_t t0 = beg / kTileN, t1 = (end - 1) / kTileN;
+    const int64_t t0 = beg / kStatsTileN, t1 = (end - 1) / kStatsTileN;
     float mr = -INFINITY, sr = 0.0f;
     for (int64_t tt = t0 + lane; tt <= t1; tt += 32) {
       const float4 e = row[tt];
-      const bool second = (tt == t0) && (beg % kTileN != 0);
+      const bool second = (tt == t0) && (beg % kStatsTileN != 0);
       ms_combine_acc(mr, sr, second ? e.z : e.x, second ? e.w : e.y);
     }
 #pragma unroll
@@ -849,7 +849,7 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
   }
 }
 
-bool ce_tile_stats_supported(int64_t V, int32_t parts) { return parts >= 1 && V / parts >= kTileN; }
+bool ce_tile_stats_supported(int64_t V, int32_t parts) { return parts >= 1 && V / parts >= kStatsTileN; }
 
 int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,
                               uint32_t* dev_err, cudaStream_t stream) {

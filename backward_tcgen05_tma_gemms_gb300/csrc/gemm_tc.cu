@@ -1,8 +1,10 @@
 // gemm_tc.cu -- persistent, warp-specialised bf16 GEMM on the sm_103a
-// tensor cores: TMA loads tiles into 128-byte-swizzled shared memory,
-// one thread issues tcgen05.mma (cta_group::1, M=128, N=256, K=16) into a
-// double-buffered fp32 accumulator in tensor memory, and four epilogue warps
-// drain the other buffer with tcgen05.ld and apply the fused epilogue.
+// tensor cores, one CTA per 128 x 256 output tile: TMA loads tiles into
+// 128-byte-swizzled shared memory, one thread issues tcgen05.mma
+// (cta_group::1, M=128, N=256, K=16) into a double-buffered fp32
+// accumulator in tensor memory, and four epilogue warps drain the other
+// buffer with tcgen05.ld and apply the fused epilogue.  gemm_tc2.cu holds
+// the CTA-pair variant; this file also holds the host code both share.
 //
 // This is the shard GEMM of "Sharded GEMM与Backprop：行、列、内维三种切分"
 // (解题路线 steps 2-4) and of the column/row-parallel layers of
@@ -20,19 +22,16 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
-#include "epilogue.cuh"
-#include "internal.cuh"
-#include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace tps {
 
 constexpr int TC_BM = 128;
 constexpr int TC_BN = 256;
-static_assert(TC_BN == kTileN, "CE tile statistics assume the GEMM's N tile");
-constexpr int TC_BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int TC_STAGES = 4;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 32 KB
@@ -40,14 +39,9 @@ constexpr int TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
 constexpr int TC_THREADS = 192;
 constexpr int TC_EPI_THREADS = 128;
 constexpr uint32_t TC_TMEM_COLS = 2 * TC_BN;  // two fp32 accumulators of BN columns
-constexpr int TC_GROUP_M = 16;                // tile raster: groups of 16 M-tiles
-// A box of an MN-major operand: 64 MN elements (128 B) x 64 K rows.
-constexpr int TC_MN_BOX_BYTES = 64 * TC_BK * 2;  // 8 KB
-// Epilogue staging for TMA stores, per epilogue warp: a 32 x 32 fp32 box
-// (128-byte swizzle) and a 32 x 32 bf16 box (64-byte swizzle).
-constexpr int TC_STG_F32_BYTES = 32 * 32 * 4;
-constexpr int TC_STG_BF16_BYTES = 32 * 32 * 2;
+constexpr int TC_GROUP_M = 16;                // default tile raster: groups of 16 M-tiles
 constexpr int TC_STAGING_BYTES = 4 * (TC_STG_F32_BYTES + TC_STG_BF16_BYTES);
+static_assert(TC_BN % kStatsTileN == 0, "CE statistics tiles must divide the N tile");
 
 struct TcBarriers {
   uint64_t full[TC_STAGES];
@@ -65,80 +59,12 @@ constexpr size_t TC_SMEM_BYTES =
 struct TcParams {
   int M, N, K;
   int m_tiles, n_tiles, k_tiles, num_tiles;
-  int tma_store;  // 1: outputs leave through swizzled staging + TMA stores
+  int raster_n, group;  // tile order (tc_raster)
+  int pol_a, pol_b;     // L2 policy per operand: 0 normal, 1 evict-first, 2 evict-last
+  int tma_store;        // 1: outputs leave through swizzled staging + TMA stores
   Epilogue epi;
   uint32_t* err;
 };
-
-// Row `r` of a warp's staging box, in the layout the TMA unit expects for
-// 128-byte (fp32, 8 chunks of 16 B per row) and 64-byte (bf16, 4 chunks per
-// row) swizzling: chunk i of row r sits at chunk i ^ f(r).  Consecutive rows
-// land in different bank groups, so the per-lane row writes do not conflict.
-__device__ __forceinline__ void stage_f32_sw128(uint8_t* buf, int r, const float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    *reinterpret_cast<float4*>(buf + r * 128 + ((i ^ (r & 7)) << 4)) =
-        make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-}
-__device__ __forceinline__ void stage_bf16_sw64(uint8_t* buf, int r, const float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 b0 = __floats2bfloat162_rn(v[8 * i + 0], v[8 * i + 1]);
-    __nv_bfloat162 b1 = __floats2bfloat162_rn(v[8 * i + 2], v[8 * i + 3]);
-    __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 4], v[8 * i + 5]);
-    __nv_bfloat162 b3 = __floats2bfloat162_rn(v[8 * i + 6], v[8 * i + 7]);
-    uint4 w;
-    w.x = *reinterpret_cast<uint32_t*>(&b0);
-    w.y = *reinterpret_cast<uint32_t*>(&b1);
-    w.z = *reinterpret_cast<uint32_t*>(&b2);
-    w.w = *reinterpret_cast<uint32_t*>(&b3);
-    *reinterpret_cast<uint4*>(buf + r * 64 + ((i ^ ((r >> 1) & 3)) << 4)) = w;
-  }
-}
-
-__device__ __forceinline__ void tc_tile_coords(int tile, int m_tiles, int n_tiles, int& mt, int& nt) {
-  const int group_size = TC_GROUP_M * n_tiles;
-  const int group = tile / group_size;
-  const int first_m = group * TC_GROUP_M;
-  const int gm = min(m_tiles - first_m, TC_GROUP_M);
-  const int in_group = tile - group * group_size;
-  mt = first_m + in_group % gm;
-  nt = in_group / gm;
-}
-
-// ---- vocabulary-CE statistics in the logits epilogue --------------------
-// Each epilogue thread owns one output row of the tile, so the statistics
-// of the tile's 256 columns need no cross-thread reduction: the thread folds
-// its 8 chunks of 32 columns into (max, sum of e^{z - max}) for the part of
-// the tile in shard a (the shard of the tile's first column) and the part in
-// shard b (the next one).
-constexpr float kTcLog2e = 1.4426950408889634f;
-
-// Fold elements [i0, i1) of v into (m, s); the range is a compile-time-free
-// runtime interval, so each element is predicated.
-__device__ __forceinline__ void ce_fold(const float (&v)[32], int i0, int i1, float& m, float& s) {
-  float cm = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (i >= i0 && i < i1) cm = fmaxf(cm, v[i]);
-  if (cm == -INFINITY) return;
-  if (cm > m) {
-    s = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - cm) * kTcLog2e);
-    m = cm;
-  }
-  const float ml = m * kTcLog2e;
-  float acc = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (i >= i0 && i < i1) acc += ex2_approx(fmaf(v[i], kTcLog2e, -ml));
-  s += acc;
-}
-
-// The shard owning column c under the array_split of n into p parts.
-__device__ __forceinline__ int64_t shard_of(int64_t c, int64_t n, int64_t p) {
-  const int64_t q = n / p, r = n % p, big = r * (q + 1);
-  return c < big ? c / (q + 1) : r + (c - big) / q;
-}
 
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -188,9 +114,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
+      const uint64_t pa = tc_policy(p.pol_a), pb = tc_policy(p.pol_b);
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         int mt, nt;
-        tc_tile_coords(tile, p.m_tiles, p.n_tiles, mt, nt);
+        tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
         const int m0 = mt * TC_BM, n0 = nt * TC_BN;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.err)) {
@@ -203,16 +130,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           mbar_expect_tx(fb, TC_STAGE_BYTES);
           const int k0 = kt * TC_BK;
           if (!A_MN) {
-            tma_load_2d(sa, &tmA, fb, k0, m0);
+            tma_load_maybe_hint(sa, &tmA, fb, k0, m0, p.pol_a, pa);
           } else {
 #pragma unroll
-            for (int j = 0; j < TC_BM / 64; ++j) tma_load_2d(sa + j * TC_MN_BOX_BYTES, &tmA, fb, m0 + 64 * j, k0);
+            for (int j = 0; j < TC_BM / 64; ++j)
+              tma_load_maybe_hint(sa + j * TC_MN_BOX_BYTES, &tmA, fb, m0 + 64 * j, k0, p.pol_a, pa);
           }
           if (!B_MN) {
-            tma_load_2d(sb, &tmB, fb, k0, n0);
+            tma_load_maybe_hint(sb, &tmB, fb, k0, n0, p.pol_b, pb);
           } else {
 #pragma unroll
-            for (int j = 0; j < TC_BN / 64; ++j) tma_load_2d(sb + j * TC_MN_BOX_BYTES, &tmB, fb, n0 + 64 * j, k0);
+            for (int j = 0; j < TC_BN / 64; ++j)
+              tma_load_maybe_hint(sb + j * TC_MN_BOX_BYTES, &tmB, fb, n0 + 64 * j, k0, p.pol_b, pb);
           }
           ++issued;
           if (++stage == TC_STAGES) {
@@ -277,10 +206,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t* stg_f32 = staging + (warp - 2) * TC_STG_F32_BYTES;
     uint8_t* stg_bf16 = staging + 4 * TC_STG_F32_BYTES + (warp - 2) * TC_STG_BF16_BYTES;
     const Epilogue& e = p.epi;
+    const bool ce = (e.mode == EPI_CE_STATS);
+    const bool bwd = p.tma_store && e.mode == EPI_ACT_BWD;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mt, nt;
-      tc_tile_coords(tile, p.m_tiles, p.n_tiles, mt, nt);
+      tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
       const int m0 = mt * TC_BM, n0 = nt * TC_BN;
       if (!mbar_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
@@ -290,7 +221,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       // act-bwd: the pre-activation of the next 32 columns is loaded while
       // the current ones are processed
       float a_next[32];
-      const bool bwd = p.tma_store && e.mode == EPI_ACT_BWD;
       if (bwd) {
         if (row < p.M) {
           load_run32(e.aux + row * e.ld_aux + n0, min(32, p.N - n0), a_next);
@@ -299,11 +229,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int i = 0; i < 32; ++i) a_next[i] = 0.0f;
         }
       }
-      // CE statistics: columns < split belong to shard a, the rest to b
-      const bool ce = (e.mode == EPI_CE_STATS);
-      int64_t split = 0;
-      float ma = -INFINITY, sa = 0.0f, mb = -INFINITY, sb = 0.0f;
-      if (ce) split = shard_offset(p.N, e.ce_parts, shard_of(n0, p.N, e.ce_parts) + 1);
+      CeTileAcc st;
       for (int c = 0; c < TC_BN / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= p.N) break;  // warp-uniform
@@ -322,9 +248,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         const int n = min(32, p.N - col0);
         if (ce) {
-          const int na = static_cast<int>(split - col0 < 0 ? 0 : (split - col0 > n ? n : split - col0));
-          ce_fold(v, 0, na, ma, sa);
-          if (na < n) ce_fold(v, na, n, mb, sb);
+          constexpr int kChunks = kStatsTileN / 32;
+          if (c % kChunks == 0) st.reset(e, p.N, col0);
+          st.fold(v, col0, n);
+          if ((c % kChunks == kChunks - 1 || col0 + 32 >= p.N) && row < p.M)
+            st.flush(e, row, static_cast<int64_t>(col0) / kStatsTileN);
         }
         if (!p.tma_store) {
           if (row < p.M) epilogue_run32(e, row, col0, n, v);
@@ -332,40 +260,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         // TMA store path: the box (32 rows x 32 columns) is clipped to the
         // tensor by the TMA unit, so rows >= M and columns >= N are dropped.
-        if (lane == 0) bulk_wait_read0();  // previous boxes have left staging
-        __syncwarp();
-        if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
-          if (e.d_dtype == TPS_F32)
-            stage_f32_sw128(stg_f32, lane, v);
-          else
-            stage_bf16_sw64(stg_bf16, lane, v);
-        } else if (e.mode == EPI_ACT_FWD) {
-          if (e.d != nullptr) stage_f32_sw128(stg_f32, lane, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = act_fwd(e.act, v[i]);
-          stage_bf16_sw64(stg_bf16, lane, v);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= act_grad(e.act, a[i]);
-          if (e.d_dtype == TPS_F32)
-            stage_f32_sw128(stg_f32, lane, v);
-          else
-            stage_bf16_sw64(stg_bf16, lane, v);
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (e.mode == EPI_ACT_FWD) {
-            if (e.d != nullptr) tma_store_2d(&tmD, stg_f32, col0, row0);
-            tma_store_2d(&tmD2, stg_bf16, col0, row0);
-          } else {
-            tma_store_2d(&tmD, e.d_dtype == TPS_F32 ? stg_f32 : stg_bf16, col0, row0);
-          }
-          bulk_commit();
-        }
+        tc_store_chunk<0>(e, &tmD, &tmD2, stg_f32, stg_bf16, lane, row0, col0, v, a);
       }
-      if (ce && row < p.M)
-        *reinterpret_cast<float4*>(e.stats + (row * e.n_tiles + nt) * 4) = make_float4(ma, sa, mb, sb);
       tc_fence_before();
       mbar_arrive(&bars->tmem_empty[acc]);
       acc ^= 1u;
@@ -397,10 +293,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix view: `rows` x `cols`, `cols` contiguous, row pitch
-// `ld` elements.  Box: `box_cols` x `box_rows`, 128-byte swizzle, OOB -> 0.
-static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
-                     int box_rows) {
+bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                 int box_rows) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -413,9 +307,7 @@ static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
   return r == CUDA_SUCCESS;
 }
 
-// Output view for TMA stores: rows x cols row-major with pitch `ld`
-// elements, box 32 x 32, swizzle matching the staging layout.
-static bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int dtype) {
+bool tc_make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int dtype) {
   auto fn = encode_fn();
   if (fn == nullptr || base == nullptr) return false;
   const int es = (dtype == TPS_F32) ? 4 : 2;
@@ -430,6 +322,29 @@ static bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64
                   dtype == TPS_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+int tc_num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+// Tile order and L2 policy.  Consecutive tiles walk groups of 16 M-tiles
+// (M fastest), so a wave of tiles touches a compact block of A rows and B
+// columns and consecutive waves share the group's A slabs.
+// TPS_GEMM_GROUP overrides the group size; TPS_GEMM_L2_HINTS=1 marks A (the
+// operand a group revisits) evict-last and B evict-first.
+void tc_raster_choice(int m_tiles, int* raster_n, int* group, int* pol_a, int* pol_b) {
+  const char* gv = getenv("TPS_GEMM_GROUP");
+  const char* hv = getenv("TPS_GEMM_L2_HINTS");
+  const int g = (gv && atoi(gv) > 0) ? atoi(gv) : TC_GROUP_M;
+  const int hints = hv ? atoi(hv) : 0;
+  *raster_n = 0;
+  *group = g < m_tiles ? g : m_tiles;
+  *pol_a = hints ? 2 : 0;
+  *pol_b = hints ? 1 : 0;
 }
 
 // The tensor-core path needs bf16 operands that TMA can describe: 16-byte
@@ -450,6 +365,19 @@ bool gemm_tc_supported(const GemmDesc& g) {
   return a_ok && b_ok;
 }
 
+// Output maps for the TMA-store epilogue; false when an output cannot be
+// described (the kernels then store directly).
+bool tc_make_output_maps(const GemmDesc& g, CUtensorMap* td, CUtensorMap* td2) {
+  memset(td, 0, sizeof(*td));
+  memset(td2, 0, sizeof(*td2));
+  if (g.epi.mode == EPI_ACT_FWD) {
+    bool ok = true;
+    if (g.epi.d != nullptr) ok = tc_make_out_map(td, g.epi.d, g.M, g.N, g.epi.ldd, TPS_F32);
+    return ok && g.epi.d2_dtype == TPS_BF16 && tc_make_out_map(td2, g.epi.d2, g.M, g.N, g.epi.ldd2, TPS_BF16);
+  }
+  return tc_make_out_map(td, g.epi.d, g.M, g.N, g.epi.ldd, g.epi.d_dtype);
+}
+
 template <bool A_MN, bool B_MN>
 static int launch_typed(const GemmDesc& g, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
                         const CUtensorMap& td2, const TcParams& p, int grid, cudaStream_t stream) {
@@ -466,21 +394,14 @@ static int launch_typed(const GemmDesc& g, const CUtensorMap& ta, const CUtensor
   return cudaPeekAtLastError() == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
 }
 
-static int num_sms() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
-}
-
-int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
+int launch_gemm_tc1(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   const bool a_mn = (g.a_sk != 1);
   const bool b_mn = (g.b_sk != 1);
   CUtensorMap ta, tb;
-  bool ok = a_mn ? make_map(&ta, g.a, g.K, g.M, g.a_sk, 64, TC_BK)     // stored K x M
-                 : make_map(&ta, g.a, g.M, g.K, g.a_sm, TC_BK, TC_BM);  // stored M x K
-  ok = ok && (b_mn ? make_map(&tb, g.b, g.K, g.N, g.b_sk, 64, TC_BK)    // stored K x N
-                   : make_map(&tb, g.b, g.N, g.K, g.b_sn, TC_BK, TC_BN)); // stored N x K
+  bool ok = a_mn ? tc_make_map(&ta, g.a, g.K, g.M, g.a_sk, 64, TC_BK)     // stored K x M
+                 : tc_make_map(&ta, g.a, g.M, g.K, g.a_sm, TC_BK, TC_BM);  // stored M x K
+  ok = ok && (b_mn ? tc_make_map(&tb, g.b, g.K, g.N, g.b_sk, 64, TC_BK)    // stored K x N
+                   : tc_make_map(&tb, g.b, g.N, g.K, g.b_sn, TC_BK, TC_BN)); // stored N x K
   if (!ok) return TPS_ERR_CUDA;
 
   TcParams p;
@@ -491,26 +412,27 @@ int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   p.n_tiles = static_cast<int>((g.N + TC_BN - 1) / TC_BN);
   p.k_tiles = static_cast<int>((g.K + TC_BK - 1) / TC_BK);
   p.num_tiles = p.m_tiles * p.n_tiles;
+  tc_raster_choice(p.m_tiles, &p.raster_n, &p.group, &p.pol_a, &p.pol_b);
   p.epi = g.epi;
   p.err = dev_err;
-  // TMA stores when every output can be described (else direct stores).
   CUtensorMap td, td2;
-  memset(&td, 0, sizeof(td));
-  memset(&td2, 0, sizeof(td2));
-  bool tma = true;
-  if (g.epi.mode == EPI_ACT_FWD) {
-    if (g.epi.d != nullptr) tma = make_out_map(&td, g.epi.d, g.M, g.N, g.epi.ldd, TPS_F32);
-    tma = tma && g.epi.d2_dtype == TPS_BF16 && make_out_map(&td2, g.epi.d2, g.M, g.N, g.epi.ldd2, TPS_BF16);
-  } else {
-    tma = make_out_map(&td, g.epi.d, g.M, g.N, g.epi.ldd, g.epi.d_dtype);
-  }
-  p.tma_store = tma ? 1 : 0;
-  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  p.tma_store = tc_make_output_maps(g, &td, &td2) ? 1 : 0;
+  const int sms = tc_num_sms();
+  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
 
   if (!a_mn && !b_mn) return launch_typed<false, false>(g, ta, tb, td, td2, p, grid, stream);
   if (!a_mn && b_mn) return launch_typed<false, true>(g, ta, tb, td, td2, p, grid, stream);
   if (a_mn && !b_mn) return launch_typed<true, false>(g, ta, tb, td, td2, p, grid, stream);
   return launch_typed<true, true>(g, ta, tb, td, td2, p, grid, stream);
+}
+
+// Kernel choice: CTA pairs (gemm_tc2.cu) when M spans at least one 256-row
+// pair tile, else single CTAs.  TPS_GEMM_KERNEL=1 or 2 forces one.
+int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
+  const char* kv = getenv("TPS_GEMM_KERNEL");
+  const int forced = kv ? atoi(kv) : 0;
+  const bool pair = forced == 2 || (forced != 1 && g.M >= 256);
+  return pair ? launch_gemm_tc2(g, dev_err, stream) : launch_gemm_tc1(g, dev_err, stream);
 }
 
 }  // namespace tps

@@ -1,0 +1,353 @@
+// gemm_tc2.cu -- the tensor-core GEMM on CTA pairs (tcgen05 cta_group::2).
+//
+// A cluster of two CTAs on neighbouring SMs computes one 256 x 256 output
+// tile: each CTA stages its own 128 rows of A and its own 128 columns of B
+// (so B is loaded once per pair, halving B's shared-memory footprint and
+// L2->SM traffic per SM against the one-CTA kernel), the even CTA issues
+// tcgen05.mma with M=256, and each CTA's tensor memory receives its 128
+// rows of the fp32 accumulator.  The shared memory this frees holds eight
+// epilogue warps with double-buffered TMA-store staging.
+//
+// Same GEMM, shard semantics and epilogues as gemm_tc.cu ("Sharded GEMM与
+// Backprop", 解题路线 steps 2-4; "第 6 课：张量并行 TP", core concept 1).
+//
+// Synchronisation (barriers live at the same offsets in both CTAs):
+//   full[s]       even CTA only: its producer expects both CTAs' bytes and
+//                 both CTAs' TMA loads complete on it
+//   empty[s]      each CTA: arrived by the MMA commit multicast to the pair
+//   tmem_full[b]  each CTA: arrived by the MMA commit multicast to the pair
+//   tmem_empty[b] even CTA only: one arrival per epilogue warp of each CTA
+//
+// Warp roles (320 threads, one CTA per SM):
+//   warp 0      TMA producer (one thread)
+//   warp 1      TMEM allocator; MMA issuer on the even CTA (one thread)
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 and
+//               columns 128*((w-2)/4)..+127 of the accumulator
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "tc_common.cuh"
+
+namespace tps {
+
+constexpr int T2_BM = 128;      // rows per CTA (256 per pair)
+constexpr int T2_BN = 256;      // columns per pair tile
+constexpr int T2_BN_CTA = 128;  // B columns staged by each CTA
+constexpr int T2_STAGES = 4;
+constexpr int T2_A_BYTES = T2_BM * TC_BK * 2;      // 16 KB
+constexpr int T2_B_BYTES = T2_BN_CTA * TC_BK * 2;  // 16 KB
+constexpr int T2_STAGE_BYTES = T2_A_BYTES + T2_B_BYTES;
+constexpr int T2_THREADS = 320;
+constexpr int T2_EPI_WARPS = 8;
+constexpr uint32_t T2_TMEM_COLS = 2 * T2_BN;  // two fp32 accumulators
+constexpr int T2_STG_BUF = TC_STG_F32_BYTES + TC_STG_BF16_BYTES;  // 6 KB, one buffer
+constexpr int T2_STAGING_BYTES = T2_EPI_WARPS * 2 * T2_STG_BUF;   // 96 KB
+static_assert(T2_BN / 2 == kStatsTileN, "each epilogue warp covers one CE statistics tile");
+
+struct T2Barriers {
+  uint64_t full[T2_STAGES];
+  uint64_t empty[T2_STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_slot;
+  uint32_t abort;
+};
+
+constexpr size_t T2_SMEM_BYTES = 1024 + T2_STAGES * T2_STAGE_BYTES + T2_STAGING_BYTES + sizeof(T2Barriers);
+static_assert(T2_SMEM_BYTES <= 232448, "exceeds the opt-in shared memory per block");
+
+struct T2Params {
+  int M, N, K;
+  int m_tiles, n_tiles, k_tiles, num_tiles;  // m_tiles counts 256-row pair tiles
+  int raster_n, group;
+  int tma_store;
+  Epilogue epi;
+  uint32_t* err;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(T2_THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
+                    const T2Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* staging = smem + T2_STAGES * T2_STAGE_BYTES;  // 1024-aligned
+  T2Barriers* bars = reinterpret_cast<T2Barriers*>(staging + T2_STAGING_BYTES);
+  volatile uint32_t* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < T2_STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->tmem_full[b], 1);
+      mbar_init(&bars->tmem_empty[b], 2 * T2_EPI_WARPS);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&bars->tmem_slot, T2_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_slot;
+  const uint32_t full0_leader = cluster_map(smem_u32(&bars->full[0]), 0);
+  const uint32_t tmem_empty0_leader = cluster_map(smem_u32(&bars->tmem_empty[0]), 0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      uint32_t stage = 0, phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        int mt, nt;
+        tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
+        const int m0 = mt * 2 * T2_BM + static_cast<int>(rank) * T2_BM;
+        const int nb0 = nt * T2_BN + static_cast<int>(rank) * T2_BN_CTA;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * T2_STAGE_BYTES;
+          uint8_t* sb = sa + T2_A_BYTES;
+          if (rank == 0) mbar_expect_tx(&bars->full[stage], 2 * T2_STAGE_BYTES);
+          const uint32_t fb = full0_leader + stage * static_cast<uint32_t>(sizeof(uint64_t));
+          const int k0 = kt * TC_BK;
+          if (!A_MN) {
+            tma_load_2d_pair(sa, &tmA, fb, k0, m0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < T2_BM / 64; ++j) tma_load_2d_pair(sa + j * TC_MN_BOX_BYTES, &tmA, fb, m0 + 64 * j, k0);
+          }
+          if (!B_MN) {
+            tma_load_2d_pair(sb, &tmB, fb, k0, nb0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < T2_BN_CTA / 64; ++j)
+              tma_load_2d_pair(sb + j * TC_MN_BOX_BYTES, &tmB, fb, nb0 + 64 * j, k0);
+          }
+          ++issued;
+          if (++stage == T2_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain (even CTA: the full barriers count both CTAs' bytes).
+      if (rank == 0) {
+        const int64_t first = issued > T2_STAGES ? issued - T2_STAGES : 0;
+        for (int64_t i = first; i < issued; ++i)
+          mbar_wait_drain(&bars->full[i % T2_STAGES], static_cast<uint32_t>((i / T2_STAGES) & 1), p.err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * T2_BM, T2_BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        if (!mbar_wait(&bars->tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * T2_BN;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(&bars->full[stage], phase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * T2_STAGE_BYTES);
+          const uint32_t sb = sa + T2_A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(sa + kk * 2048, TC_MN_BOX_BYTES, 1024)
+                                     : smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, TC_MN_BOX_BYTES, 1024)
+                                     : smem_desc_sw128(sb + kk * 32, 16, 1024);
+            tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kt | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(&bars->empty[stage], 0x3);  // frees the stage in both CTAs
+          if (++stage == T2_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&bars->tmem_full[acc], 0x3);  // both CTAs' accumulators complete
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      tc_commit_pair(&bars->drain);
+      mbar_wait_drain(&bars->drain, 0, p.err);
+    }
+  } else {
+    // -------------------------------------------------- epilogue warps
+    const int ew = warp - 2;       // 0..7
+    const int q = warp & 3;        // TMEM lane quadrant
+    const int h = ew >> 2;         // column half of the 256-column tile
+    uint8_t* stg = staging + ew * 2 * T2_STG_BUF;
+    const Epilogue& e = p.epi;
+    const bool ce = (e.mode == EPI_CE_STATS);
+    const bool bwd = p.tma_store && e.mode == EPI_ACT_BWD;
+    uint32_t acc = 0, acc_phase = 0, chunk = 0;
+    for (int tile = pair; tile < p.num_tiles; tile += npairs) {
+      int mt, nt;
+      tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
+      const int m0 = mt * 2 * T2_BM + static_cast<int>(rank) * T2_BM;
+      const int nh0 = nt * T2_BN + h * (T2_BN / 2);  // first column of this warp's half
+      if (!mbar_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int row0 = m0 + q * 32;
+      const int64_t row = row0 + lane;
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * T2_BN + static_cast<uint32_t>(h * (T2_BN / 2));
+      float a_next[32];
+      if (bwd) {
+        if (row < p.M && nh0 < p.N) {
+          load_run32(e.aux + row * e.ld_aux + nh0, min(32, p.N - nh0), a_next);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a_next[i] = 0.0f;
+        }
+      }
+      CeTileAcc st;
+      for (int c = 0; c < (T2_BN / 2) / 32; ++c) {
+        const int col0 = nh0 + c * 32;
+        if (col0 >= p.N) break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        float a[32];
+        if (bwd) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = a_next[i];
+          if (row < p.M && col0 + 32 < p.N && c + 1 < (T2_BN / 2) / 32)
+            load_run32(e.aux + row * e.ld_aux + col0 + 32, min(32, p.N - col0 - 32), a_next);
+        }
+        tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        const int n = min(32, p.N - col0);
+        if (ce) {
+          if (c == 0) st.reset(e, p.N, col0);
+          st.fold(v, col0, n);
+          if ((c == (T2_BN / 2) / 32 - 1 || col0 + 32 >= p.N) && row < p.M)
+            st.flush(e, row, static_cast<int64_t>(nh0) / kStatsTileN);
+        }
+        if (!p.tma_store) {
+          if (row < p.M) epilogue_run32(e, row, col0, n, v);
+          continue;
+        }
+        uint8_t* buf = stg + (chunk & 1u) * T2_STG_BUF;
+        tc_store_chunk<1>(e, &tmD, &tmD2, buf, buf + TC_STG_F32_BYTES, lane, row0, col0, v, a);
+        ++chunk;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tmem_empty0_leader + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (p.tma_store && lane == 0) bulk_wait0();
+  }
+
+  tc_fence_before();
+  cluster_sync();  // the pair's MMAs, loads and epilogues are all finished
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, T2_TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host
+
+bool tc_make_output_maps(const GemmDesc& g, CUtensorMap* td, CUtensorMap* td2);
+
+template <bool A_MN, bool B_MN>
+static int launch_pair_typed(const GemmDesc& g, const CUtensorMap& ta, const CUtensorMap& tb,
+                             const CUtensorMap& td, const CUtensorMap& td2, const T2Params& p, int pairs,
+                             cudaStream_t stream) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(T2_SMEM_BYTES));
+  });
+  if (attr_err != cudaSuccess) return TPS_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(T2_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = T2_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ProfScope prof("gemm_tc", g.name, 2.0 * double(g.M) * double(g.N) * double(g.K), 0.0, stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN>, ta, tb, td, td2, p);
+  note_launch();
+  return e == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
+}
+
+int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
+  const bool a_mn = (g.a_sk != 1);
+  const bool b_mn = (g.b_sk != 1);
+  CUtensorMap ta, tb;
+  bool ok = a_mn ? tc_make_map(&ta, g.a, g.K, g.M, g.a_sk, 64, TC_BK)       // stored K x M
+                 : tc_make_map(&ta, g.a, g.M, g.K, g.a_sm, TC_BK, T2_BM);    // stored M x K
+  ok = ok && (b_mn ? tc_make_map(&tb, g.b, g.K, g.N, g.b_sk, 64, TC_BK)      // stored K x N
+                   : tc_make_map(&tb, g.b, g.N, g.K, g.b_sn, TC_BK, T2_BN_CTA));  // stored N x K
+  if (!ok) return TPS_ERR_CUDA;
+
+  T2Params p;
+  p.M = static_cast<int>(g.M);
+  p.N = static_cast<int>(g.N);
+  p.K = static_cast<int>(g.K);
+  p.m_tiles = static_cast<int>((g.M + 2 * T2_BM - 1) / (2 * T2_BM));
+  p.n_tiles = static_cast<int>((g.N + T2_BN - 1) / T2_BN);
+  p.k_tiles = static_cast<int>((g.K + TC_BK - 1) / TC_BK);
+  p.num_tiles = p.m_tiles * p.n_tiles;
+  int pol_a = 0, pol_b = 0;
+  // groups of pair tiles cover the same rows as twice as many single tiles
+  tc_raster_choice(2 * p.m_tiles, &p.raster_n, &p.group, &pol_a, &pol_b);
+  p.group = (p.group + 1) / 2;
+  if (p.group < 1) p.group = 1;
+  if (p.group > p.m_tiles) p.group = p.m_tiles;
+  p.epi = g.epi;
+  p.err = dev_err;
+  CUtensorMap td, td2;
+  p.tma_store = tc_make_output_maps(g, &td, &td2) ? 1 : 0;
+  const int max_pairs = tc_num_sms() / 2;
+  const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
+
+  if (!a_mn && !b_mn) return launch_pair_typed<false, false>(g, ta, tb, td, td2, p, pairs, stream);
+  if (!a_mn && b_mn) return launch_pair_typed<false, true>(g, ta, tb, td, td2, p, pairs, stream);
+  if (a_mn && !b_mn) return launch_pair_typed<true, false>(g, ta, tb, td, td2, p, pairs, stream);
+  return launch_pair_typed<true, true>(g, ta, tb, td, td2, p, pairs, stream);
+}
+
+}  // namespace tps

@@ -16,14 +16,14 @@ constexpr uint32_t TPS_DEVERR_LABEL = 2u;
 // EPI_STORE    D = acc                                  (dtype d_dtype)
 // EPI_ACT_FWD  D = acc (fp32, may be null), D2 = phi(acc) (dtype d2_dtype)
 // EPI_ACT_BWD  D = acc * phi'(AUX), AUX the fp32 pre-activation
-// EPI_CE_STATS D = acc (fp32 logits), and per (row, 256-column tile) the
+// EPI_CE_STATS D = acc (fp32 logits), and per (row, 128-column tile) the
 //              softmax statistics of the tile's columns, split at the
 //              vocabulary-shard boundary (see CeTileStats)
 enum EpiMode : int { EPI_STORE = 0, EPI_ACT_FWD = 1, EPI_ACT_BWD = 2, EPI_CE_STATS = 3 };
 
-// Width of the N tiles of the tensor-core GEMM (the CE statistics are kept
-// per tile of this width).
-constexpr int kTileN = 256;
+// Width of the column tiles the CE statistics are kept for (the GEMM
+// epilogue thread that owns a row folds this many columns at a time).
+constexpr int kStatsTileN = 128;
 
 struct Epilogue {
   int mode = EPI_STORE;
@@ -41,7 +41,7 @@ struct Epilogue {
   // in the shard that owns the tile's first column (a) and in the next shard
   // (b, empty = (-inf, 0) unless a shard boundary falls inside the tile).
   // Shards are the array_split of N into ce_parts; every shard must be at
-  // least kTileN wide so that a tile meets at most two.
+  // least kStatsTileN wide so that a tile meets at most two.
   float* stats = nullptr;
   int64_t n_tiles = 0;
   int32_t ce_parts = 1;
@@ -65,7 +65,9 @@ struct GemmDesc {
 };
 
 // Launchers (return a TPS_* status; asynchronous on `stream`).
-int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);
+int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);   // picks one of:
+int launch_gemm_tc1(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);  // one CTA per tile
+int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);  // CTA pairs
 int launch_gemm_simt(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);
 bool gemm_tc_supported(const GemmDesc& g);
 

@@ -1,0 +1,194 @@
+// tc_common.cuh -- pieces shared by the two tensor-core GEMM kernels
+// (gemm_tc.cu: one CTA per 128 x 256 tile; gemm_tc2.cu: a CTA pair per
+// 256 x 256 tile): output staging for TMA stores, the fused epilogue of one
+// 32-column chunk, the vocabulary-CE tile statistics, the tile raster and
+// the host-side tensor-map helpers.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "epilogue.cuh"
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace tps {
+
+constexpr int TC_BK = 64;  // one 128-byte swizzle row of bf16
+// A box of an MN-major operand: 64 MN elements (128 B) x 64 K rows.
+constexpr int TC_MN_BOX_BYTES = 64 * TC_BK * 2;  // 8 KB
+// Epilogue staging per warp and buffer: a 32 x 32 fp32 box (128-byte
+// swizzle) and a 32 x 32 bf16 box (64-byte swizzle).
+constexpr int TC_STG_F32_BYTES = 32 * 32 * 4;
+constexpr int TC_STG_BF16_BYTES = 32 * 32 * 2;
+constexpr float kTcLog2e = 1.4426950408889634f;
+
+// Row `r` of a warp's staging box, in the layout the TMA unit expects for
+// 128-byte (fp32, 8 chunks of 16 B per row) and 64-byte (bf16, 4 chunks per
+// row) swizzling: chunk i of row r sits at chunk i ^ f(r).  Consecutive rows
+// land in different bank groups, so the per-lane row writes do not conflict.
+__device__ __forceinline__ void stage_f32_sw128(uint8_t* buf, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    *reinterpret_cast<float4*>(buf + r * 128 + ((i ^ (r & 7)) << 4)) =
+        make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+__device__ __forceinline__ void stage_bf16_sw64(uint8_t* buf, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b0 = __floats2bfloat162_rn(v[8 * i + 0], v[8 * i + 1]);
+    __nv_bfloat162 b1 = __floats2bfloat162_rn(v[8 * i + 2], v[8 * i + 3]);
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 4], v[8 * i + 5]);
+    __nv_bfloat162 b3 = __floats2bfloat162_rn(v[8 * i + 6], v[8 * i + 7]);
+    uint4 w;
+    w.x = *reinterpret_cast<uint32_t*>(&b0);
+    w.y = *reinterpret_cast<uint32_t*>(&b1);
+    w.z = *reinterpret_cast<uint32_t*>(&b2);
+    w.w = *reinterpret_cast<uint32_t*>(&b3);
+    *reinterpret_cast<uint4*>(buf + r * 64 + ((i ^ ((r >> 1) & 3)) << 4)) = w;
+  }
+}
+
+// Fused epilogue of one 32 x 32 chunk (lane = row) through TMA stores.
+// `v` holds the accumulators, `a` the pre-activation for EPI_ACT_BWD.
+// PENDING is the number of this warp's earlier bulk-store groups that may
+// still be reading staging when the buffers are overwritten (0 for one
+// staging buffer, 1 when the caller alternates two).
+template <int PENDING>
+__device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensorMap* tmD, const CUtensorMap* tmD2,
+                                               uint8_t* stg_f32, uint8_t* stg_bf16, int lane, int row0, int col0,
+                                               float (&v)[32], const float (&a)[32]) {
+  if (lane == 0) {
+    if constexpr (PENDING == 0)
+      bulk_wait_read0();
+    else
+      asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+  }
+  __syncwarp();
+  if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
+    if (e.d_dtype == TPS_F32)
+      stage_f32_sw128(stg_f32, lane, v);
+    else
+      stage_bf16_sw64(stg_bf16, lane, v);
+  } else if (e.mode == EPI_ACT_FWD) {
+    if (e.d != nullptr) stage_f32_sw128(stg_f32, lane, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = act_fwd(e.act, v[i]);
+    stage_bf16_sw64(stg_bf16, lane, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= act_grad(e.act, a[i]);
+    if (e.d_dtype == TPS_F32)
+      stage_f32_sw128(stg_f32, lane, v);
+    else
+      stage_bf16_sw64(stg_bf16, lane, v);
+  }
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (e.mode == EPI_ACT_FWD) {
+      if (e.d != nullptr) tma_store_2d(tmD, stg_f32, col0, row0);
+      tma_store_2d(tmD2, stg_bf16, col0, row0);
+    } else {
+      tma_store_2d(tmD, e.d_dtype == TPS_F32 ? stg_f32 : stg_bf16, col0, row0);
+    }
+    bulk_commit();
+  }
+}
+
+// ---- vocabulary-CE statistics in the logits epilogue ----------------------
+// Each epilogue thread owns one output row, so the statistics of a
+// kStatsTileN-column tile need no cross-thread reduction: the thread folds
+// its chunks into (max, sum of e^{z - max}) for the part of the tile in
+// shard a (the shard of the tile's first column) and the part in shard b
+// (the next one).
+
+// Fold elements [i0, i1) of v into (m, s); each element is predicated.
+__device__ __forceinline__ void ce_fold(const float (&v)[32], int i0, int i1, float& m, float& s) {
+  float cm = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i >= i0 && i < i1) cm = fmaxf(cm, v[i]);
+  if (cm == -INFINITY) return;
+  if (cm > m) {
+    s = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - cm) * kTcLog2e);
+    m = cm;
+  }
+  const float ml = m * kTcLog2e;
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i >= i0 && i < i1) acc += ex2_approx(fmaf(v[i], kTcLog2e, -ml));
+  s += acc;
+}
+
+// The shard owning column c under the array_split of n into p parts.
+__device__ __forceinline__ int64_t shard_of(int64_t c, int64_t n, int64_t p) {
+  const int64_t q = n / p, r = n % p, big = r * (q + 1);
+  return c < big ? c / (q + 1) : r + (c - big) / q;
+}
+
+// Per-row running statistics of one kStatsTileN-column tile.
+struct CeTileAcc {
+  int64_t split;  // first column of shard b
+  float ma, sa, mb, sb;
+  __device__ __forceinline__ void reset(const Epilogue& e, int64_t N, int64_t tile_col0) {
+    split = shard_offset(N, e.ce_parts, shard_of(tile_col0, N, e.ce_parts) + 1);
+    ma = -INFINITY;
+    sa = 0.0f;
+    mb = -INFINITY;
+    sb = 0.0f;
+  }
+  // Fold the chunk of columns [col0, col0 + n).
+  __device__ __forceinline__ void fold(const float (&v)[32], int64_t col0, int n) {
+    const int na = static_cast<int>(split - col0 < 0 ? 0 : (split - col0 > n ? n : split - col0));
+    ce_fold(v, 0, na, ma, sa);
+    if (na < n) ce_fold(v, na, n, mb, sb);
+  }
+  __device__ __forceinline__ void flush(const Epilogue& e, int64_t row, int64_t stat_tile) const {
+    *reinterpret_cast<float4*>(e.stats + (row * e.n_tiles + stat_tile) * 4) = make_float4(ma, sa, mb, sb);
+  }
+};
+
+// ---- tile raster and L2 policy -------------------------------------------
+// Tiles are walked in groups of `group` M-tiles, M fastest (raster_n = 0),
+// or groups of `group` N-tiles, N fastest (raster_n = 1).
+__device__ __forceinline__ void tc_raster(int raster_n, int group, int m_tiles, int n_tiles, int tile, int& mt,
+                                          int& nt) {
+  const int fast_tiles = raster_n ? n_tiles : m_tiles;
+  const int slow_tiles = raster_n ? m_tiles : n_tiles;
+  const int group_size = group * slow_tiles;
+  const int gi = tile / group_size;
+  const int first = gi * group;
+  const int g = min(fast_tiles - first, group);
+  const int in_group = tile - gi * group_size;
+  const int f = first + in_group % g, sl = in_group / g;
+  mt = raster_n ? sl : f;
+  nt = raster_n ? f : sl;
+}
+
+__device__ __forceinline__ uint64_t tc_policy(int kind) {
+  return kind == 2 ? l2_policy_evict_last() : (kind == 1 ? l2_policy_evict_first() : l2_policy_evict_normal());
+}
+// A TMA load that carries an L2 policy only when one was chosen (kind != 0):
+// a load without the hint measured faster than one with evict_normal.
+__device__ __forceinline__ void tma_load_maybe_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0,
+                                                    int32_t c1, int kind, uint64_t policy) {
+  if (kind != 0)
+    tma_load_2d_hint(dst, map, bar, c0, c1, policy);
+  else
+    tma_load_2d(dst, map, bar, c0, c1);
+}
+
+// ---- host helpers (defined in gemm_tc.cu) --------------------------------
+// Row-major bf16 operand view (rows x cols, pitch ld elements) with a
+// box_cols x box_rows box, 128-byte swizzle, zero fill out of bounds.
+bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                 int box_rows);
+// Row-major output view (fp32 or bf16) with a 32 x 32 box whose swizzle
+// matches the staging layout.
+bool tc_make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int dtype);
+int tc_num_sms();
+// Tile group size and L2 policies for the GEMM (environment overrides).
+void tc_raster_choice(int m_tiles, int* raster_n, int* group, int* pol_a, int* pol_b);
+
+}  // namespace tps

@@ -16,3 +16,11 @@ def pytest_configure(config):
 def orc():
     import oracle
     return oracle.get()
+
+
+@pytest.fixture(params=["1", "2"], ids=["cta1", "cta2"])
+def gemm_kernel(request, monkeypatch):
+    """Run a tensor-core test once with the one-CTA GEMM and once with the
+    CTA-pair GEMM (TPS_GEMM_KERNEL is read at every launch)."""
+    monkeypatch.setenv("TPS_GEMM_KERNEL", request.param)
+    return request.param

@@ -82,7 +82,7 @@ def test_fp32_empty_shards(orc):
 
 @pytest.mark.parametrize("tp", [8, 7])
 @pytest.mark.parametrize("layout", ["in_out", "out_in"])
-def test_bf16_tensor_core(orc, tp, layout):
+def test_bf16_tensor_core(orc, tp, layout, gemm_kernel):
     h, W, labels = inputs.ce_case(40 + tp, 200, 256, 32000, torch.bfloat16)
     if layout == "out_in":
         W = W.t().contiguous()
@@ -93,7 +93,7 @@ def test_bf16_tensor_core(orc, tp, layout):
 
 
 @pytest.mark.parametrize("tp,V,T", [(8, 4096, 130), (3, 2048 + 768, 64), (2, 520, 33), (8, 1000, 50), (1, 32768, 17)])
-def test_bf16_shard_layouts(orc, tp, V, T):
+def test_bf16_shard_layouts(orc, tp, V, T, gemm_kernel):
     """Shard boundaries on and off the 256-column tile edges, shards of
     exactly one tile, a ragged last tile, and shards narrower than a tile
     (which take the cluster kernel instead of the epilogue statistics)."""

@@ -54,7 +54,7 @@ TC_SHAPES = [(128, 64, 256), (300, 200, 520), (1, 64, 8), (257, 1000, 136), (520
 
 
 @pytest.mark.parametrize("M,K,N", TC_SHAPES)
-def test_bf16_tensor_core(orc, M, K, N):
+def test_bf16_tensor_core(orc, M, K, N, gemm_kernel):
     A, B, G = inputs.matmul_case(M * 7 + K, M, K, N, torch.bfloat16)
     with api.profile() as p:
         check(orc, A, B, G, 3, "inner", bf16=True, what=f"{M}x{K}x{N}")
@@ -70,7 +70,7 @@ def test_bf16_unaligned_strides_use_simt(orc):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_transposed_views_and_column_major_outputs(orc, dtype):
+def test_transposed_views_and_column_major_outputs(orc, dtype, gemm_kernel):
     M, K, N = 136, 192, 264
     A, B, G = inputs.matmul_case(11, M, K, N, dtype)
     At = A.t().contiguous().cuda().t()      # A viewed column-major

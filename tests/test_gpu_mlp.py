@@ -58,7 +58,7 @@ def test_fp32_uneven_and_empty_shards(orc, tp):
 
 @pytest.mark.parametrize("act", list(ACTS))
 @pytest.mark.parametrize("layout", ["in_out", "out_in"])
-def test_bf16_tensor_core(orc, act, layout):
+def test_bf16_tensor_core(orc, act, layout, gemm_kernel):
     T, d, F = 300, 192, 520
     X, W1, W2, GY = inputs.mlp_case(17, T, d, F, torch.bfloat16, w_std=0.05, layout=layout)
     with api.profile() as p:
@@ -67,7 +67,7 @@ def test_bf16_tensor_core(orc, act, layout):
     assert p.launches == 6
 
 
-def test_bf16_multi_wave(orc):
+def test_bf16_multi_wave(orc, gemm_kernel):
     T, d, F = 1024, 512, 2048
     X, W1, W2, GY = inputs.mlp_case(23, T, d, F, torch.bfloat16)
     run_and_check(orc, X, W1, W2, GY, 8, "gelu_tanh", "in_out", True, "1024x512x2048")
