@@ -64,7 +64,7 @@ WORKLOAD = ("TP-MLP fwd+bwd (T=8192, d=4096, F=14336, tp=8, tanh-GELU) + vocab-p
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
-GEMM_SOURCES = ["gemm_tc.cu", "ptx.cuh", "epilogue.cuh", "internal.cuh"]
+GEMM_SOURCES = ["gemm_tc.cu", "gemm_tc2.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh", "internal.cuh"]
 
 
 def kernel_source_hash(names):

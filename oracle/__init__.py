@@ -17,6 +17,9 @@ Parity status per function (what pins it is in ``tests/test_oracle_*.py``):
   mlp_rows, mlp_cols          pinned (finite differences, torch autograd)
   ce_tokens, ce_sharded_one   pinned (closed-form softmax on the worked
                               example's logits, torch cross_entropy, FD)
+  ce_ex                       pinned (torch cross_entropy with ignore_index
+                              and sum/mean reduction + autograd of h and W,
+                              truncated-vocabulary equivalence, ce_tokens)
 """
 from __future__ import annotations
 
@@ -72,6 +75,9 @@ def _declare(lib):
     lib.orc_ce_tokens.restype = ctypes.c_int
     lib.orc_ce_sharded_one.argtypes = [ctypes.c_int64, _dp, ctypes.c_int64, ctypes.c_int32, _dp, _dp, _dp]
     lib.orc_ce_sharded_one.restype = ctypes.c_double
+    lib.orc_ce_ex.argtypes = ([ctypes.c_int64] * 3 + [_dp, _dp, _i64p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+                              ctypes.c_int, ctypes.c_double, _dp, _dp, _dp, _dp, _dp, _i32p])
+    lib.orc_ce_ex.restype = ctypes.c_int
     return lib
 
 
@@ -196,6 +202,32 @@ class Oracle:
         if rc != 0:
             raise ValueError("partition" if rc == 2 else "shape")
         return loss, dlog, dh, own
+
+    def ce_ex(self, h, W, labels, parts: int, ignore_index: int = -(2 ** 63), vocab_real: int = 0,
+              reduction: int = 0, denominator: float = 0.0, want_dwhead: bool = True):
+        """Cross-entropy with vocabulary padding, ignore_index and a sum / mean
+        reduction (reduction 0 none, 1 sum, 2 mean).  Returns (loss [T],
+        loss_reduced or None, dlogits [T, V], dhidden [T, d], dwhead [d, V]
+        or None, owner [T])."""
+        h, W = self._f64(h), self._f64(W)
+        labels = np.ascontiguousarray(labels, dtype=np.int64)
+        T, d = h.shape
+        V = W.shape[1]
+        vr = V if vocab_real in (0, None) else vocab_real
+        loss = np.empty(T)
+        red = np.zeros(1)
+        dlog = np.empty((T, V))
+        dh = np.empty((T, d))
+        dw = np.empty((d, V)) if want_dwhead else None
+        own = np.empty(T, dtype=np.int32)
+        rc = self.lib.orc_ce_ex(T, d, V, self._p(h), self._p(W), self._p(labels, _i64p), parts, int(ignore_index),
+                                int(vr), int(reduction), float(denominator), self._p(loss), self._p(red),
+                                self._p(dlog), self._p(dh), self._p(dw), self._p(own, _i32p))
+        if rc == 5:
+            raise ValueError("label")
+        if rc != 0:
+            raise ValueError("partition" if rc == 2 else "shape")
+        return loss, (float(red[0]) if reduction else None), dlog, dh, dw, own
 
     def ce_sharded_one(self, z, y: int, parts: int):
         """The pages' per-shard form for one position: (L, m_r, s_r, t_r)."""

@@ -338,3 +338,81 @@ double orc_ce_sharded_one(int64_t V, const double* z, int64_t y, int32_t parts,
     free(off);
     return log(s) - tsum;
 }
+
+/* ------------------------------------------------------------------------
+ * Vocabulary cross-entropy with the extensions a real implementation needs,
+ * which [MC] "04 / VOCABULARY SHARDS" lists after its example (vocabulary
+ * padding, ignore_index) and [SG] "易错点与追问" raises (a loss denominator
+ * that stays the same across ranks with uneven numbers of supervised
+ * tokens).  Full computation over all T tokens.
+ *   Columns v >= vocab_real are padding: outside the softmax, gradient 0.
+ *   A label equal to ignore_index gives loss 0, gradient 0, owner -1 and
+ *   does not count.
+ *   reduction 0 (none) / 1 (sum): loss_reduced = sum_t L_t (not written for
+ *   none); reduction 2 (mean): loss_reduced = sum_t L_t / D with D =
+ *   denominator if > 0, else the number of counted labels (1 if none).
+ *   dlogits, dhidden = dlogits W^T and dwhead = h^T dlogits are the
+ *   gradients of sum_t L_t (none, sum) or of loss_reduced (mean).
+ * Returns ORC_ERR_LABEL for a label outside [0, vocab_real) that is not
+ * ignore_index, ORC_ERR_SHAPE for vocab_real outside [1, V].
+ * ---------------------------------------------------------------------- */
+int orc_ce_ex(int64_t T, int64_t d, int64_t V,
+              const double* h, const double* W, const int64_t* labels, int32_t parts,
+              int64_t ignore_index, int64_t vocab_real, int reduction, double denominator,
+              double* loss, double* loss_reduced, double* dlogits, double* dhidden, double* dwhead,
+              int32_t* owner) {
+    if (vocab_real < 1 || vocab_real > V) return ORC_ERR_SHAPE;
+    int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(parts + 1));
+    int rc = orc_plan_shards(V, parts, off);
+    if (rc != ORC_OK) { free(off); return rc; }
+    int64_t count = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        if (labels[t] == ignore_index) continue;
+        if (labels[t] < 0 || labels[t] >= vocab_real) { free(off); return ORC_ERR_LABEL; }
+        ++count;
+    }
+    const double D = (reduction == 2) ? (denominator > 0.0 ? denominator : (count > 0 ? (double)count : 1.0)) : 1.0;
+    double total = 0.0;
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int64_t t = 0; t < T; ++t) {
+        double* dz = dlogits + t * V;
+        const int64_t y = labels[t];
+        if (y == ignore_index) {
+            for (int64_t v = 0; v < V; ++v) dz[v] = 0.0;
+            loss[t] = 0.0;
+            owner[t] = -1;
+            continue;
+        }
+        for (int64_t v = 0; v < V; ++v) z[v] = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            double hv = h[t * d + c];
+            for (int64_t v = 0; v < V; ++v) z[v] += hv * W[c * V + v];
+        }
+        double m = -INFINITY;
+        for (int64_t v = 0; v < vocab_real; ++v) if (z[v] > m) m = z[v];
+        double s = 0.0;
+        for (int64_t v = 0; v < vocab_real; ++v) s += exp(z[v] - m);
+        loss[t] = log(s) + m - z[y];
+        total += loss[t];
+        for (int64_t v = 0; v < V; ++v)
+            dz[v] = (v < vocab_real) ? (exp(z[v] - m) / s - (v == y ? 1.0 : 0.0)) / D : 0.0;
+        owner[t] = orc_owner(y, off, parts);
+    }
+    if (loss_reduced && reduction != 0) *loss_reduced = total / D;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int64_t v = 0; v < V; ++v) acc += dlogits[t * V + v] * W[c * V + v];
+            dhidden[t * d + c] = acc;
+        }
+    if (dwhead)
+        for (int64_t c = 0; c < d; ++c)
+            for (int64_t v = 0; v < V; ++v) {
+                double acc = 0.0;
+                for (int64_t t = 0; t < T; ++t) acc += h[t * d + c] * dlogits[t * V + v];
+                dwhead[c * V + v] = acc;
+            }
+    free(z);
+    free(off);
+    return ORC_OK;
+}

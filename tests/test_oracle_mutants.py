@@ -38,6 +38,13 @@ MUTANTS = [
      "dz[v] = exp(z[v] - m) / s + (v == y ? 1.0 : 0.0);", "test_oracle_ce.py"),
     ("ce_loss_missing_max", "if (loss) loss[i] = log(s) + m - z[y];", "if (loss) loss[i] = log(s) - z[y];",
      "test_oracle_ce.py"),
+    ("ce_ex_padding_in_softmax", "for (int64_t v = 0; v < vocab_real; ++v) s += exp(z[v] - m);",
+     "for (int64_t v = 0; v < V; ++v) s += exp(z[v] - m);", "test_oracle_ce_ex.py"),
+    ("ce_ex_mean_gradient_unscaled",
+     "dz[v] = (v < vocab_real) ? (exp(z[v] - m) / s - (v == y ? 1.0 : 0.0)) / D : 0.0;",
+     "dz[v] = (v < vocab_real) ? (exp(z[v] - m) / s - (v == y ? 1.0 : 0.0)) : 0.0;", "test_oracle_ce_ex.py"),
+    ("ce_ex_denominator_counts_ignored", "(count > 0 ? (double)count : 1.0)", "(T > 0 ? (double)T : 1.0)",
+     "test_oracle_ce_ex.py"),
     ("ce_sharded_local_max", "for (int64_t j = off[r]; j < off[r + 1]; ++j) sr += exp(z[j] - m);",
      "for (int64_t j = off[r]; j < off[r + 1]; ++j) sr += exp(z[j] - m_r[r]);", "test_oracle_ce.py"),
 ]
