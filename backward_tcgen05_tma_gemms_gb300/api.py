@@ -31,6 +31,16 @@ class TpsTensor(ctypes.Structure):
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
 
 
+class TpsCeOptions(ctypes.Structure):
+    """tps_ce_options of include/tps.h."""
+    _fields_ = [("ignore_index", ctypes.c_int64), ("vocab_size", ctypes.c_int64), ("reduction", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("denominator", ctypes.c_double)]
+
+
+NO_IGNORE = -(2 ** 63)
+REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
+
+
 class TpsError(RuntimeError):
     def __init__(self, code: int, what: str):
         super().__init__(f"{what} (code {code})")
@@ -58,6 +68,8 @@ def library():
     lib.tps_mlp_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     lib.tps_mlp_workspace_bytes.restype = sz
     lib.tps_vocab_ce_fwd_bwd.argtypes = [P, P, P, i32, i32, P, P, P, P, vp, sz, vp]
+    lib.tps_vocab_ce_fwd_bwd_ex.argtypes = [P, P, P, i32, i32, ctypes.POINTER(TpsCeOptions), P, P, P, P, P, P, vp,
+                                            sz, vp]
     lib.tps_ce_workspace_bytes.argtypes = [i64, i64, i32]
     lib.tps_ce_workspace_bytes.restype = sz
     lib.tps_last_device_error.argtypes = [vp]
@@ -241,6 +253,44 @@ def vocab_ce_fwd_bwd(h: torch.Tensor, Whead: torch.Tensor, labels: torch.Tensor,
                                           *[_ref(a) for a in args[3:]], ctypes.c_void_p(workspace.data_ptr()),
                                           workspace.numel() * workspace.element_size(), _stream(h.device)))
     return loss, dlog, dh, owner
+
+
+def vocab_ce_fwd_bwd_ex(h: torch.Tensor, Whead: torch.Tensor, labels: torch.Tensor, tp: int,
+                        weight_layout: str = "in_out", ignore_index: Optional[int] = None, vocab_size: int = 0,
+                        reduction: str = "none", denominator: float = 0.0, want_dwhead: bool = False,
+                        workspace: Optional[torch.Tensor] = None):
+    """Cross-entropy with vocabulary padding (the first `vocab_size` columns
+    of the head are real, 0 = all), `ignore_index`, a "sum" or "mean"
+    reduction (the mean divides by `denominator` when > 0, e.g. the
+    job-wide count of supervised tokens, else by this call's count), and
+    optionally the head's gradient.  Returns (loss [T], loss_reduced (0-d)
+    or None, dlogits, dHidden, dWhead or None, owner)."""
+    _parts(tp, "tp")
+    if weight_layout not in LAYOUTS or reduction not in REDUCTIONS:
+        raise ValueError("argument")
+    d = h.shape[-1]
+    T = h.numel() // d if d else 0
+    V = Whead.shape[1] if weight_layout == "in_out" else Whead.shape[0]
+    dev = h.device
+    loss = torch.empty(T, device=dev, dtype=torch.float32)
+    red = torch.zeros((), device=dev, dtype=torch.float32) if reduction != "none" else None
+    dlog = torch.empty(T, V, device=dev, dtype=h.dtype)
+    dh = torch.empty(h.shape, device=dev, dtype=torch.float32)
+    dw = torch.empty(Whead.shape, device=dev, dtype=torch.float32) if want_dwhead else None
+    owner = torch.empty(T, device=dev, dtype=torch.int32)
+    if workspace is None:
+        workspace = torch.empty(max(ce_workspace_bytes(T, V, tp), 1), dtype=torch.uint8, device=dev)
+    opts = TpsCeOptions(NO_IGNORE if ignore_index is None else int(ignore_index), int(vocab_size),
+                        REDUCTIONS[reduction], 0, float(denominator))
+    red_t = _tt(red.reshape(1)) if red is not None else None
+    head = [_tt(t) for t in (h, Whead, labels, loss)]
+    tail = [_tt(t) for t in (dlog, dh, dw, owner)]
+    _check(library().tps_vocab_ce_fwd_bwd_ex(_ref(head[0]), _ref(head[1]), _ref(head[2]), tp,
+                                             LAYOUTS[weight_layout], ctypes.byref(opts), _ref(head[3]),
+                                             _ref(red_t), *[_ref(a) for a in tail],
+                                             ctypes.c_void_p(workspace.data_ptr()),
+                                             workspace.numel() * workspace.element_size(), _stream(dev)))
+    return loss, red, dlog, dh, dw, owner
 
 
 def selftest_wait_timeout(limit_ns: int = 50_000_000) -> None:

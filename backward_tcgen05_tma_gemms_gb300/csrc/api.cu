@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -435,10 +436,11 @@ extern "C" int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const 
 }
 
 // CE workspace: logits (T x V fp32) | per-shard stats of the two-pass path
-// (T x tp x 2) | label logits (T) | per-tile stats (T x ceil(V/256) x 4) |
-// combined (m, 1/s) per token (T x 2).
+// (T x tp x 2) | label logits (T) | per-tile stats (T x ceil(V/128) x 4) |
+// combined (m, 1/s) per token (T x 2) | 256 bytes of scalars (the count of
+// supervised labels, int32 at +0, and the gradient scale, f32 at +16).
 struct CeWs {
-  size_t z, stats, zy, tiles, ms, total;
+  size_t z, stats, zy, tiles, ms, scal, total;
 };
 static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp) {
   const size_t t = static_cast<size_t>(T);
@@ -449,7 +451,8 @@ static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp) {
   w.zy = w.stats + align256(t * static_cast<size_t>(tp) * 2 * 4);
   w.tiles = w.zy + align256(t * 4);
   w.ms = w.tiles + align256(t * n_tiles * 4 * 4);
-  w.total = w.ms + align256(t * 2 * 4);
+  w.scal = w.ms + align256(t * 2 * 4);
+  w.total = w.scal + 256;
   return w;
 }
 
@@ -458,12 +461,15 @@ extern "C" size_t tps_ce_workspace_bytes(int64_t T, int64_t V, int32_t tp) {
   return ce_ws_layout(T, V, tp).total;
 }
 
-extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead, const tps_tensor* labels,
-                                    int32_t tp, int32_t weight_layout, const tps_tensor* loss,
-                                    const tps_tensor* dlogits, const tps_tensor* dHidden, const tps_tensor* owner,
-                                    void* workspace, size_t workspace_bytes, void* cuda_stream) {
+// Both CE entry points: `opts` NULL is the plain form (every label in
+// [0, V), no reduction); `loss_reduced` and `dWhead` are nullable.
+static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tensor* labels, int32_t tp,
+                   int32_t weight_layout, const tps_ce_options* opts, const tps_tensor* loss,
+                   const tps_tensor* loss_reduced, const tps_tensor* dlogits, const tps_tensor* dHidden,
+                   const tps_tensor* dWhead, const tps_tensor* owner, void* workspace, size_t workspace_bytes,
+                   void* cuda_stream) {
   t_detail.clear();
-  Mat hm, w, dl, dh;
+  Mat hm, w, dl, dh, dw;
   int rc;
   if ((rc = as_mat(h, "h", true, &hm)) || (rc = as_mat(Whead, "Whead", false, &w))) return rc;
   if (weight_layout != TPS_W_IN_OUT && weight_layout != TPS_W_OUT_IN)
@@ -476,14 +482,16 @@ extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead
   if (V < 1) return fail(TPS_ERR_SHAPE, "empty vocabulary");
   const int dt = hm.dtype;
   if ((dt != TPS_F32 && dt != TPS_BF16) || w.dtype != dt) return fail(TPS_ERR_DTYPE, "h and Whead must share f32 or bf16");
-  if (labels == nullptr || labels->data == nullptr) return fail(TPS_ERR_ARG, "labels missing");
+  // With no tokens the per-token tensors may have no storage (NULL data).
+  if (labels == nullptr || (labels->data == nullptr && T > 0)) return fail(TPS_ERR_ARG, "labels missing");
   if (labels->ndim < 1 || (labels->dtype != TPS_I64 && labels->dtype != TPS_I32))
     return fail(TPS_ERR_DTYPE, "labels must be i32 or i64");
   int64_t nl = 1;
   for (int i = 0; i < labels->ndim; ++i) nl *= labels->shape[i];
   if (nl != T) return fail(TPS_ERR_SHAPE, "labels hold %lld entries for %lld tokens", (long long)nl, (long long)T);
   if (labels->stride[labels->ndim - 1] != 1 && T > 1) return fail(TPS_ERR_LAYOUT, "labels must be contiguous");
-  if (loss == nullptr || loss->data == nullptr || loss->dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "loss must be f32");
+  if (loss == nullptr || (loss->data == nullptr && T > 0) || loss->dtype != TPS_F32)
+    return fail(TPS_ERR_DTYPE, "loss must be f32");
   int64_t nloss = 1;
   for (int i = 0; i < loss->ndim; ++i) nloss *= loss->shape[i];
   if (nloss != T || (loss->stride[loss->ndim - 1] != 1 && T > 1)) return fail(TPS_ERR_SHAPE, "loss must be T contiguous floats");
@@ -500,11 +508,51 @@ extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead
       return fail(TPS_ERR_SHAPE, "owner must be T contiguous i32");
     own = static_cast<int32_t*>(owner->data);
   }
+  int64_t vreal = V;
+  if (opts != nullptr) {
+    if (opts->vocab_size < 0 || opts->vocab_size > V)
+      return fail(TPS_ERR_SHAPE, "vocab_size %lld outside [0, %lld]", (long long)opts->vocab_size, (long long)V);
+    if (opts->vocab_size > 0) vreal = opts->vocab_size;
+    if (opts->reduction != TPS_REDUCE_NONE && opts->reduction != TPS_REDUCE_SUM && opts->reduction != TPS_REDUCE_MEAN)
+      return fail(TPS_ERR_ARG, "unknown reduction %d", opts->reduction);
+    if (!(opts->denominator >= 0.0) || !std::isfinite(opts->denominator))
+      return fail(TPS_ERR_ARG, "denominator must be finite and >= 0");
+    if (opts->reserved != 0) return fail(TPS_ERR_ARG, "reserved must be 0");
+  }
+  // The plain kernels serve options that change nothing.
+  const bool ext = opts != nullptr && (opts->ignore_index != TPS_NO_IGNORE || vreal != V ||
+                                       opts->reduction != TPS_REDUCE_NONE);
+  float* red = nullptr;
+  if (loss_reduced != nullptr && loss_reduced->data != nullptr) {
+    int64_t n = 1;
+    for (int i = 0; i < loss_reduced->ndim; ++i) n *= loss_reduced->shape[i];
+    if (loss_reduced->dtype != TPS_F32 || n != 1) return fail(TPS_ERR_SHAPE, "loss_reduced must be one f32");
+    red = static_cast<float*>(loss_reduced->data);
+  }
+  const bool want_dw = dWhead != nullptr;
+  int64_t dw_in = 0, dw_out = 0;  // dWhead(dd, v) strides
+  if (want_dw) {
+    if ((rc = as_mat(dWhead, "dWhead", false, &dw)) || (rc = expect(dw, "dWhead", w.rows, w.cols))) return rc;
+    if (dw.dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "dWhead must be f32");
+    weight_strides(dw, weight_layout, &dw_in, &dw_out);
+  }
   const size_t need = tps_ce_workspace_bytes(T, V, tp);
   if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return fail(TPS_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  if (T == 0) return TPS_OK;
+  if (T == 0) {  // no tokens: a zero sum and a zero head gradient
+    if (red != nullptr && opts != nullptr && opts->reduction != TPS_REDUCE_NONE &&
+        cudaMemsetAsync(red, 0, sizeof(float), s) != cudaSuccess)
+      return fail(TPS_ERR_CUDA, "memset failed");
+    if (want_dw) {
+      GemmDesc g;
+      g.name = "ce_dwhead";
+      g.M = d; g.N = V; g.K = 0; g.in_dtype = dt;
+      g.epi.d = dw.data; g.epi.d_dtype = TPS_F32;
+      return run_gemm(g, dw_in, dw_out, s);
+    }
+    return TPS_OK;
+  }
 
   char* ws = static_cast<char*>(workspace);
   const CeWs lay = ce_ws_layout(T, V, tp);
@@ -513,6 +561,7 @@ extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead
   float* zy = reinterpret_cast<float*>(ws + lay.zy);
   float* tile_stats = reinterpret_cast<float*>(ws + lay.tiles);
   float* ms = reinterpret_cast<float*>(ws + lay.ms);
+  char* scal = ws + lay.scal;
   const int64_t n_tiles = (V + kStatsTileN - 1) / kStatsTileN;
   int64_t w_in, w_out;
   weight_strides(w, weight_layout, &w_in, &w_out);  // W(dd, v)
@@ -532,6 +581,7 @@ extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead
     g.epi.stats = tile_stats;
     g.epi.n_tiles = n_tiles;
     g.epi.ce_parts = tp;
+    g.epi.ce_vreal = vreal;
   }
   if ((rc = run_gemm(g, V, 1, s))) return rc;
   {
@@ -542,6 +592,16 @@ extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead
     c.loss = static_cast<float*>(loss->data);
     c.dlogits = dl.data; c.ldg = dl.sr; c.dlogits_dtype = dt;
     c.owner = own; c.stats = stats; c.zy = zy;
+    if (ext) {
+      c.options = true;
+      c.ignore_index = opts->ignore_index;
+      c.vreal = vreal;
+      c.reduction = opts->reduction;
+      c.denominator = opts->denominator;
+      c.loss_reduced = red;
+      c.count = reinterpret_cast<int32_t*>(scal);
+      c.scale = reinterpret_cast<float*>(scal + 16);
+    }
     uint32_t* err = dev_err_ptr();
     if (err == nullptr) return fail(TPS_ERR_CUDA, "cannot resolve the device error word");
     rc = fused ? launch_ce_from_tile_stats(c, tile_stats, n_tiles, ms, err, s) : launch_ce(c, err, s, nullptr);
@@ -557,7 +617,35 @@ extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead
     g.kparts = tp;
     if ((rc = run_gemm(g, dh.sr, dh.sc, s))) return rc;
   }
+  if (want_dw) {  // dWhead = h^T dlogits; shard r's columns are its head slice
+    GemmDesc g;
+    g.name = "ce_dwhead";
+    g.M = d; g.N = V; g.K = T; g.in_dtype = dt;
+    g.a = hm.data; g.a_sm = hm.sc; g.a_sk = hm.sr;
+    g.b = dl.data; g.b_sk = dl.sr; g.b_sn = 1;
+    g.epi.d = dw.data; g.epi.d_dtype = TPS_F32;
+    if ((rc = run_gemm(g, dw_in, dw_out, s))) return rc;
+  }
   return TPS_OK;
+}
+
+extern "C" int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead, const tps_tensor* labels,
+                                    int32_t tp, int32_t weight_layout, const tps_tensor* loss,
+                                    const tps_tensor* dlogits, const tps_tensor* dHidden, const tps_tensor* owner,
+                                    void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  return ce_impl(h, Whead, labels, tp, weight_layout, nullptr, loss, nullptr, dlogits, dHidden, nullptr, owner,
+                 workspace, workspace_bytes, cuda_stream);
+}
+
+extern "C" int tps_vocab_ce_fwd_bwd_ex(const tps_tensor* h, const tps_tensor* Whead, const tps_tensor* labels,
+                                       int32_t tp, int32_t weight_layout, const tps_ce_options* options,
+                                       const tps_tensor* loss, const tps_tensor* loss_reduced,
+                                       const tps_tensor* dlogits, const tps_tensor* dHidden,
+                                       const tps_tensor* dWhead, const tps_tensor* owner, void* workspace,
+                                       size_t workspace_bytes, void* cuda_stream) {
+  tps_ce_options defaults = {TPS_NO_IGNORE, 0, TPS_REDUCE_NONE, 0, 0.0};
+  return ce_impl(h, Whead, labels, tp, weight_layout, options ? options : &defaults, loss, loss_reduced, dlogits,
+                 dHidden, dWhead, owner, workspace, workspace_bytes, cuda_stream);
 }
 
 extern "C" int tps_last_device_error(void* cuda_stream) {

@@ -15,8 +15,14 @@
 // shard holds the label writes loss = log s + m - z_y and the owner index.
 //
 // Two-pass path (ce_stats_kernel + ce_grad_kernel) for plans the cluster
-// cannot hold (more than 8 ranks or a shard larger than shared memory):
-// the statistics go through a workspace and z is read twice.
+// cannot hold (more than 8 ranks or a shard larger than shared memory), and
+// for the extended form (vocabulary padding, ignore_index, reductions): the
+// statistics go through a workspace and z is read twice.
+//
+// Extended form: columns [vreal, V) are padding -- outside every max and
+// sum, gradient 0; a label equal to ignore_index gives loss 0, gradient 0,
+// owner -1 and is not counted; the gradient is scaled by 1 / D for a mean
+// (ce_finalize_kernel forms D and the reduced loss).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -47,6 +53,10 @@ struct CeParams {
   float* stats;
   float* zy;
   uint32_t* err;
+  int64_t ignore_index;  // TPS_NO_IGNORE: every label is supervised
+  int64_t vreal;         // columns [vreal, V) are vocabulary padding
+  const float* scale;    // gradient scale 1 / D (nullptr: 1)
+  int32_t* count;        // supervised labels are counted here (nullable)
 };
 
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -55,6 +65,13 @@ __device__ __forceinline__ int64_t load_label(const CeParams& p, int64_t t) {
   return p.label_is_i64 ? static_cast<const int64_t*>(p.labels)[t]
                         : static_cast<int64_t>(static_cast<const int32_t*>(p.labels)[t]);
 }
+
+// 0: a supervised label in [0, vreal); 1: ignore_index; 2: invalid.
+__device__ __forceinline__ int label_kind(const CeParams& p, int64_t y) {
+  if (p.ignore_index != TPS_NO_IGNORE && y == p.ignore_index) return 1;
+  return (y >= 0 && y < p.vreal) ? 0 : 2;
+}
+__device__ __forceinline__ float grad_scale(const CeParams& p) { return p.scale ? *p.scale : 1.0f; }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -657,7 +674,7 @@ __global__ void __launch_bounds__(256) ce_stats_kernel(const CeParams p) {
   const int32_t r = blockIdx.x;
   const int64_t t = blockIdx.y;
   const int64_t beg = shard_offset(p.V, p.parts, r);
-  const int64_t end = shard_offset(p.V, p.parts, r + 1);
+  const int64_t end = imin64(shard_offset(p.V, p.parts, r + 1), p.vreal);  // padding stays out
   const float* zrow = p.z + t * p.ldz;
   float m = -INFINITY, s = 0.0f;
   for (int64_t j = beg + threadIdx.x; j < end; j += blockDim.x) {
@@ -692,11 +709,15 @@ __global__ void __launch_bounds__(256) ce_stats_kernel(const CeParams p) {
     p.stats[(t * p.parts + r) * 2 + 0] = M;
     p.stats[(t * p.parts + r) * 2 + 1] = S;
     const int64_t y = load_label(p, t);
-    const bool valid = (y >= 0 && y < p.V);
-    if (valid && y >= beg && y < end) {
+    const int kind = label_kind(p, y);
+    if (kind == 0 && y >= beg && y < end) {
       p.zy[t] = zrow[y];
       if (p.owner) p.owner[t] = r;
-    } else if (!valid && r == 0) {
+      if (p.count) atomicAdd(p.count, 1);
+    } else if (kind == 1 && r == 0) {
+      p.zy[t] = 0.0f;
+      if (p.owner) p.owner[t] = -1;
+    } else if (kind == 2 && r == 0) {
       p.zy[t] = __int_as_float(0x7fc00000);
       if (p.owner) p.owner[t] = -1;
       atomicOr(p.err, TPS_DEVERR_LABEL);
@@ -723,17 +744,44 @@ __global__ void __launch_bounds__(256) ce_grad_kernel(const CeParams p) {
     }
     comb[0] = m;
     comb[1] = s;
-    if (blockIdx.x == 0) p.loss[t] = logf(s) + m - p.zy[t];  // NaN propagates for a bad label
+    if (blockIdx.x == 0)  // NaN propagates for a bad label
+      p.loss[t] = label_kind(p, load_label(p, t)) == 1 ? 0.0f : logf(s) + m - p.zy[t];
   }
   __syncthreads();
-  const float m = comb[0], inv_s = 1.0f / comb[1];
   const int64_t y = load_label(p, t);
+  const bool ignored = label_kind(p, y) == 1;
+  const float sc = grad_scale(p);
+  const float m = comb[0], inv_s = ignored ? 0.0f : sc / comb[1], hot = ignored ? 0.0f : sc;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * CE_GRAD_CHUNK;
   const int64_t c1 = imin64(p.V, c0 + CE_GRAD_CHUNK);
   const float* zrow = p.z + t * p.ldz;
   TOut* grow = static_cast<TOut*>(p.dlog) + t * p.ldg;
   for (int64_t j = c0 + threadIdx.x; j < c1; j += blockDim.x)
-    store_grad(grow + j, __expf(zrow[j] - m) * inv_s - (j == y ? 1.0f : 0.0f));
+    store_grad(grow + j, j < p.vreal ? __expf(zrow[j] - m) * inv_s - (j == y ? hot : 0.0f) : 0.0f);
+}
+
+// One block: the divisor D of a mean (the caller's denominator if > 0,
+// else the number of supervised labels, at least 1; D = 1 for a sum), the
+// gradient scale 1 / D, and the reduced loss sum_t loss_t / D.
+__global__ void __launch_bounds__(1024) ce_finalize_kernel(const float* loss, int64_t T, const int32_t* count,
+                                                           int reduction, double denominator, float* scale,
+                                                           float* loss_reduced) {
+  __shared__ double red[32];
+  double D = 1.0;
+  if (reduction == TPS_REDUCE_MEAN) D = denominator > 0.0 ? denominator : (*count > 0 ? double(*count) : 1.0);
+  if (scale != nullptr && threadIdx.x == 0) *scale = static_cast<float>(1.0 / D);
+  if (loss_reduced == nullptr) return;
+  double acc = 0.0;
+  for (int64_t t = threadIdx.x; t < T; t += blockDim.x) acc += loss[t];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double total = 0.0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += red[w];
+    *loss_reduced = static_cast<float>(total / D);
+  }
 }
 
 // ------------------------------------------------------------ from tile statistics
@@ -767,15 +815,20 @@ __global__ void __launch_bounds__(32 * CEF_TOK_PER_BLOCK) ce_combine_kernel(cons
   }
   if (lane == 0) {
     const int64_t y = load_label(p, t);
-    const bool valid = (y >= 0 && y < p.V);
-    reinterpret_cast<float2*>(ms)[t] = make_float2(m, 1.0f / s);
-    if (valid) {
+    const int kind = label_kind(p, y);
+    // an ignored token gets (m, 1/s) = (+inf, 0): every e^{z - m} / s is 0
+    reinterpret_cast<float2*>(ms)[t] = kind == 1 ? make_float2(INFINITY, 0.0f) : make_float2(m, 1.0f / s);
+    if (kind == 1) {
+      p.loss[t] = 0.0f;
+      if (p.owner) p.owner[t] = -1;
+    } else if (kind == 0) {
       p.loss[t] = logf(s) + m - p.z[t * p.ldz + y];
       if (p.owner) {
         int32_t r = 0;
         while (r + 1 < p.parts && shard_offset(p.V, p.parts, r + 1) <= y) ++r;
         p.owner[t] = r;
       }
+      if (p.count) atomicAdd(p.count, 1);
     } else {
       p.loss[t] = __int_as_float(0x7fc00000);  // NaN
       if (p.owner) p.owner[t] = -1;
@@ -797,12 +850,14 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
   const bool vec = ((p.ldz & 3) == 0) && ((p.ldg & 3) == 0) &&
                    ((reinterpret_cast<uintptr_t>(p.z) & 15u) == 0) &&
                    ((reinterpret_cast<uintptr_t>(p.dlog) & (4 * sizeof(TOut) - 1)) == 0);
+  const float sc = grad_scale(p);
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
     const int64_t t = it / per_row;
     const int64_t c0 = (it - t * per_row) * CEF_ITEM;
     const float2 mi = reinterpret_cast<const float2*>(ms)[t];
-    const float ml = mi.x * kLog2e;
-    const int64_t y = load_label(p, t);
+    const float ml = mi.x * kLog2e, inv = mi.y * sc;
+    const int64_t y0 = load_label(p, t);
+    const int64_t y = label_kind(p, y0) == 1 ? -1 : y0;  // an ignored row has no one-hot
     const float* zrow = p.z + t * p.ldz;
     TOut* grow = static_cast<TOut*>(p.dlog) + t * p.ldg;
     float4 v[CEF_VEC];
@@ -820,14 +875,20 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
 #pragma unroll
     for (int k = 0; k < CEF_VEC; ++k) {
       const int64_t e = c0 + 4 * (threadIdx.x + k * CEF_THREADS);
-      float g0 = exp_shift(v[k].x, ml) * mi.y, g1 = exp_shift(v[k].y, ml) * mi.y;
-      float g2 = exp_shift(v[k].z, ml) * mi.y, g3 = exp_shift(v[k].w, ml) * mi.y;
+      float g0 = exp_shift(v[k].x, ml) * inv, g1 = exp_shift(v[k].y, ml) * inv;
+      float g2 = exp_shift(v[k].z, ml) * inv, g3 = exp_shift(v[k].w, ml) * inv;
       if (y >= e && y < e + 4) {
         const int64_t d = y - e;
-        g0 -= (d == 0) ? 1.0f : 0.0f;
-        g1 -= (d == 1) ? 1.0f : 0.0f;
-        g2 -= (d == 2) ? 1.0f : 0.0f;
-        g3 -= (d == 3) ? 1.0f : 0.0f;
+        g0 -= (d == 0) ? sc : 0.0f;
+        g1 -= (d == 1) ? sc : 0.0f;
+        g2 -= (d == 2) ? sc : 0.0f;
+        g3 -= (d == 3) ? sc : 0.0f;
+      }
+      if (e + 3 >= p.vreal) {  // vocabulary padding
+        g0 = (e + 0 < p.vreal) ? g0 : 0.0f;
+        g1 = (e + 1 < p.vreal) ? g1 : 0.0f;
+        g2 = (e + 2 < p.vreal) ? g2 : 0.0f;
+        g3 = (e + 3 < p.vreal) ? g3 : 0.0f;
       }
       if (vec && e + 3 < p.V) {
         if constexpr (sizeof(TOut) == 2) {
@@ -851,9 +912,7 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
 
 bool ce_tile_stats_supported(int64_t V, int32_t parts) { return parts >= 1 && V / parts >= kStatsTileN; }
 
-int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,
-                              uint32_t* dev_err, cudaStream_t stream) {
-  if (c.T == 0) return TPS_OK;
+static CeParams make_params(const CeDesc& c, uint32_t* dev_err) {
   CeParams p;
   p.T = c.T;
   p.V = c.V;
@@ -866,17 +925,47 @@ int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t 
   p.dlog = c.dlogits;
   p.ldg = c.ldg;
   p.owner = c.owner;
+  p.stats = c.stats;
+  p.zy = c.zy;
+  p.err = dev_err;
+  p.ignore_index = c.options ? c.ignore_index : TPS_NO_IGNORE;
+  p.vreal = c.options ? c.vreal : c.V;
+  p.scale = (c.options && c.reduction == TPS_REDUCE_MEAN) ? c.scale : nullptr;
+  p.count = c.options ? c.count : nullptr;
+  return p;
+}
+
+// The divisor's scale (before the gradient) and / or the reduced loss
+// (once every loss is written) of the extended form.
+static int launch_finalize(const CeDesc& c, bool want_scale, bool want_reduced, cudaStream_t stream) {
+  float* scale = (want_scale && c.reduction == TPS_REDUCE_MEAN) ? c.scale : nullptr;
+  float* red = (want_reduced && c.reduction != TPS_REDUCE_NONE) ? c.loss_reduced : nullptr;
+  if (scale == nullptr && red == nullptr) return TPS_OK;
+  ProfScope prof("ce_finalize", "ce_core", 0.0, double(c.T) * 4.0, stream);
+  ce_finalize_kernel<<<1, 1024, 0, stream>>>(c.loss, c.T, c.count, c.reduction, c.denominator, scale, red);
+  note_launch();
+  return cudaPeekAtLastError() == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
+}
+
+int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,
+                              uint32_t* dev_err, cudaStream_t stream) {
+  if (c.T == 0) return TPS_OK;
+  CeParams p = make_params(c, dev_err);
   p.stats = nullptr;
   p.zy = nullptr;
-  p.err = dev_err;
   const int64_t gsize = c.dlogits_dtype == TPS_F32 ? 4 : 2;
   const double bytes = double(c.T) * double(c.V) * (4.0 + gsize) + double(c.T) * (8.0 + 4.0);
   ProfScope prof("ce_stream", "ce_core", 0.0, bytes, stream);
   const int64_t nb = (c.T + CEF_TOK_PER_BLOCK - 1) / CEF_TOK_PER_BLOCK;
   if (nb > 0x7FFFFFFF) return TPS_ERR_SHAPE;
+  if (c.options && cudaMemsetAsync(c.count, 0, sizeof(int32_t), stream) != cudaSuccess) return TPS_ERR_CUDA;
   ce_combine_kernel<<<static_cast<unsigned>(nb), 32 * CEF_TOK_PER_BLOCK, 0, stream>>>(p, tile_stats, n_tiles, ms);
   note_launch();
   if (cudaPeekAtLastError() != cudaSuccess) return TPS_ERR_CUDA;
+  if (c.options) {  // every loss and the count are known after the combine
+    const int rc = launch_finalize(c, true, true, stream);
+    if (rc != TPS_OK) return rc;
+  }
   int dev = 0, sms = 1;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -960,62 +1049,68 @@ static int launch_cluster(const CeParams& p, cudaStream_t stream) {
   return e == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
 }
 
-template <typename TOut>
-static int launch_two_pass(const CeParams& p, cudaStream_t stream) {
-  {
-    ProfScope prof("ce_stats", "ce_core", 0.0, double(p.T) * double(p.V) * 4.0, stream);
-    ce_stats_kernel<<<dim3(static_cast<unsigned>(p.parts), static_cast<unsigned>(p.T)), 256, 0, stream>>>(p);
-    note_launch();
-  }
-  if (cudaPeekAtLastError() != cudaSuccess) return TPS_ERR_CUDA;
-  {
-    const int64_t chunks = (p.V + CE_GRAD_CHUNK - 1) / CE_GRAD_CHUNK;
-    ProfScope prof("ce_grad", "ce_core", 0.0, double(p.T) * double(p.V) * (4.0 + sizeof(TOut)), stream);
-    ce_grad_kernel<TOut><<<dim3(static_cast<unsigned>(chunks), static_cast<unsigned>(p.T)), 256, 0, stream>>>(p);
-    note_launch();
-  }
+static int launch_stats(const CeParams& p, cudaStream_t stream) {
+  ProfScope prof("ce_stats", "ce_core", 0.0, double(p.T) * double(p.V) * 4.0, stream);
+  ce_stats_kernel<<<dim3(static_cast<unsigned>(p.parts), static_cast<unsigned>(p.T)), 256, 0, stream>>>(p);
+  note_launch();
   return cudaPeekAtLastError() == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
 }
 
+template <typename TOut>
+static int launch_grad(const CeParams& p, cudaStream_t stream) {
+  const int64_t chunks = (p.V + CE_GRAD_CHUNK - 1) / CE_GRAD_CHUNK;
+  ProfScope prof("ce_grad", "ce_core", 0.0, double(p.T) * double(p.V) * (4.0 + sizeof(TOut)), stream);
+  ce_grad_kernel<TOut><<<dim3(static_cast<unsigned>(chunks), static_cast<unsigned>(p.T)), 256, 0, stream>>>(p);
+  note_launch();
+  return cudaPeekAtLastError() == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
+}
+
+// Tokens [t0, t0 + min(65535, T - t0)) of `p`: tokens go on grid.y.
+static CeParams slab(const CeParams& p, int64_t t0, size_t gsize) {
+  CeParams q = p;
+  q.T = imin64(65535, p.T - t0);
+  q.z = p.z + t0 * p.ldz;
+  q.labels = p.label_is_i64 ? static_cast<const void*>(static_cast<const int64_t*>(p.labels) + t0)
+                            : static_cast<const void*>(static_cast<const int32_t*>(p.labels) + t0);
+  q.loss = p.loss + t0;
+  q.dlog = static_cast<char*>(p.dlog) + t0 * p.ldg * gsize;
+  q.owner = p.owner ? p.owner + t0 : nullptr;
+  q.stats = p.stats ? p.stats + t0 * p.parts * 2 : nullptr;
+  q.zy = p.zy ? p.zy + t0 : nullptr;
+  return q;
+}
+
 int launch_ce(const CeDesc& c, uint32_t* dev_err, cudaStream_t stream, bool* used_cluster) {
-  CeParams p;
-  p.T = c.T;
-  p.V = c.V;
-  p.parts = c.parts;
-  p.z = c.logits;
-  p.ldz = c.ldz;
-  p.labels = c.labels;
-  p.label_is_i64 = (c.label_dtype == TPS_I64);
-  p.loss = c.loss;
-  p.dlog = c.dlogits;
-  p.ldg = c.ldg;
-  p.owner = c.owner;
-  p.stats = c.stats;
-  p.zy = c.zy;
-  p.err = dev_err;
-  const bool cl = ce_cluster_supported(c.V, c.parts, c.dlogits_dtype);
+  const CeParams p = make_params(c, dev_err);
+  // The cluster kernels serve the plain form only.
+  const bool cl = !c.options && ce_cluster_supported(c.V, c.parts, c.dlogits_dtype);
   if (used_cluster) *used_cluster = cl;
-  const size_t gsize = (c.dlogits_dtype == TPS_F32) ? 4 : 2;
-  // Tokens go on grid.y (at most 65535 per launch): process slabs.
+  const bool f32 = c.dlogits_dtype == TPS_F32;
+  const size_t gsize = f32 ? 4 : 2;
+  if (cl) {
+    for (int64_t t0 = 0; t0 < c.T; t0 += 65535) {
+      const CeParams q = slab(p, t0, gsize);
+      const int rc = f32 ? launch_cluster<float>(q, stream) : launch_cluster<__nv_bfloat16>(q, stream);
+      if (rc != TPS_OK) return rc;
+    }
+    return TPS_OK;
+  }
+  if (c.options && c.T > 0 && cudaMemsetAsync(c.count, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return TPS_ERR_CUDA;
   for (int64_t t0 = 0; t0 < c.T; t0 += 65535) {
-    CeParams q = p;
-    q.T = imin64(65535, c.T - t0);
-    q.z = p.z + t0 * p.ldz;
-    q.labels = p.label_is_i64 ? static_cast<const void*>(static_cast<const int64_t*>(p.labels) + t0)
-                              : static_cast<const void*>(static_cast<const int32_t*>(p.labels) + t0);
-    q.loss = p.loss + t0;
-    q.dlog = static_cast<char*>(p.dlog) + t0 * p.ldg * gsize;
-    q.owner = p.owner ? p.owner + t0 : nullptr;
-    q.stats = p.stats ? p.stats + t0 * p.parts * 2 : nullptr;
-    q.zy = p.zy ? p.zy + t0 : nullptr;
-    int rc;
-    if (cl)
-      rc = (c.dlogits_dtype == TPS_F32) ? launch_cluster<float>(q, stream) : launch_cluster<__nv_bfloat16>(q, stream);
-    else
-      rc = (c.dlogits_dtype == TPS_F32) ? launch_two_pass<float>(q, stream)
-                                        : launch_two_pass<__nv_bfloat16>(q, stream);
+    const int rc = launch_stats(slab(p, t0, gsize), stream);
     if (rc != TPS_OK) return rc;
   }
+  if (c.options && c.T > 0) {  // the mean's divisor needs every count
+    const int rc = launch_finalize(c, true, false, stream);
+    if (rc != TPS_OK) return rc;
+  }
+  for (int64_t t0 = 0; t0 < c.T; t0 += 65535) {
+    const CeParams q = slab(p, t0, gsize);
+    const int rc = f32 ? launch_grad<float>(q, stream) : launch_grad<__nv_bfloat16>(q, stream);
+    if (rc != TPS_OK) return rc;
+  }
+  if (c.options && c.T > 0) return launch_finalize(c, false, true, stream);  // every loss is written
   return TPS_OK;
 }
 

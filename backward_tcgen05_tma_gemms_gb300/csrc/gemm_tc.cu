@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (ce) {
           constexpr int kChunks = kStatsTileN / 32;
           if (c % kChunks == 0) st.reset(e, p.N, col0);
-          st.fold(v, col0, n);
+          st.fold(v, col0, n, e.ce_vreal);
           if ((c % kChunks == kChunks - 1 || col0 + 32 >= p.N) && row < p.M)
             st.flush(e, row, static_cast<int64_t>(col0) / kStatsTileN);
         }

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         const int n = min(32, p.N - col0);
         if (ce) {
           if (c == 0) st.reset(e, p.N, col0);
-          st.fold(v, col0, n);
+          st.fold(v, col0, n, e.ce_vreal);
           if ((c == (T2_BN / 2) / 32 - 1 || col0 + 32 >= p.N) && row < p.M)
             st.flush(e, row, static_cast<int64_t>(nh0) / kStatsTileN);
         }

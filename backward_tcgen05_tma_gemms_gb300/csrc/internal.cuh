@@ -45,6 +45,9 @@ struct Epilogue {
   float* stats = nullptr;
   int64_t n_tiles = 0;
   int32_t ce_parts = 1;
+  // Columns at or beyond ce_vreal are vocabulary padding: they are stored
+  // but left out of the statistics.
+  int64_t ce_vreal = INT64_MAX;
 };
 
 // One GEMM D[M x N] = sum_k A(m, k) B(k, n), operands addressed by element
@@ -85,6 +88,16 @@ struct CeDesc {
   int32_t* owner = nullptr;       // T, nullable
   float* stats = nullptr;         // workspace T x parts x 2 (two-pass path)
   float* zy = nullptr;            // workspace T (two-pass path)
+  // Extended form (tps_vocab_ce_fwd_bwd_ex); when `options` is false the
+  // fields below are ignored and every label must lie in [0, V).
+  bool options = false;
+  int64_t ignore_index = TPS_NO_IGNORE;  // label value that is not supervised
+  int64_t vreal = 0;                     // columns [vreal, V) are padding
+  int reduction = TPS_REDUCE_NONE;
+  double denominator = 0.0;              // > 0: the mean's divisor
+  float* loss_reduced = nullptr;         // 1 float, nullable
+  int32_t* count = nullptr;              // workspace: supervised labels
+  float* scale = nullptr;                // workspace: 1 / divisor
 };
 // Vocabulary CE when the logits GEMM already produced per-tile statistics
 // (EPI_CE_STATS): a combine kernel forms each shard's (m_r, s_r), the global

@@ -139,7 +139,10 @@ struct CeTileAcc {
     sb = 0.0f;
   }
   // Fold the chunk of columns [col0, col0 + n).
-  __device__ __forceinline__ void fold(const float (&v)[32], int64_t col0, int n) {
+  // Fold the chunk of columns [col0, col0 + n); columns at or beyond
+  // `vreal` are vocabulary padding and stay out of the statistics.
+  __device__ __forceinline__ void fold(const float (&v)[32], int64_t col0, int n, int64_t vreal) {
+    if (vreal - col0 < n) n = static_cast<int>(vreal - col0 < 0 ? 0 : vreal - col0);
     const int na = static_cast<int>(split - col0 < 0 ? 0 : (split - col0 > n ? n : split - col0));
     ce_fold(v, 0, na, ma, sa);
     if (na < n) ce_fold(v, na, n, mb, sb);

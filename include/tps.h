@@ -200,9 +200,53 @@ int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead, const tps
                          const tps_tensor* dHidden, const tps_tensor* owner, void* workspace,
                          size_t workspace_bytes, void* cuda_stream);
 
-/* Workspace bytes tps_vocab_ce_fwd_bwd needs for T tokens, vocabulary V and
- * `tp` shards. */
+/* Workspace bytes tps_vocab_ce_fwd_bwd and tps_vocab_ce_fwd_bwd_ex need for
+ * T tokens, vocabulary V and `tp` shards. */
 size_t tps_ce_workspace_bytes(int64_t T, int64_t V, int32_t tp);
+
+/* ------------------------------------------------------------------------
+ * tps_vocab_ce_fwd_bwd_ex -- tps_vocab_ce_fwd_bwd with the extensions a
+ * production loss needs, which [MC] "04 / VOCABULARY SHARDS" names after its
+ * worked example (a vocabulary padded to a shardable size, an ignore_index)
+ * and [SG] "易错点与追问" raises (a mean whose denominator is the same on every
+ * rank even when ranks hold different numbers of supervised tokens), plus
+ * the head's own gradient dWhead = h^T dlogits, the other half of the
+ * backward of z = h Whead ([SG] "解题路线" step 1: dB = A^T G).
+ *   options->vocab_size (0 = V): columns [vocab_size, V) of Whead are
+ *     padding.  They are left out of every softmax, their dlogits are 0,
+ *     and a label there is an error.  Shards stay the array_split of the
+ *     padded V (so `owner` is the rank of the padded plan).
+ *   options->ignore_index (TPS_NO_IGNORE = none): a token whose label
+ *     equals it has loss 0, dlogits row 0, owner -1, and is not counted.
+ *   options->reduction: TPS_REDUCE_NONE, _SUM or _MEAN.  `loss` always
+ *     holds the per-token losses; `loss_reduced` (one f32, may be NULL)
+ *     receives sum_t loss_t (SUM) or sum_t loss_t / D (MEAN), where D =
+ *     options->denominator if > 0 (e.g. the job-wide count of supervised
+ *     tokens, summed over data-parallel ranks by the caller), else the
+ *     number of supervised tokens of this call (1 if none).  dlogits,
+ *     dHidden and dWhead are the gradients of sum_t loss_t (NONE, SUM) or
+ *     of the mean (MEAN, i.e. divided by D).
+ *   dWhead (Whead's shape, f32, may be NULL): the head's gradient, a
+ *     tensor-core GEMM over the T tokens for bf16 operands.
+ * options == NULL means all defaults (no padding, no ignore, NONE).
+ * Other arguments, workspace size and errors as tps_vocab_ce_fwd_bwd;
+ * additionally TPS_ERR_SHAPE for vocab_size outside [0, V] and TPS_ERR_ARG
+ * for an unknown reduction or a negative / non-finite denominator.
+ * ---------------------------------------------------------------------- */
+#define TPS_NO_IGNORE INT64_MIN
+enum { TPS_REDUCE_NONE = 0, TPS_REDUCE_SUM = 1, TPS_REDUCE_MEAN = 2 };
+typedef struct tps_ce_options {
+  int64_t ignore_index;
+  int64_t vocab_size;
+  int32_t reduction;
+  int32_t reserved; /* must be 0 */
+  double denominator;
+} tps_ce_options;
+int tps_vocab_ce_fwd_bwd_ex(const tps_tensor* h, const tps_tensor* Whead, const tps_tensor* labels, int32_t tp,
+                            int32_t weight_layout, const tps_ce_options* options, const tps_tensor* loss,
+                            const tps_tensor* loss_reduced, const tps_tensor* dlogits, const tps_tensor* dHidden,
+                            const tps_tensor* dWhead, const tps_tensor* owner, void* workspace,
+                            size_t workspace_bytes, void* cuda_stream);
 
 /* ------------------------------------------------------------------------
  * tps_last_device_error -- synchronizes `cuda_stream`, then reads and clears
