@@ -15,6 +15,9 @@ Parity status per function (what pins it is in ``tests/test_oracle_*.py``):
                               torch float64 autograd, sharded == unsharded)
   act, act_grad               pinned (torch gelu/tanh, closed forms, FD)
   mlp_rows, mlp_cols          pinned (finite differences, torch autograd)
+  glu_rows, glu_cols          pinned (torch autograd, finite differences,
+                              reduction to mlp_* when U = 1, the lesson's
+                              per-rank sum)
   ce_tokens, ce_sharded_one   pinned (closed-form softmax on the worked
                               example's logits, torch cross_entropy, FD)
   ce_ex                       pinned (torch cross_entropy with ignore_index
@@ -36,7 +39,7 @@ _LIB_PATH = os.path.join(_HERE, "_liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-ACT_GELU_ERF, ACT_GELU_TANH, ACT_TANH = 0, 1, 2
+ACT_GELU_ERF, ACT_GELU_TANH, ACT_TANH, ACT_SILU = 0, 1, 2, 3
 
 _dp = ctypes.POINTER(ctypes.c_double)
 _i64p = ctypes.POINTER(ctypes.c_int64)
@@ -70,6 +73,11 @@ def _declare(lib):
     lib.orc_mlp_rows.restype = None
     lib.orc_mlp_cols.argtypes = [ctypes.c_int64] * 3 + [_dp] * 4 + [ctypes.c_int, ctypes.c_int64, _i64p, _dp, _dp]
     lib.orc_mlp_cols.restype = None
+    lib.orc_glu_rows.argtypes = [ctypes.c_int64] * 3 + [_dp] * 5 + [ctypes.c_int, ctypes.c_int64, _i64p, _dp, _dp]
+    lib.orc_glu_rows.restype = None
+    lib.orc_glu_cols.argtypes = ([ctypes.c_int64] * 3 + [_dp] * 5 + [ctypes.c_int, ctypes.c_int64, _i64p, _dp, _dp,
+                                 _dp])
+    lib.orc_glu_cols.restype = None
     lib.orc_ce_tokens.argtypes = ([ctypes.c_int64] * 3 + [_dp, _dp, _i64p, ctypes.c_int32, ctypes.c_int64, _i64p,
                                   _dp, _dp, _dp, _i32p])
     lib.orc_ce_tokens.restype = ctypes.c_int
@@ -180,6 +188,38 @@ class Oracle:
         Y, dX = self.mlp_rows(X, W1, W2, GY, act)
         dW1, dW2 = self.mlp_cols(X, W1, W2, GY, act)
         return Y, dX, dW1, dW2
+
+    # -- gated MLP (weights (in, out): Wg, Wu d x F, W2 F x d) -------------
+    def glu_rows(self, X, Wg, Wu, W2, GY, act: int, rows=None):
+        """(Y[rows], dX[rows]) of the gated MLP."""
+        X, Wg, Wu, W2, GY = map(self._f64, (X, Wg, Wu, W2, GY))
+        T, d = X.shape
+        F = Wg.shape[1]
+        rows = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        Y = np.empty((len(rows), d))
+        dX = np.empty((len(rows), d))
+        self.lib.orc_glu_rows(T, d, F, self._p(X), self._p(Wg), self._p(Wu), self._p(W2), self._p(GY), act,
+                              len(rows), self._p(rows, _i64p), self._p(Y), self._p(dX))
+        return Y, dX
+
+    def glu_cols(self, X, Wg, Wu, W2, GY, act: int, cols=None):
+        """(dWg[:, cols], dWu[:, cols] as d x ncols, dW2[cols, :] as ncols x d)."""
+        X, Wg, Wu, W2, GY = map(self._f64, (X, Wg, Wu, W2, GY))
+        T, d = X.shape
+        F = Wg.shape[1]
+        cols = np.arange(F, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+        dWg = np.empty((d, len(cols)))
+        dWu = np.empty((d, len(cols)))
+        dW2 = np.empty((len(cols), d))
+        self.lib.orc_glu_cols(T, d, F, self._p(X), self._p(Wg), self._p(Wu), self._p(W2), self._p(GY), act,
+                              len(cols), self._p(cols, _i64p), self._p(dWg), self._p(dWu), self._p(dW2))
+        return dWg, dWu, dW2
+
+    def glu(self, X, Wg, Wu, W2, GY, act: int):
+        """Full (Y, dX, dWg, dWu, dW2), weights in (in, out) layout."""
+        Y, dX = self.glu_rows(X, Wg, Wu, W2, GY, act)
+        dWg, dWu, dW2 = self.glu_cols(X, Wg, Wu, W2, GY, act)
+        return Y, dX, dWg, dWu, dW2
 
     # -- cross-entropy ---------------------------------------------------
     def ce_tokens(self, h, W, labels, parts: int, toks=None):

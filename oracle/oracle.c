@@ -38,6 +38,7 @@
 #define ORC_ACT_GELU_ERF 0
 #define ORC_ACT_GELU_TANH 1
 #define ORC_ACT_TANH 2
+#define ORC_ACT_SILU 3
 
 int orc_num_threads(void) {
 #ifdef _OPENMP
@@ -119,6 +120,9 @@ void orc_matmul(int64_t M, int64_t K, int64_t N,
  *   GELU_TANH: the tanh approximation of GELU (Hendrycks & Gimpel 2016),
  *              0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
  *   TANH     : tanh, whose derivative [MC] "02 / BACKWARD" writes as 1 - H^2.
+ *   SILU     : x sigma(x) with the logistic sigma(x) = 1 / (1 + e^{-x}), an
+ *              element-wise activation [TP] core concept 2.A step 3 names;
+ *              d/dx = sigma(x) + x sigma(x) (1 - sigma(x)).
  * ---------------------------------------------------------------------- */
 static const double ORC_PI = 3.14159265358979323846;
 
@@ -128,6 +132,8 @@ double orc_act(int kind, double x) {
     } else if (kind == ORC_ACT_GELU_TANH) {
         double c = sqrt(2.0 / ORC_PI);
         return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+    } else if (kind == ORC_ACT_SILU) {
+        return x / (1.0 + exp(-x));
     } else {
         return tanh(x);
     }
@@ -144,6 +150,9 @@ double orc_act_grad(int kind, double x) {
         double c = sqrt(2.0 / ORC_PI);
         double u = tanh(c * (x + 0.044715 * x * x * x));
         return 0.5 * (1.0 + u) + 0.5 * x * (1.0 - u * u) * c * (1.0 + 3.0 * 0.044715 * x * x);
+    } else if (kind == ORC_ACT_SILU) {
+        double sg = 1.0 / (1.0 + exp(-x));
+        return sg + x * sg * (1.0 - sg);
     } else {
         double h = tanh(x);
         return 1.0 - h * h;
@@ -245,6 +254,119 @@ void orc_mlp_cols(int64_t T, int64_t d, int64_t F,
         }
         free(ha);
         free(dz);
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * Gated column-then-row MLP (SwiGLU when phi = SiLU), unsharded definition.
+ * [TP] reference answer Q1 puts the "gate/up" projections and the
+ * activation in the column-parallel layer and the "down" projection in the
+ * row-parallel one; the gate and up weights are both split along F with the
+ * same shard plan, so the element-wise gating stays shard-local exactly as
+ * phi does in core concept 2.A step 3.  The gating product itself is the
+ * usual gated linear unit (the pages give no formula; this is the plain
+ * reading of "gate/up"):
+ *     Hg = X Wg,  U = X Wu,  A = phi(Hg) * U,  Y = A W2.
+ * Backward (upstream G_Y given, no scaling; chain rule through the product):
+ *     dA = G_Y W2^T,  dU = dA * phi(Hg),  dHg = dA * U * phi'(Hg),
+ *     dWg = X^T dHg,  dWu = X^T dU,  dW2 = A^T G_Y,
+ *     dX = dHg Wg^T + dU Wu^T.
+ * Shapes: X T x d, Wg and Wu d x F (in,out), W2 F x d (in,out), G_Y T x d.
+ *
+ * orc_glu_rows computes rows `rows[i]` of Y and dX (nrows x d each).
+ * ---------------------------------------------------------------------- */
+void orc_glu_rows(int64_t T, int64_t d, int64_t F,
+                  const double* X, const double* Wg, const double* Wu, const double* W2, const double* GY,
+                  int act, int64_t nrows, const int64_t* rows, double* Y, double* dX) {
+    (void)T;
+    #pragma omp parallel
+    {
+        double* hg = (double*)malloc(sizeof(double) * (size_t)(F > 0 ? F : 1));
+        double* u = (double*)malloc(sizeof(double) * (size_t)(F > 0 ? F : 1));
+        double* dhg = (double*)malloc(sizeof(double) * (size_t)(F > 0 ? F : 1));
+        double* du = (double*)malloc(sizeof(double) * (size_t)(F > 0 ? F : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nrows; ++i) {
+            int64_t t = rows[i];
+            /* Hg[t,:] = X[t,:] Wg,  U[t,:] = X[t,:] Wu */
+            for (int64_t f = 0; f < F; ++f) { hg[f] = 0.0; u[f] = 0.0; }
+            for (int64_t c = 0; c < d; ++c) {
+                double x = X[t * d + c];
+                for (int64_t f = 0; f < F; ++f) {
+                    hg[f] += x * Wg[c * F + f];
+                    u[f] += x * Wu[c * F + f];
+                }
+            }
+            if (Y) {
+                /* Y[t,:] = (phi(Hg[t,:]) * U[t,:]) W2 */
+                for (int64_t c = 0; c < d; ++c) Y[i * d + c] = 0.0;
+                for (int64_t f = 0; f < F; ++f) {
+                    double a = orc_act(act, hg[f]) * u[f];
+                    for (int64_t c = 0; c < d; ++c) Y[i * d + c] += a * W2[f * d + c];
+                }
+            }
+            if (dX) {
+                for (int64_t f = 0; f < F; ++f) {
+                    double da = 0.0; /* dA[t,f] = G_Y[t,:] . W2[f,:] */
+                    for (int64_t c = 0; c < d; ++c) da += GY[t * d + c] * W2[f * d + c];
+                    du[f] = da * orc_act(act, hg[f]);
+                    dhg[f] = da * u[f] * orc_act_grad(act, hg[f]);
+                }
+                /* dX[t,:] = dHg[t,:] Wg^T + dU[t,:] Wu^T */
+                for (int64_t c = 0; c < d; ++c) {
+                    double s = 0.0;
+                    for (int64_t f = 0; f < F; ++f) s += dhg[f] * Wg[c * F + f];
+                    for (int64_t f = 0; f < F; ++f) s += du[f] * Wu[c * F + f];
+                    dX[i * d + c] = s;
+                }
+            }
+        }
+        free(hg);
+        free(u);
+        free(dhg);
+        free(du);
+    }
+}
+
+/* orc_glu_cols computes, for each selected hidden unit f = cols[j], column f
+ * of dWg and of dWu (written to column j of d x ncols arrays) and row f of
+ * dW2 (row j of an ncols x d array).  Each needs column f of Hg and U over
+ * all T.  Any output may be NULL. */
+void orc_glu_cols(int64_t T, int64_t d, int64_t F,
+                  const double* X, const double* Wg, const double* Wu, const double* W2, const double* GY,
+                  int act, int64_t ncols, const int64_t* cols, double* dWg, double* dWu, double* dW2) {
+    #pragma omp parallel
+    {
+        double* a = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        double* dhg = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        double* du = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t j = 0; j < ncols; ++j) {
+            int64_t f = cols[j];
+            for (int64_t t = 0; t < T; ++t) {
+                double hg = 0.0, u = 0.0, da = 0.0;
+                for (int64_t c = 0; c < d; ++c) hg += X[t * d + c] * Wg[c * F + f];
+                for (int64_t c = 0; c < d; ++c) u += X[t * d + c] * Wu[c * F + f];
+                for (int64_t c = 0; c < d; ++c) da += GY[t * d + c] * W2[f * d + c];
+                a[t] = orc_act(act, hg) * u;
+                du[t] = da * orc_act(act, hg);
+                dhg[t] = da * u * orc_act_grad(act, hg);
+            }
+            for (int64_t c = 0; c < d; ++c) {
+                double sg = 0.0, su = 0.0, s2 = 0.0;
+                for (int64_t t = 0; t < T; ++t) {
+                    sg += X[t * d + c] * dhg[t];
+                    su += X[t * d + c] * du[t];
+                    s2 += a[t] * GY[t * d + c];
+                }
+                if (dWg) dWg[c * ncols + j] = sg;
+                if (dWu) dWu[c * ncols + j] = su;
+                if (dW2) dW2[j * d + c] = s2;
+            }
+        }
+        free(a);
+        free(dhg);
+        free(du);
     }
 }
 

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 
-KINDS = [oracle.ACT_GELU_ERF, oracle.ACT_GELU_TANH, oracle.ACT_TANH]
+KINDS = [oracle.ACT_GELU_ERF, oracle.ACT_GELU_TANH, oracle.ACT_TANH, oracle.ACT_SILU]
 XS = np.linspace(-6.0, 6.0, 241)
 
 
@@ -23,6 +23,8 @@ def test_gelu_matches_torch(orc):
     np.testing.assert_allclose(orc.act(oracle.ACT_GELU_TANH, XS),
                                torch.nn.functional.gelu(x, approximate="tanh").numpy(), rtol=0, atol=1e-15)
     np.testing.assert_allclose(orc.act(oracle.ACT_TANH, XS), np.tanh(XS), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(orc.act(oracle.ACT_SILU, XS), torch.nn.functional.silu(x).numpy(), rtol=0,
+                               atol=1e-15)
 
 
 @pytest.mark.parametrize("kind", KINDS)
@@ -32,6 +34,8 @@ def test_grad_matches_autograd(orc, kind):
         y = torch.nn.functional.gelu(x)
     elif kind == oracle.ACT_GELU_TANH:
         y = torch.nn.functional.gelu(x, approximate="tanh")
+    elif kind == oracle.ACT_SILU:
+        y = torch.nn.functional.silu(x)
     else:
         y = torch.tanh(x)
     y.sum().backward()
@@ -55,6 +59,16 @@ def test_gelu_closed_forms(orc):
     # the tanh approximation stays within 1e-3 of the erf form on [-3, 3]
     x = np.linspace(-3, 3, 601)
     assert np.max(np.abs(orc.act(oracle.ACT_GELU_TANH, x) - orc.act(oracle.ACT_GELU_ERF, x))) < 1e-3
+
+
+def test_silu_closed_forms(orc):
+    # SiLU(0) = 0, SiLU'(0) = 1/2, x s(x) - (-x) s(-x) = x (s(x) + s(-x)) = x,
+    # SiLU(x) -> x for large x and -> 0 for very negative x
+    assert orc.act(oracle.ACT_SILU, 0.0) == 0.0
+    assert orc.act_grad(oracle.ACT_SILU, 0.0) == 0.5
+    np.testing.assert_allclose(orc.act(oracle.ACT_SILU, XS) - orc.act(oracle.ACT_SILU, -XS), XS, rtol=0, atol=1e-14)
+    assert abs(orc.act(oracle.ACT_SILU, 40.0) - 40.0) < 1e-12 and abs(orc.act(oracle.ACT_SILU, -40.0)) < 1e-15
+    assert abs(orc.act(oracle.ACT_SILU, 1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
 
 
 def test_activation_does_not_commute_with_partial_sum(orc):

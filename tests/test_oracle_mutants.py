@@ -45,6 +45,14 @@ MUTANTS = [
      "dz[v] = (v < vocab_real) ? (exp(z[v] - m) / s - (v == y ? 1.0 : 0.0)) : 0.0;", "test_oracle_ce_ex.py"),
     ("ce_ex_denominator_counts_ignored", "(count > 0 ? (double)count : 1.0)", "(T > 0 ? (double)T : 1.0)",
      "test_oracle_ce_ex.py"),
+    ("silu_grad_dropped_term", "return sg + x * sg * (1.0 - sg);", "return sg;", "test_oracle_act.py"),
+    ("glu_gate_and_up_swapped", "double a = orc_act(act, hg[f]) * u[f];", "double a = orc_act(act, u[f]) * hg[f];",
+     "test_oracle_glu.py"),
+    ("glu_dX_missing_up_branch", "for (int64_t f = 0; f < F; ++f) s += du[f] * Wu[c * F + f];",
+     "for (int64_t f = 0; f < F && 0; ++f) s += du[f] * Wu[c * F + f];", "test_oracle_glu.py"),
+    ("glu_dHg_missing_up_factor", "dhg[t] = da * u * orc_act_grad(act, hg);", "dhg[t] = da * orc_act_grad(act, hg);",
+     "test_oracle_glu.py"),
+    ("glu_dWu_wrong_operand", "su += X[t * d + c] * du[t];", "su += X[t * d + c] * dhg[t];", "test_oracle_glu.py"),
     ("ce_sharded_local_max", "for (int64_t j = off[r]; j < off[r + 1]; ++j) sr += exp(z[j] - m);",
      "for (int64_t j = off[r]; j < off[r + 1]; ++j) sr += exp(z[j] - m_r[r]);", "test_oracle_ce.py"),
 ]
