@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libtps.so")
 F32, BF16, I32, I64 = 0, 1, 2, 3
 OK, ERR_SHAPE, ERR_PARTITION, ERR_DTYPE, ERR_LAYOUT, ERR_LABEL, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_ARG = range(10)
 AXES = {"rows": 0, "columns": 1, "inner": 2}
-ACTS = {"gelu": 0, "gelu_erf": 0, "gelu_tanh": 1, "tanh": 2}
+ACTS = {"gelu": 0, "gelu_erf": 0, "gelu_tanh": 1, "tanh": 2, "silu": 3}
 LAYOUTS = {"in_out": 0, "out_in": 1}
 
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16, torch.int32: I32, torch.int64: I64}
@@ -65,6 +65,9 @@ def library():
     lib.tps_matmul_fwd_bwd.argtypes = [P, P, P, i32, i32, P, P, P, vp]
     lib.tps_mlp_fwd_bwd.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, vp, sz, vp]
     lib.tps_mlp_fwd_bwd_noalloc.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, vp]
+    lib.tps_glu_mlp_fwd_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P, P, P, vp, sz, vp]
+    lib.tps_glu_mlp_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
+    lib.tps_glu_mlp_workspace_bytes.restype = sz
     lib.tps_mlp_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     lib.tps_mlp_workspace_bytes.restype = sz
     lib.tps_vocab_ce_fwd_bwd.argtypes = [P, P, P, i32, i32, P, P, P, P, vp, sz, vp]
@@ -225,6 +228,38 @@ def mlp_fwd_bwd_noalloc(X: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, GY:
 
 def ce_workspace_bytes(T: int, V: int, tp: int) -> int:
     return int(library().tps_ce_workspace_bytes(T, V, tp))
+
+
+def glu_mlp_workspace_bytes(T: int, d: int, F: int, tp: int, dtype: torch.dtype) -> int:
+    return int(library().tps_glu_mlp_workspace_bytes(T, d, F, tp, _DTYPES[dtype]))
+
+
+def glu_mlp_fwd_bwd(X: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, W2: torch.Tensor, GY: torch.Tensor,
+                    tp: int, act: str = "silu", weight_layout: str = "in_out",
+                    workspace: Optional[torch.Tensor] = None, out: Optional[Sequence[torch.Tensor]] = None):
+    """Gated tensor-parallel MLP (SwiGLU for act="silu") forward + backward.
+    Returns fp32 (Y, dX, dWg, dWu, dW2)."""
+    _parts(tp, "tp")
+    if act not in ACTS or weight_layout not in LAYOUTS:
+        raise ValueError("argument")
+    d = X.shape[-1]
+    T = X.numel() // d if d else 0
+    F = Wg.shape[1] if weight_layout == "in_out" else Wg.shape[0]
+    dev = X.device
+    if out is None:
+        out = (torch.empty(X.shape, device=dev, dtype=torch.float32),
+               torch.empty(X.shape, device=dev, dtype=torch.float32),
+               torch.empty(Wg.shape, device=dev, dtype=torch.float32),
+               torch.empty(Wu.shape, device=dev, dtype=torch.float32),
+               torch.empty(W2.shape, device=dev, dtype=torch.float32))
+    if workspace is None:
+        need = glu_mlp_workspace_bytes(T, d, F, tp, X.dtype)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    args = [_tt(t) for t in (X, Wg, Wu, W2, GY, *out)]
+    _check(library().tps_glu_mlp_fwd_bwd(*[_ref(a) for a in args[:5]], tp, ACTS[act], LAYOUTS[weight_layout],
+                                         *[_ref(a) for a in args[5:]], ctypes.c_void_p(workspace.data_ptr()),
+                                         workspace.numel() * workspace.element_size(), _stream(dev)))
+    return tuple(out)
 
 
 def vocab_ce_fwd_bwd(h: torch.Tensor, Whead: torch.Tensor, labels: torch.Tensor, tp: int,

@@ -196,13 +196,21 @@ static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream)
   if (g.M == 0 || g.N == 0) return TPS_OK;
   uint32_t* err = dev_err_ptr();
   if (err == nullptr) return fail(TPS_ERR_CUDA, "cannot resolve the device error word");
+  if (g.K == 0 && g.K2 > 0) {  // only the second segment has terms
+    g.a = g.a2; g.a_sm = g.a2_sm; g.a_sk = g.a2_sk;
+    g.b = g.b2; g.b_sk = g.b2_sk; g.b_sn = g.b2_sn;
+    g.K = g.K2; g.K2 = 0;
+  }
   if (g.K == 0) {
     // An empty contraction is the zero matrix; phi(0) = 0 and 0 * phi' = 0
-    // for every supported activation.
-    int rc = launch_fill(g.epi.d, g.epi.mode == EPI_ACT_FWD ? TPS_F32 : g.epi.d_dtype, g.M, g.N, d_sm, d_sn,
-                         stream);
-    if (rc == TPS_OK && g.epi.mode == EPI_ACT_FWD)
+    // for every supported activation, and every gated output is a product
+    // with a zero factor.
+    const int m = g.epi.mode;
+    const bool f32_d = (m == EPI_ACT_FWD || m == EPI_GLU_FWD || m == EPI_GLU_UP);
+    int rc = launch_fill(g.epi.d, f32_d ? TPS_F32 : g.epi.d_dtype, g.M, g.N, d_sm, d_sn, stream);
+    if (rc == TPS_OK && (m == EPI_ACT_FWD || m == EPI_GLU_FWD || m == EPI_GLU_UP || m == EPI_GLU_BWD))
       rc = launch_fill(g.epi.d2, g.epi.d2_dtype, g.M, g.N, g.epi.ldd2, 1, stream);
+    if (rc == TPS_OK && m == EPI_GLU_FWD) rc = launch_fill(g.epi.d3, TPS_F32, g.M, g.N, g.epi.ldd3, 1, stream);
     return rc;
   }
   if (d_sn != 1) {
@@ -216,6 +224,12 @@ static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream)
     t.b = g.a;
     t.b_sk = g.a_sk;
     t.b_sn = g.a_sm;
+    t.a2 = g.b2;
+    t.a2_sm = g.b2_sn;
+    t.a2_sk = g.b2_sk;
+    t.b2 = g.a2;
+    t.b2_sk = g.a2_sk;
+    t.b2_sn = g.a2_sm;
     t.epi.ldd = d_sn;
     g = t;
   } else {
@@ -342,7 +356,7 @@ extern "C" int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const 
   if ((rc = expect(w2, "W2", io ? F : d, io ? d : F))) return rc;
   if ((rc = expect(gy, "GY", T, d))) return rc;
   if (tp < 1) return fail(TPS_ERR_PARTITION, "tp must be >= 1 (got %d)", tp);
-  if (act != TPS_ACT_GELU_ERF && act != TPS_ACT_GELU_TANH && act != TPS_ACT_TANH)
+  if (act != TPS_ACT_GELU_ERF && act != TPS_ACT_GELU_TANH && act != TPS_ACT_TANH && act != TPS_ACT_SILU)
     return fail(TPS_ERR_ARG, "unknown activation %d", act);
   const int dt = x.dtype;
   if ((dt != TPS_F32 && dt != TPS_BF16) || w1.dtype != dt || w2.dtype != dt || gy.dtype != dt)
@@ -428,6 +442,168 @@ extern "C" int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const 
     g.M = T; g.N = d; g.K = F; g.in_dtype = dt;
     g.a = dZ; g.a_sm = F; g.a_sk = 1;
     g.b = w1.data; g.b_sk = w1_out; g.b_sn = w1_in;
+    g.epi.d = dx.data; g.epi.d_dtype = TPS_F32;
+    g.kparts = tp;
+    if ((rc = run_gemm(g, dx.sr, dx.sc, s))) return rc;
+  }
+  return TPS_OK;
+}
+
+// ------------------------------------------------------------ gated MLP
+// Workspace: Hg and U (T x F fp32 each), then A, dHg and dU (T x F in the
+// operand dtype each).
+extern "C" size_t tps_glu_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int32_t dtype) {
+  (void)d;
+  (void)tp;
+  if (T < 0 || F < 0) return 0;
+  const size_t e = (dtype == TPS_F32) ? 4 : 2;
+  const size_t n = static_cast<size_t>(T) * static_cast<size_t>(F);
+  return 2 * align256(n * 4) + 3 * align256(n * e);
+}
+
+extern "C" int tps_glu_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* Wg, const tps_tensor* Wu,
+                                   const tps_tensor* W2, const tps_tensor* GY, int32_t tp, int32_t act,
+                                   int32_t weight_layout, const tps_tensor* Y, const tps_tensor* dX,
+                                   const tps_tensor* dWg, const tps_tensor* dWu, const tps_tensor* dW2,
+                                   void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  t_detail.clear();
+  Mat x, wg, wu, w2, gy, y, dx, dwg, dwu, dw2;
+  int rc;
+  if ((rc = as_mat(X, "X", true, &x)) || (rc = as_mat(Wg, "Wg", false, &wg)) || (rc = as_mat(Wu, "Wu", false, &wu)) ||
+      (rc = as_mat(W2, "W2", false, &w2)) || (rc = as_mat(GY, "GY", true, &gy)))
+    return rc;
+  if (weight_layout != TPS_W_IN_OUT && weight_layout != TPS_W_OUT_IN)
+    return fail(TPS_ERR_ARG, "unknown weight layout %d", weight_layout);
+  const bool io = weight_layout == TPS_W_IN_OUT;
+  const int64_t T = x.rows, d = x.cols;
+  const int64_t F = io ? wg.cols : wg.rows;
+  if ((io ? wg.rows : wg.cols) != d) return fail(TPS_ERR_SHAPE, "Wg does not match X's width %lld", (long long)d);
+  if ((rc = expect(wu, "Wu", wg.rows, wg.cols))) return rc;
+  if ((rc = expect(w2, "W2", io ? F : d, io ? d : F))) return rc;
+  if ((rc = expect(gy, "GY", T, d))) return rc;
+  if (tp < 1) return fail(TPS_ERR_PARTITION, "tp must be >= 1 (got %d)", tp);
+  if (act != TPS_ACT_GELU_ERF && act != TPS_ACT_GELU_TANH && act != TPS_ACT_TANH && act != TPS_ACT_SILU)
+    return fail(TPS_ERR_ARG, "unknown activation %d", act);
+  const int dt = x.dtype;
+  if ((dt != TPS_F32 && dt != TPS_BF16) || wg.dtype != dt || wu.dtype != dt || w2.dtype != dt || gy.dtype != dt)
+    return fail(TPS_ERR_DTYPE, "X, Wg, Wu, W2, GY must all be f32 or all bf16");
+  if ((rc = as_mat(Y, "Y", true, &y)) || (rc = expect(y, "Y", T, d)) || (rc = as_mat(dX, "dX", true, &dx)) ||
+      (rc = expect(dx, "dX", T, d)) || (rc = as_mat(dWg, "dWg", false, &dwg)) ||
+      (rc = expect(dwg, "dWg", wg.rows, wg.cols)) || (rc = as_mat(dWu, "dWu", false, &dwu)) ||
+      (rc = expect(dwu, "dWu", wg.rows, wg.cols)) || (rc = as_mat(dW2, "dW2", false, &dw2)) ||
+      (rc = expect(dw2, "dW2", w2.rows, w2.cols)))
+    return rc;
+  for (const Mat* o : {&y, &dx, &dwg, &dwu, &dw2})
+    if (o->dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "gated MLP results must be f32");
+  const size_t need = tps_glu_mlp_workspace_bytes(T, d, F, tp, dt);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255)))
+    return fail(TPS_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+  const size_t n = static_cast<size_t>(T) * static_cast<size_t>(F);
+  const size_t e = (dt == TPS_F32) ? 4 : 2;
+  char* ws = static_cast<char*>(workspace);
+  float* Hg = reinterpret_cast<float*>(ws);                          // T x F gate pre-activation
+  float* U = reinterpret_cast<float*>(ws + align256(n * 4));         // T x F up projection
+  void* A = ws + 2 * align256(n * 4);                                // T x F phi(Hg) * U
+  void* dHg = ws + 2 * align256(n * 4) + align256(n * e);            // T x F
+  void* dU = ws + 2 * align256(n * 4) + 2 * align256(n * e);         // T x F
+
+  int64_t wg_in, wg_out, wu_in, wu_out, w2_in, w2_out;
+  weight_strides(wg, weight_layout, &wg_in, &wg_out);  // Wg(dd, f)
+  weight_strides(wu, weight_layout, &wu_in, &wu_out);  // Wu(dd, f)
+  weight_strides(w2, weight_layout, &w2_in, &w2_out);  // W2(f, dd)
+  int64_t dwg_in, dwg_out, dwu_in, dwu_out, dw2_in, dw2_out;
+  weight_strides(dwg, weight_layout, &dwg_in, &dwg_out);
+  weight_strides(dwu, weight_layout, &dwu_in, &dwu_out);
+  weight_strides(dw2, weight_layout, &dw2_in, &dw2_out);
+
+  {  // Hg = X Wg, U = X Wu, A = phi(Hg) * U: column-parallel, shard-local gating
+    GemmDesc g;
+    g.name = "glu_gate_up";
+    g.M = T; g.N = F; g.K = d; g.in_dtype = dt;
+    g.a = x.data; g.a_sm = x.sr; g.a_sk = x.sc;
+    g.b = wg.data; g.b_sk = wg_in; g.b_sn = wg_out;
+    g.b_up = wu.data;
+    g.epi.mode = EPI_GLU_FWD; g.epi.act = act;
+    g.epi.d = Hg; g.epi.ldd = F; g.epi.d_dtype = TPS_F32;
+    g.epi.d3 = U; g.epi.ldd3 = F;
+    g.epi.d2 = A; g.epi.ldd2 = F; g.epi.d2_dtype = dt;
+    const bool fused = (wu_in == wg_in && wu_out == wg_out) && (T == 0 || F == 0 || d == 0 || gemm_tc_supported(g));
+    if (fused) {
+      if ((rc = run_gemm(g, F, 1, s))) return rc;
+    } else {  // two GEMMs: Hg, then U with the gating in its epilogue
+      GemmDesc h = g;
+      h.name = "glu_gate";
+      h.b_up = nullptr;
+      h.epi = Epilogue();
+      h.epi.d = Hg; h.epi.d_dtype = TPS_F32;
+      if ((rc = run_gemm(h, F, 1, s))) return rc;
+      GemmDesc u = h;
+      u.name = "glu_up";
+      u.b = wu.data; u.b_sk = wu_in; u.b_sn = wu_out;
+      u.epi.mode = EPI_GLU_UP; u.epi.act = act;
+      u.epi.d = U; u.epi.d_dtype = TPS_F32;
+      u.epi.d2 = A; u.epi.ldd2 = F; u.epi.d2_dtype = dt;
+      u.epi.aux = Hg; u.epi.ld_aux = F;
+      if ((rc = run_gemm(u, F, 1, s))) return rc;
+    }
+  }
+  {  // Y = sum_r A_r W2_r: row-parallel, rank sum in the K loop
+    GemmDesc g;
+    g.name = "glu_down";
+    g.M = T; g.N = d; g.K = F; g.in_dtype = dt;
+    g.a = A; g.a_sm = F; g.a_sk = 1;
+    g.b = w2.data; g.b_sk = w2_in; g.b_sn = w2_out;
+    g.epi.d = y.data; g.epi.d_dtype = TPS_F32;
+    g.kparts = tp;
+    if ((rc = run_gemm(g, y.sr, y.sc, s))) return rc;
+  }
+  {  // dA = GY W2^T; dHg = dA * U * phi'(Hg), dU = dA * phi(Hg), per rank
+    GemmDesc g;
+    g.name = "glu_dgate_dup";
+    g.M = T; g.N = F; g.K = d; g.in_dtype = dt;
+    g.a = gy.data; g.a_sm = gy.sr; g.a_sk = gy.sc;
+    g.b = w2.data; g.b_sk = w2_out; g.b_sn = w2_in;
+    g.epi.mode = EPI_GLU_BWD; g.epi.act = act;
+    g.epi.d = dHg; g.epi.d_dtype = dt;
+    g.epi.d2 = dU; g.epi.ldd2 = F; g.epi.d2_dtype = dt;
+    g.epi.aux = Hg; g.epi.ld_aux = F;
+    g.epi.aux2 = U; g.epi.ld_aux2 = F;
+    if ((rc = run_gemm(g, F, 1, s))) return rc;
+  }
+  {  // dW2(f, dd) = sum_t A[t, f] GY[t, dd]
+    GemmDesc g;
+    g.name = "glu_dW2";
+    g.M = F; g.N = d; g.K = T; g.in_dtype = dt;
+    g.a = A; g.a_sm = 1; g.a_sk = F;
+    g.b = gy.data; g.b_sk = gy.sr; g.b_sn = gy.sc;
+    g.epi.d = dw2.data; g.epi.d_dtype = TPS_F32;
+    if ((rc = run_gemm(g, dw2_in, dw2_out, s))) return rc;
+  }
+  {  // dWg(dd, f) = sum_t X[t, dd] dHg[t, f];  dWu likewise with dU
+    GemmDesc g;
+    g.name = "glu_dWg";
+    g.M = d; g.N = F; g.K = T; g.in_dtype = dt;
+    g.a = x.data; g.a_sm = x.sc; g.a_sk = x.sr;
+    g.b = dHg; g.b_sk = F; g.b_sn = 1;
+    g.epi.d = dwg.data; g.epi.d_dtype = TPS_F32;
+    if ((rc = run_gemm(g, dwg_in, dwg_out, s))) return rc;
+    g.name = "glu_dWu";
+    g.b = dU;
+    g.epi.d = dwu.data;
+    if ((rc = run_gemm(g, dwu_in, dwu_out, s))) return rc;
+  }
+  {  // dX = sum_r (dHg_r Wg_r^T + dU_r Wu_r^T): both branches and the rank
+     // sum in one K loop
+    GemmDesc g;
+    g.name = "glu_dX";
+    g.M = T; g.N = d; g.K = F; g.in_dtype = dt;
+    g.a = dHg; g.a_sm = F; g.a_sk = 1;
+    g.b = wg.data; g.b_sk = wg_out; g.b_sn = wg_in;
+    g.a2 = dU; g.a2_sm = F; g.a2_sk = 1;
+    g.b2 = wu.data; g.b2_sk = wu_out; g.b2_sn = wu_in;
+    g.K2 = F;
     g.epi.d = dx.data; g.epi.d_dtype = TPS_F32;
     g.kparts = tp;
     if ((rc = run_gemm(g, dx.sr, dx.sc, s))) return rc;

@@ -1,6 +1,7 @@
 // epilogue.cuh -- per-element epilogue arithmetic shared by the tensor-core
 // and SIMT GEMM kernels: plain store, activation forward (pre-activation and
-// activation), activation backward (multiply by phi' of the pre-activation).
+// activation), activation backward (multiply by phi' of the pre-activation),
+// and the gated MLP's forms (gate times up, and its backward).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -80,6 +81,13 @@ __device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, i
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = act_fwd(e.act, v[i]);
     store_run32(e.d2, e.d2_dtype, row * e.ldd2 + col0, n, v);
+  } else if (e.mode == EPI_GLU_UP) {
+    if (e.d != nullptr) store_run32(e.d, TPS_F32, row * e.ldd + col0, n, v);
+    float a[32];
+    load_run32(e.aux + row * e.ld_aux + col0, n, a);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= act_fwd(e.act, a[i]);
+    store_run32(e.d2, e.d2_dtype, row * e.ldd2 + col0, n, v);
   } else {
     float a[32];
     load_run32(e.aux + row * e.ld_aux + col0, n, a);
@@ -89,6 +97,36 @@ __device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, i
   }
 }
 
+// EPI_GLU_BWD without TMA stores (kept apart from epilogue_run32 so that
+// the kernels which never run it do not carry its registers).
+__device__ __forceinline__ void epilogue_glu_bwd_run32(const Epilogue& e, int64_t row, int64_t col0, int n,
+                                                       float (&v)[32]) {
+  float hg[32], u[32];
+  load_run32(e.aux + row * e.ld_aux + col0, n, hg);
+  load_run32(e.aux2 + row * e.ld_aux2 + col0, n, u);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float f, g;
+    act_fwd_grad(e.act, hg[i], f, g);
+    const float da = v[i];
+    v[i] = da * u[i] * g;
+    u[i] = da * f;
+  }
+  store_run32(e.d, e.d_dtype, row * e.ldd + col0, n, v);
+  store_run32(e.d2, e.d2_dtype, row * e.ldd2 + col0, n, u);
+}
+
+// EPI_GLU_FWD without TMA stores: `hg` and `u` are the gate and up
+// accumulators of the same 32 columns.
+__device__ __forceinline__ void epilogue_glu_run32(const Epilogue& e, int64_t row, int64_t col0, int n,
+                                                   float (&hg)[32], float (&u)[32]) {
+  store_run32(e.d, TPS_F32, row * e.ldd + col0, n, hg);
+  store_run32(e.d3, TPS_F32, row * e.ldd3 + col0, n, u);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) u[i] *= act_fwd(e.act, hg[i]);
+  store_run32(e.d2, e.d2_dtype, row * e.ldd2 + col0, n, u);
+}
+
 // Scalar form used by the SIMT kernel.
 __device__ __forceinline__ void epilogue_elem(const Epilogue& e, int64_t row, int64_t col, float v) {
   if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
@@ -96,6 +134,14 @@ __device__ __forceinline__ void epilogue_elem(const Epilogue& e, int64_t row, in
   } else if (e.mode == EPI_ACT_FWD) {
     if (e.d != nullptr) store_elem(e.d, TPS_F32, row * e.ldd + col, v);
     store_elem(e.d2, e.d2_dtype, row * e.ldd2 + col, act_fwd(e.act, v));
+  } else if (e.mode == EPI_GLU_UP) {
+    if (e.d != nullptr) store_elem(e.d, TPS_F32, row * e.ldd + col, v);
+    store_elem(e.d2, e.d2_dtype, row * e.ldd2 + col, v * act_fwd(e.act, e.aux[row * e.ld_aux + col]));
+  } else if (e.mode == EPI_GLU_BWD) {
+    float f, g;
+    act_fwd_grad(e.act, e.aux[row * e.ld_aux + col], f, g);
+    store_elem(e.d, e.d_dtype, row * e.ldd + col, v * e.aux2[row * e.ld_aux2 + col] * g);
+    store_elem(e.d2, e.d2_dtype, row * e.ldd2 + col, v * f);
   } else {
     store_elem(e.d, e.d_dtype, row * e.ldd + col, v * act_grad(e.act, e.aux[row * e.ld_aux + col]));
   }

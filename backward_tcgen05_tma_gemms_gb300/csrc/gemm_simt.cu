@@ -7,7 +7,9 @@
 // ("Sharded GEMM与Backprop：行、列、内维三种切分", 解题路线 steps 2-4: a
 // result that needs sum/all-reduce), each rank's partial product over its
 // array_split segment of K is accumulated separately and the partials are
-// then added in rank order, inside the kernel.
+// then added in rank order, inside the kernel.  A second contraction
+// segment (D = A B + A2 B2) adds each rank's segment of the second pair to
+// the same rank partial.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -19,11 +21,15 @@ namespace tps {
 constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16, SG_THREADS = 256;
 
 struct SimtParams {
-  int64_t M, N, K;
+  int64_t M, N, K, K2;
   const void* a;
   int64_t a_sm, a_sk;
   const void* b;
   int64_t b_sk, b_sn;
+  const void* a2;
+  int64_t a2_sm, a2_sk;
+  const void* b2;
+  int64_t b2_sk, b2_sn;
   int32_t kparts;
   Epilogue epi;
 };
@@ -34,6 +40,56 @@ __device__ __forceinline__ float ld_as_float(const void* base, int64_t idx) {
     return static_cast<const float*>(base)[idx];
   else
     return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[idx]);
+}
+
+// part += A[m0.., kb..ke) B[kb..ke, n0..) for this thread's 4 x 4 outputs.
+template <typename T>
+__device__ __forceinline__ void simt_segment(const void* a, int64_t a_sm, int64_t a_sk, const void* b, int64_t b_sk,
+                                             int64_t b_sn, int64_t M, int64_t N, int64_t m0, int64_t n0, int64_t kb,
+                                             int64_t ke, float (&As)[SG_BK][SG_BM + 4], float (&Bs)[SG_BK][SG_BN + 4],
+                                             float (&part)[4][4]) {
+  const int tid = threadIdx.x;
+  const int tx = tid % 16, ty = tid / 16;
+  for (int64_t k0 = kb; k0 < ke; k0 += SG_BK) {
+    for (int e = tid; e < SG_BM * SG_BK; e += SG_THREADS) {
+      int mm, kk;
+      if (a_sk == 1) {
+        mm = e / SG_BK;
+        kk = e % SG_BK;
+      } else {
+        mm = e % SG_BM;
+        kk = e / SG_BM;
+      }
+      const int64_t m = m0 + mm, k = k0 + kk;
+      As[kk][mm] = (m < M && k < ke) ? ld_as_float<T>(a, m * a_sm + k * a_sk) : 0.0f;
+    }
+    for (int e = tid; e < SG_BN * SG_BK; e += SG_THREADS) {
+      int nn, kk;
+      if (b_sk == 1) {
+        nn = e / SG_BK;
+        kk = e % SG_BK;
+      } else {
+        nn = e % SG_BN;
+        kk = e / SG_BN;
+      }
+      const int64_t n = n0 + nn, k = k0 + kk;
+      Bs[kk][nn] = (n < N && k < ke) ? ld_as_float<T>(b, k * b_sk + n * b_sn) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < SG_BK; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
+    }
+    __syncthreads();
+  }
 }
 
 template <typename T>
@@ -52,54 +108,16 @@ __global__ void __launch_bounds__(SG_THREADS) gemm_simt_kernel(const SimtParams 
     for (int j = 0; j < 4; ++j) total[i][j] = 0.0f;
 
   for (int32_t r = 0; r < p.kparts; ++r) {
-    const int64_t kb = shard_offset(p.K, p.kparts, r);
-    const int64_t ke = shard_offset(p.K, p.kparts, r + 1);
     float part[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) part[i][j] = 0.0f;
-
-    for (int64_t k0 = kb; k0 < ke; k0 += SG_BK) {
-      for (int e = tid; e < SG_BM * SG_BK; e += SG_THREADS) {
-        int mm, kk;
-        if (p.a_sk == 1) {
-          mm = e / SG_BK;
-          kk = e % SG_BK;
-        } else {
-          mm = e % SG_BM;
-          kk = e / SG_BM;
-        }
-        const int64_t m = m0 + mm, k = k0 + kk;
-        As[kk][mm] = (m < p.M && k < ke) ? ld_as_float<T>(p.a, m * p.a_sm + k * p.a_sk) : 0.0f;
-      }
-      for (int e = tid; e < SG_BN * SG_BK; e += SG_THREADS) {
-        int nn, kk;
-        if (p.b_sk == 1) {
-          nn = e / SG_BK;
-          kk = e % SG_BK;
-        } else {
-          nn = e % SG_BN;
-          kk = e / SG_BN;
-        }
-        const int64_t n = n0 + nn, k = k0 + kk;
-        Bs[kk][nn] = (n < p.N && k < ke) ? ld_as_float<T>(p.b, k * p.b_sk + n * p.b_sn) : 0.0f;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int kk = 0; kk < SG_BK; ++kk) {
-        float av[4], bv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
-      }
-      __syncthreads();
-    }
+    simt_segment<T>(p.a, p.a_sm, p.a_sk, p.b, p.b_sk, p.b_sn, p.M, p.N, m0, n0, shard_offset(p.K, p.kparts, r),
+                    shard_offset(p.K, p.kparts, r + 1), As, Bs, part);
+    if (p.K2 > 0)
+      simt_segment<T>(p.a2, p.a2_sm, p.a2_sk, p.b2, p.b2_sk, p.b2_sn, p.M, p.N, m0, n0,
+                      shard_offset(p.K2, p.kparts, r), shard_offset(p.K2, p.kparts, r + 1), As, Bs, part);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -129,12 +147,20 @@ int launch_gemm_simt(const GemmDesc& g, uint32_t* /*dev_err*/, cudaStream_t stre
   p.b = g.b;
   p.b_sk = g.b_sk;
   p.b_sn = g.b_sn;
+  p.K2 = g.K2;
+  p.a2 = g.a2;
+  p.a2_sm = g.a2_sm;
+  p.a2_sk = g.a2_sk;
+  p.b2 = g.b2;
+  p.b2_sk = g.b2_sk;
+  p.b2_sn = g.b2_sn;
   p.kparts = g.kparts < 1 ? 1 : g.kparts;
+  if (g.epi.mode == EPI_GLU_FWD) return TPS_ERR_ARG;  // the fused gate/up form is tensor-core only
   p.epi = g.epi;
   const int64_t gx = (g.N + SG_BN - 1) / SG_BN, gy = (g.M + SG_BM - 1) / SG_BM;
   if (gx > 0x7FFFFFFF || gy > 65535) return TPS_ERR_SHAPE;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
-  ProfScope prof("gemm_simt", g.name, 2.0 * double(g.M) * double(g.N) * double(g.K), 0.0, stream);
+  ProfScope prof("gemm_simt", g.name, 2.0 * double(g.M) * double(g.N) * (double(g.K) + double(g.K2)), 0.0, stream);
   if (g.in_dtype == TPS_F32)
     gemm_simt_kernel<float><<<grid, SG_THREADS, 0, stream>>>(p);
   else

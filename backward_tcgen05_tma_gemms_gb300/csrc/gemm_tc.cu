@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t* stg_bf16 = staging + 4 * TC_STG_F32_BYTES + (warp - 2) * TC_STG_BF16_BYTES;
     const Epilogue& e = p.epi;
     const bool ce = (e.mode == EPI_CE_STATS);
-    const bool bwd = p.tma_store && e.mode == EPI_ACT_BWD;
+    const bool bwd = p.tma_store && (e.mode == EPI_ACT_BWD || e.mode == EPI_GLU_UP);  // AUX prefetch
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mt, nt;
@@ -350,10 +350,13 @@ void tc_raster_choice(int m_tiles, int* raster_n, int* group, int* pol_a, int* p
 // The tensor-core path needs bf16 operands that TMA can describe: 16-byte
 // aligned base, unit stride in one dimension and a pitch that is a multiple
 // of 16 bytes.
+// The gated forms need their second operands to qualify too, with the same
+// contiguous dimension.
 bool gemm_tc_supported(const GemmDesc& g) {
   if (g.in_dtype != TPS_BF16) return false;
-  if (g.M < 1 || g.N < 1 || g.K < 1) return false;
-  if (g.M >= (1ll << 31) || g.N >= (1ll << 31) || g.K >= (1ll << 31)) return false;
+  if (g.M < 1 || g.N < 1 || g.K < 1 || g.K2 < 0) return false;
+  if (g.M >= (1ll << 31) || g.N >= (1ll << 31) || g.K >= (1ll << 31) || g.K2 >= (1ll << 31)) return false;
+  if (g.epi.mode == EPI_GLU_FWD && (g.b_up == nullptr || g.K2 > 0)) return false;
   auto ok_operand = [](const void* ptr, int64_t s_outer, int64_t s_inner, int64_t inner_extent) {
     if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return false;
     if (s_inner != 1) return false;
@@ -362,15 +365,40 @@ bool gemm_tc_supported(const GemmDesc& g) {
   };
   const bool a_ok = (g.a_sk == 1) ? ok_operand(g.a, g.a_sm, g.a_sk, g.K) : ok_operand(g.a, g.a_sk, g.a_sm, g.M);
   const bool b_ok = (g.b_sk == 1) ? ok_operand(g.b, g.b_sn, g.b_sk, g.K) : ok_operand(g.b, g.b_sk, g.b_sn, g.N);
-  return a_ok && b_ok;
+  if (!a_ok || !b_ok) return false;
+  if (g.epi.mode == EPI_GLU_FWD &&
+      !((g.b_sk == 1) ? ok_operand(g.b_up, g.b_sn, g.b_sk, g.K) : ok_operand(g.b_up, g.b_sk, g.b_sn, g.N)))
+    return false;
+  if (g.K2 > 0) {
+    if ((g.a2_sk == 1) != (g.a_sk == 1) || (g.b2_sk == 1) != (g.b_sk == 1)) return false;
+    const bool a2_ok =
+        (g.a2_sk == 1) ? ok_operand(g.a2, g.a2_sm, g.a2_sk, g.K2) : ok_operand(g.a2, g.a2_sk, g.a2_sm, g.M);
+    const bool b2_ok =
+        (g.b2_sk == 1) ? ok_operand(g.b2, g.b2_sn, g.b2_sk, g.K2) : ok_operand(g.b2, g.b2_sk, g.b2_sn, g.N);
+    if (!a2_ok || !b2_ok) return false;
+  }
+  return true;
 }
 
 // Output maps for the TMA-store epilogue; false when an output cannot be
-// described (the kernels then store directly).
-bool tc_make_output_maps(const GemmDesc& g, CUtensorMap* td, CUtensorMap* td2) {
+// described (the kernels then store directly).  `td3` (U of EPI_GLU_FWD)
+// may be null for the other modes.
+bool tc_make_output_maps(const GemmDesc& g, CUtensorMap* td, CUtensorMap* td2, CUtensorMap* td3) {
   memset(td, 0, sizeof(*td));
   memset(td2, 0, sizeof(*td2));
-  if (g.epi.mode == EPI_ACT_FWD) {
+  if (td3) memset(td3, 0, sizeof(*td3));
+  if (g.epi.mode == EPI_GLU_FWD) {  // Hg and U fp32, A bf16, 128-wide hidden-unit tiles
+    return td3 != nullptr && g.epi.d2_dtype == TPS_BF16 &&
+           tc_make_out_map(td, g.epi.d, g.M, g.N, g.epi.ldd, TPS_F32) &&
+           tc_make_out_map(td3, g.epi.d3, g.M, g.N, g.epi.ldd3, TPS_F32) &&
+           tc_make_out_map(td2, g.epi.d2, g.M, g.N, g.epi.ldd2, TPS_BF16);
+  }
+  if (g.epi.mode == EPI_GLU_BWD) {  // dHg and dU leave as two bf16 boxes
+    return g.epi.d_dtype == TPS_BF16 && g.epi.d2_dtype == TPS_BF16 &&
+           tc_make_out_map(td, g.epi.d, g.M, g.N, g.epi.ldd, TPS_BF16) &&
+           tc_make_out_map(td2, g.epi.d2, g.M, g.N, g.epi.ldd2, TPS_BF16);
+  }
+  if (g.epi.mode == EPI_ACT_FWD || g.epi.mode == EPI_GLU_UP) {
     bool ok = true;
     if (g.epi.d != nullptr) ok = tc_make_out_map(td, g.epi.d, g.M, g.N, g.epi.ldd, TPS_F32);
     return ok && g.epi.d2_dtype == TPS_BF16 && tc_make_out_map(td2, g.epi.d2, g.M, g.N, g.epi.ldd2, TPS_BF16);
@@ -395,6 +423,8 @@ static int launch_typed(const GemmDesc& g, const CUtensorMap& ta, const CUtensor
 }
 
 int launch_gemm_tc1(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
+  // the gated forms and a second K segment exist on CTA pairs only
+  if (g.epi.mode == EPI_GLU_FWD || g.epi.mode == EPI_GLU_BWD || g.K2 > 0) return TPS_ERR_ARG;
   const bool a_mn = (g.a_sk != 1);
   const bool b_mn = (g.b_sk != 1);
   CUtensorMap ta, tb;
@@ -416,7 +446,7 @@ int launch_gemm_tc1(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   p.epi = g.epi;
   p.err = dev_err;
   CUtensorMap td, td2;
-  p.tma_store = tc_make_output_maps(g, &td, &td2) ? 1 : 0;
+  p.tma_store = tc_make_output_maps(g, &td, &td2, nullptr) ? 1 : 0;
   const int sms = tc_num_sms();
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
 
@@ -427,11 +457,13 @@ int launch_gemm_tc1(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
 }
 
 // Kernel choice: CTA pairs (gemm_tc2.cu) when M spans at least one 256-row
-// pair tile, else single CTAs.  TPS_GEMM_KERNEL=1 or 2 forces one.
+// pair tile, else single CTAs.  TPS_GEMM_KERNEL=1 or 2 forces one, except
+// that the gated forms and a second K segment always run on CTA pairs.
 int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   const char* kv = getenv("TPS_GEMM_KERNEL");
   const int forced = kv ? atoi(kv) : 0;
-  const bool pair = forced == 2 || (forced != 1 && g.M >= 256);
+  const bool pair_only = g.epi.mode == EPI_GLU_FWD || g.epi.mode == EPI_GLU_BWD || g.K2 > 0;
+  const bool pair = pair_only || forced == 2 || (forced != 1 && g.M >= 256);
   return pair ? launch_gemm_tc2(g, dev_err, stream) : launch_gemm_tc1(g, dev_err, stream);
 }
 

@@ -18,11 +18,22 @@
 //   tmem_full[b]  each CTA: arrived by the MMA commit multicast to the pair
 //   tmem_empty[b] even CTA only: one arrival per epilogue warp of each CTA
 //
+// Gated MLP forward (EPI_GLU_FWD): the even CTA stages 128 columns of the
+// gate weight and the odd CTA the same 128 columns of the up weight, so each
+// CTA's accumulator holds, for its 128 rows, the gate (columns 0..127) and
+// the up projection (128..255) of the same 128 hidden units, and the
+// epilogue forms phi(gate) * up without leaving the SM.  A pair tile then
+// covers 128 hidden units.
+//
+// A second contraction segment (GemmDesc::K2) continues the K loop with the
+// operands A2 and B2 into the same accumulator: D = A B + A2 B2.
+//
 // Warp roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one thread)
 //   warp 1      TMEM allocator; MMA issuer on the even CTA (one thread)
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 and
-//               columns 128*((w-2)/4)..+127 of the accumulator
+//               columns 128*((w-2)/4)..+127 of the accumulator (gated:
+//               hidden units 64*((w-2)/4)..+63, gate and up)
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -63,17 +74,24 @@ static_assert(T2_SMEM_BYTES <= 232448, "exceeds the opt-in shared memory per blo
 struct T2Params {
   int M, N, K;
   int m_tiles, n_tiles, k_tiles, num_tiles;  // m_tiles counts 256-row pair tiles
+  int k_tiles1;                              // K tiles of the first segment
+  int glu;                                   // EPI_GLU_FWD: B2 is the up weight
   int raster_n, group;
   int tma_store;
   Epilogue epi;
   uint32_t* err;
 };
 
-template <bool A_MN, bool B_MN>
+// Epilogue families, compiled as separate kernels so that the gated forms'
+// extra live registers do not cost the plain ones a spill.
+enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2 };
+
+template <bool A_MN, bool B_MN, int FAM>
 __global__ void __launch_bounds__(T2_THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                     const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
-                    const T2Params p) {
+                    const __grid_constant__ CUtensorMap tmD3, const T2Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -103,6 +121,8 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.k_tiles1 < p.k_tiles) tma_prefetch_desc(&tmA2);
+    if (p.glu || p.k_tiles1 < p.k_tiles) tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
     tmem_alloc_pair(&bars->tmem_slot, T2_TMEM_COLS);
@@ -125,7 +145,9 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         int mt, nt;
         tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
         const int m0 = mt * 2 * T2_BM + static_cast<int>(rank) * T2_BM;
-        const int nb0 = nt * T2_BN + static_cast<int>(rank) * T2_BN_CTA;
+        // gated: both CTAs stage the same 128 hidden units, gate or up
+        const int nb0 = p.glu ? nt * T2_BN_CTA : nt * T2_BN + static_cast<int>(rank) * T2_BN_CTA;
+        const CUtensorMap* mb1 = (p.glu && rank == 1) ? &tmB2 : &tmB;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -135,19 +157,22 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
           uint8_t* sb = sa + T2_A_BYTES;
           if (rank == 0) mbar_expect_tx(&bars->full[stage], 2 * T2_STAGE_BYTES);
           const uint32_t fb = full0_leader + stage * static_cast<uint32_t>(sizeof(uint64_t));
-          const int k0 = kt * TC_BK;
+          const bool seg2 = kt >= p.k_tiles1;
+          const CUtensorMap* ma = seg2 ? &tmA2 : &tmA;
+          const CUtensorMap* mb = seg2 ? &tmB2 : mb1;
+          const int k0 = (seg2 ? kt - p.k_tiles1 : kt) * TC_BK;
           if (!A_MN) {
-            tma_load_2d_pair(sa, &tmA, fb, k0, m0);
+            tma_load_2d_pair(sa, ma, fb, k0, m0);
           } else {
 #pragma unroll
-            for (int j = 0; j < T2_BM / 64; ++j) tma_load_2d_pair(sa + j * TC_MN_BOX_BYTES, &tmA, fb, m0 + 64 * j, k0);
+            for (int j = 0; j < T2_BM / 64; ++j) tma_load_2d_pair(sa + j * TC_MN_BOX_BYTES, ma, fb, m0 + 64 * j, k0);
           }
           if (!B_MN) {
-            tma_load_2d_pair(sb, &tmB, fb, k0, nb0);
+            tma_load_2d_pair(sb, mb, fb, k0, nb0);
           } else {
 #pragma unroll
             for (int j = 0; j < T2_BN_CTA / 64; ++j)
-              tma_load_2d_pair(sb + j * TC_MN_BOX_BYTES, &tmB, fb, nb0 + 64 * j, k0);
+              tma_load_2d_pair(sb + j * TC_MN_BOX_BYTES, mb, fb, nb0 + 64 * j, k0);
           }
           ++issued;
           if (++stage == T2_STAGES) {
@@ -211,19 +236,24 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     uint8_t* stg = staging + ew * 2 * T2_STG_BUF;
     const Epilogue& e = p.epi;
     const bool ce = (e.mode == EPI_CE_STATS);
-    const bool bwd = p.tma_store && e.mode == EPI_ACT_BWD;
+    const bool bwd = p.tma_store && (e.mode == EPI_ACT_BWD || e.mode == EPI_GLU_UP);  // AUX prefetch
+    constexpr bool glu = FAM == T2_GLU_FWD;
+    constexpr bool gbwd = FAM == T2_GLU_BWD;
+    // accumulator columns this warp drains: 128 (gated: 64 gate + 64 up)
+    const int warp_cols = glu ? T2_BN_CTA / 2 : T2_BN / 2;
     uint32_t acc = 0, acc_phase = 0, chunk = 0;
     for (int tile = pair; tile < p.num_tiles; tile += npairs) {
       int mt, nt;
       tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
       const int m0 = mt * 2 * T2_BM + static_cast<int>(rank) * T2_BM;
-      const int nh0 = nt * T2_BN + h * (T2_BN / 2);  // first column of this warp's half
+      // first output column of this warp's part of the tile
+      const int nh0 = glu ? nt * T2_BN_CTA + h * warp_cols : nt * T2_BN + h * warp_cols;
       if (!mbar_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const int row0 = m0 + q * 32;
       const int64_t row = row0 + lane;
       const uint32_t t_row =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * T2_BN + static_cast<uint32_t>(h * (T2_BN / 2));
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * T2_BN + static_cast<uint32_t>(h * warp_cols);
       float a_next[32];
       if (bwd) {
         if (row < p.M && nh0 < p.N) {
@@ -234,16 +264,59 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         }
       }
       CeTileAcc st;
-      for (int c = 0; c < (T2_BN / 2) / 32; ++c) {
+      for (int c = 0; c < warp_cols / 32; ++c) {
         const int col0 = nh0 + c * 32;
         if (col0 >= p.N) break;  // warp-uniform
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
+        if constexpr (glu) {  // gate in r, the same hidden units' up projection 128 columns on
+          uint32_t r2[32];
+          tmem_ld_32x32b_x32(t_row + T2_BN_CTA + c * 32, r2);
+          tmem_ld_wait();
+          float hg[32], u[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            hg[i] = __uint_as_float(r[i]);
+            u[i] = __uint_as_float(r2[i]);
+          }
+          if (!p.tma_store) {
+            if (row < p.M) epilogue_glu_run32(e, row, col0, min(32, p.N - col0), hg, u);
+          } else {
+            tc_store_glu_chunk(e, &tmD, &tmD2, &tmD3, stg, lane, row0, col0, hg, u);
+          }
+          continue;
+        }
+        if constexpr (gbwd) {
+          if (p.tma_store) {
+            float hg[32], u[32];  // Hg and U of these 32 columns
+            if (row < p.M) {
+              load_run32(e.aux + row * e.ld_aux + col0, min(32, p.N - col0), hg);
+              load_run32(e.aux2 + row * e.ld_aux2 + col0, min(32, p.N - col0), u);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) hg[i] = u[i] = 0.0f;
+            }
+            tmem_ld_wait();
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            uint8_t* buf = stg + (chunk & 1u) * T2_STG_BUF;
+            tc_store_glu_bwd_chunk(e, &tmD, &tmD2, buf, buf + TC_STG_F32_BYTES, lane, row0, col0, v, hg, u);
+            ++chunk;
+          } else {
+            tmem_ld_wait();
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            if (row < p.M) epilogue_glu_bwd_run32(e, row, col0, min(32, p.N - col0), v);
+          }
+          continue;
+        }
         float a[32];
         if (bwd) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = a_next[i];
-          if (row < p.M && col0 + 32 < p.N && c + 1 < (T2_BN / 2) / 32)
+          if (row < p.M && col0 + 32 < p.N && c + 1 < warp_cols / 32)
             load_run32(e.aux + row * e.ld_aux + col0 + 32, min(32, p.N - col0 - 32), a_next);
         }
         tmem_ld_wait();
@@ -254,7 +327,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         if (ce) {
           if (c == 0) st.reset(e, p.N, col0);
           st.fold(v, col0, n, e.ce_vreal);
-          if ((c == (T2_BN / 2) / 32 - 1 || col0 + 32 >= p.N) && row < p.M)
+          if ((c == warp_cols / 32 - 1 || col0 + 32 >= p.N) && row < p.M)
             st.flush(e, row, static_cast<int64_t>(nh0) / kStatsTileN);
         }
         if (!p.tma_store) {
@@ -282,16 +355,19 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
 
 // ------------------------------------------------------------------ host
 
-bool tc_make_output_maps(const GemmDesc& g, CUtensorMap* td, CUtensorMap* td2);
+bool tc_make_output_maps(const GemmDesc& g, CUtensorMap* td, CUtensorMap* td2, CUtensorMap* td3);
 
-template <bool A_MN, bool B_MN>
-static int launch_pair_typed(const GemmDesc& g, const CUtensorMap& ta, const CUtensorMap& tb,
-                             const CUtensorMap& td, const CUtensorMap& td2, const T2Params& p, int pairs,
+struct T2Maps {
+  CUtensorMap a, b, a2, b2, d, d2, d3;
+};
+
+template <bool A_MN, bool B_MN, int FAM>
+static int launch_pair_typed(const GemmDesc& g, const T2Maps& m, const T2Params& p, int pairs,
                              cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN, FAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(T2_SMEM_BYTES));
   });
   if (attr_err != cudaSuccess) return TPS_ERR_CUDA;
@@ -307,29 +383,63 @@ static int launch_pair_typed(const GemmDesc& g, const CUtensorMap& ta, const CUt
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  ProfScope prof("gemm_tc", g.name, 2.0 * double(g.M) * double(g.N) * double(g.K), 0.0, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN>, ta, tb, td, td2, p);
+  const double flops = 2.0 * double(g.M) * double(g.N) * (double(g.K) + double(g.K2)) * (p.glu ? 2.0 : 1.0);
+  ProfScope prof("gemm_tc", g.name, flops, 0.0, stream);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN, FAM>, m.a, m.b, m.a2, m.b2, m.d, m.d2, m.d3, p);
   note_launch();
   return e == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
+}
+
+template <int FAM>
+static int launch_pair_majors(const GemmDesc& g, const T2Maps& m, const T2Params& p, int pairs, bool a_mn,
+                              bool b_mn, cudaStream_t stream) {
+  if (!a_mn && !b_mn) return launch_pair_typed<false, false, FAM>(g, m, p, pairs, stream);
+  if (!a_mn && b_mn) return launch_pair_typed<false, true, FAM>(g, m, p, pairs, stream);
+  if (a_mn && !b_mn) return launch_pair_typed<true, false, FAM>(g, m, p, pairs, stream);
+  return launch_pair_typed<true, true, FAM>(g, m, p, pairs, stream);
+}
+
+static int launch_pair_family(const GemmDesc& g, const T2Maps& m, const T2Params& p, int pairs, bool a_mn,
+                              bool b_mn, cudaStream_t stream) {
+  if (g.epi.mode == EPI_GLU_FWD) return launch_pair_majors<T2_GLU_FWD>(g, m, p, pairs, a_mn, b_mn, stream);
+  if (g.epi.mode == EPI_GLU_BWD) return launch_pair_majors<T2_GLU_BWD>(g, m, p, pairs, a_mn, b_mn, stream);
+  return launch_pair_majors<T2_PLAIN>(g, m, p, pairs, a_mn, b_mn, stream);
+}
+
+static bool pair_operand_map(CUtensorMap* map, const void* base, bool mn, int64_t K, int64_t MN, int64_t ld,
+                             int box_mn) {
+  return mn ? tc_make_map(map, base, K, MN, ld, 64, TC_BK)       // stored K x MN
+            : tc_make_map(map, base, MN, K, ld, TC_BK, box_mn);  // stored MN x K
 }
 
 int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   const bool a_mn = (g.a_sk != 1);
   const bool b_mn = (g.b_sk != 1);
-  CUtensorMap ta, tb;
-  bool ok = a_mn ? tc_make_map(&ta, g.a, g.K, g.M, g.a_sk, 64, TC_BK)       // stored K x M
-                 : tc_make_map(&ta, g.a, g.M, g.K, g.a_sm, TC_BK, T2_BM);    // stored M x K
-  ok = ok && (b_mn ? tc_make_map(&tb, g.b, g.K, g.N, g.b_sk, 64, TC_BK)      // stored K x N
-                   : tc_make_map(&tb, g.b, g.N, g.K, g.b_sn, TC_BK, T2_BN_CTA));  // stored N x K
+  const bool glu = g.epi.mode == EPI_GLU_FWD;
+  const bool seg2 = g.K2 > 0;
+  if (glu && (seg2 || g.b_up == nullptr)) return TPS_ERR_ARG;
+  if (seg2 && ((g.a2_sk != 1) != a_mn || (g.b2_sk != 1) != b_mn)) return TPS_ERR_LAYOUT;
+  T2Maps m;
+  memset(&m, 0, sizeof(m));
+  bool ok = pair_operand_map(&m.a, g.a, a_mn, g.K, g.M, a_mn ? g.a_sk : g.a_sm, T2_BM);
+  ok = ok && pair_operand_map(&m.b, g.b, b_mn, g.K, g.N, b_mn ? g.b_sk : g.b_sn, T2_BN_CTA);
+  if (glu) ok = ok && pair_operand_map(&m.b2, g.b_up, b_mn, g.K, g.N, b_mn ? g.b_sk : g.b_sn, T2_BN_CTA);
+  if (seg2) {
+    ok = ok && pair_operand_map(&m.a2, g.a2, a_mn, g.K2, g.M, a_mn ? g.a2_sk : g.a2_sm, T2_BM);
+    ok = ok && pair_operand_map(&m.b2, g.b2, b_mn, g.K2, g.N, b_mn ? g.b2_sk : g.b2_sn, T2_BN_CTA);
+  }
   if (!ok) return TPS_ERR_CUDA;
 
   T2Params p;
   p.M = static_cast<int>(g.M);
   p.N = static_cast<int>(g.N);
   p.K = static_cast<int>(g.K);
+  p.glu = glu ? 1 : 0;
   p.m_tiles = static_cast<int>((g.M + 2 * T2_BM - 1) / (2 * T2_BM));
-  p.n_tiles = static_cast<int>((g.N + T2_BN - 1) / T2_BN);
-  p.k_tiles = static_cast<int>((g.K + TC_BK - 1) / TC_BK);
+  p.n_tiles = static_cast<int>(glu ? (g.N + T2_BN_CTA - 1) / T2_BN_CTA : (g.N + T2_BN - 1) / T2_BN);
+  p.k_tiles1 = static_cast<int>((g.K + TC_BK - 1) / TC_BK);
+  p.k_tiles = p.k_tiles1 + static_cast<int>((g.K2 + TC_BK - 1) / TC_BK);
   p.num_tiles = p.m_tiles * p.n_tiles;
   int pol_a = 0, pol_b = 0;
   // groups of pair tiles cover the same rows as twice as many single tiles
@@ -339,15 +449,11 @@ int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   if (p.group > p.m_tiles) p.group = p.m_tiles;
   p.epi = g.epi;
   p.err = dev_err;
-  CUtensorMap td, td2;
-  p.tma_store = tc_make_output_maps(g, &td, &td2) ? 1 : 0;
+  p.tma_store = tc_make_output_maps(g, &m.d, &m.d2, &m.d3) ? 1 : 0;
   const int max_pairs = tc_num_sms() / 2;
   const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
 
-  if (!a_mn && !b_mn) return launch_pair_typed<false, false>(g, ta, tb, td, td2, p, pairs, stream);
-  if (!a_mn && b_mn) return launch_pair_typed<false, true>(g, ta, tb, td, td2, p, pairs, stream);
-  if (a_mn && !b_mn) return launch_pair_typed<true, false>(g, ta, tb, td, td2, p, pairs, stream);
-  return launch_pair_typed<true, true>(g, ta, tb, td, td2, p, pairs, stream);
+  return launch_pair_family(g, m, p, pairs, a_mn, b_mn, stream);
 }
 
 }  // namespace tps

@@ -19,7 +19,23 @@ constexpr uint32_t TPS_DEVERR_LABEL = 2u;
 // EPI_CE_STATS D = acc (fp32 logits), and per (row, 128-column tile) the
 //              softmax statistics of the tile's columns, split at the
 //              vocabulary-shard boundary (see CeTileStats)
-enum EpiMode : int { EPI_STORE = 0, EPI_ACT_FWD = 1, EPI_ACT_BWD = 2, EPI_CE_STATS = 3 };
+// Gated MLP (Hg = X Wg, U = X Wu, A = phi(Hg) * U):
+// EPI_GLU_FWD  CTA-pair kernel only: each pair tile holds 128 gate columns
+//              (from B) and the same 128 up columns (from the up operand);
+//              D = Hg (fp32), D3 = U (fp32), D2 = A (dtype d2_dtype)
+// EPI_GLU_UP   acc = U: D = U (fp32, may be null), D2 = phi(AUX) * U with
+//              AUX = Hg (the two-GEMM form of EPI_GLU_FWD)
+// EPI_GLU_BWD  acc = dA: D = dHg = acc * AUX2 * phi'(AUX), D2 = dU =
+//              acc * phi(AUX), with AUX = Hg and AUX2 = U (fp32)
+enum EpiMode : int {
+  EPI_STORE = 0,
+  EPI_ACT_FWD = 1,
+  EPI_ACT_BWD = 2,
+  EPI_CE_STATS = 3,
+  EPI_GLU_FWD = 4,
+  EPI_GLU_UP = 5,
+  EPI_GLU_BWD = 6
+};
 
 // Width of the column tiles the CE statistics are kept for (the GEMM
 // epilogue thread that owns a row folds this many columns at a time).
@@ -36,6 +52,10 @@ struct Epilogue {
   int d2_dtype = TPS_BF16;
   const float* aux = nullptr; // EPI_ACT_BWD pre-activation, row-major fp32
   int64_t ld_aux = 0;
+  void* d3 = nullptr;         // EPI_GLU_FWD: U, row-major fp32
+  int64_t ldd3 = 0;
+  const float* aux2 = nullptr;  // EPI_GLU_BWD: U, row-major fp32
+  int64_t ld_aux2 = 0;
   // EPI_CE_STATS: stats[(row * n_tiles + tile) * 4 + {0,1,2,3}] =
   // (m_a, s_a, m_b, s_b): max and sum of e^{z - max} over the tile's columns
   // in the shard that owns the tile's first column (a) and in the next shard
@@ -64,6 +84,17 @@ struct GemmDesc {
   // Number of logical ranks the contraction dimension K is sharded over
   // (array_split plan).  1 when K is not sharded.
   int32_t kparts = 1;
+  // EPI_GLU_FWD: the up projection's weight, with b's strides (b is the
+  // gate's); N counts gate (= up) columns.
+  const void* b_up = nullptr;
+  // Optional second contraction segment: D = A B + A2 B2 over K2 more terms
+  // (same operand dtype and contiguous dimensions as A and B).  Under a
+  // K split each logical rank owns its array_split segment of both.
+  const void* a2 = nullptr;
+  int64_t a2_sm = 0, a2_sk = 0;
+  const void* b2 = nullptr;
+  int64_t b2_sk = 0, b2_sn = 0;
+  int64_t K2 = 0;
   const char* name = "gemm";  // label used by the launch profiler
 };
 
@@ -145,9 +176,13 @@ __device__ __forceinline__ float gelu_tanh_sigmoid(float x) {
   const float z = 0.79788456080286536f * (x + 0.044715f * x * x * x);
   return __fdividef(1.0f, 1.0f + __expf(fminf(-2.0f * z, 80.0f)));
 }
+// Logistic sigma(x) = 1 / (1 + e^{-x}); the exponent is clamped at 80
+// (sigma is already 0 in fp32 there) so the division never sees infinity.
+__device__ __forceinline__ float logistic(float x) { return __fdividef(1.0f, 1.0f + __expf(fminf(-x, 80.0f))); }
 __device__ __forceinline__ float act_fwd(int act, float x) {
   if (act == TPS_ACT_GELU_ERF) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
   if (act == TPS_ACT_GELU_TANH) return x * gelu_tanh_sigmoid(x);
+  if (act == TPS_ACT_SILU) return x * logistic(x);
   return tanhf(x);
 }
 __device__ __forceinline__ float act_grad(int act, float x) {
@@ -160,8 +195,23 @@ __device__ __forceinline__ float act_grad(int act, float x) {
     const float s = gelu_tanh_sigmoid(x);
     return s + 2.0f * x * s * (1.0f - s) * 0.79788456080286536f * (1.0f + 3.0f * 0.044715f * x * x);
   }
+  if (act == TPS_ACT_SILU) {  // d/dx x s(x) = s + x s (1 - s)
+    const float s = logistic(x);
+    return s + x * s * (1.0f - s);
+  }
   const float h = tanhf(x);
   return 1.0f - h * h;
+}
+// phi(x) and phi'(x) together (one exponential for SiLU).
+__device__ __forceinline__ void act_fwd_grad(int act, float x, float& f, float& g) {
+  if (act == TPS_ACT_SILU) {
+    const float s = logistic(x);
+    f = x * s;
+    g = s + x * s * (1.0f - s);
+  } else {
+    f = act_fwd(act, x);
+    g = act_grad(act, x);
+  }
 }
 
 }  // namespace tps

@@ -49,10 +49,10 @@ __device__ __forceinline__ void stage_bf16_sw64(uint8_t* buf, int r, const float
 }
 
 // Fused epilogue of one 32 x 32 chunk (lane = row) through TMA stores.
-// `v` holds the accumulators, `a` the pre-activation for EPI_ACT_BWD.
-// PENDING is the number of this warp's earlier bulk-store groups that may
-// still be reading staging when the buffers are overwritten (0 for one
-// staging buffer, 1 when the caller alternates two).
+// `v` holds the accumulators, `a` the pre-activation for EPI_ACT_BWD (Hg
+// for EPI_GLU_UP).  PENDING is the number of this warp's earlier
+// bulk-store groups that may still be reading staging when the buffers are
+// overwritten (0 for one staging buffer, 1 when the caller alternates two).
 template <int PENDING>
 __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensorMap* tmD, const CUtensorMap* tmD2,
                                                uint8_t* stg_f32, uint8_t* stg_bf16, int lane, int row0, int col0,
@@ -74,6 +74,11 @@ __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensor
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = act_fwd(e.act, v[i]);
     stage_bf16_sw64(stg_bf16, lane, v);
+  } else if (e.mode == EPI_GLU_UP) {
+    if (e.d != nullptr) stage_f32_sw128(stg_f32, lane, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= act_fwd(e.act, a[i]);
+    stage_bf16_sw64(stg_bf16, lane, v);
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] *= act_grad(e.act, a[i]);
@@ -85,12 +90,64 @@ __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensor
   fence_async_smem();
   __syncwarp();
   if (lane == 0) {
-    if (e.mode == EPI_ACT_FWD) {
+    if (e.mode == EPI_ACT_FWD || e.mode == EPI_GLU_UP) {
       if (e.d != nullptr) tma_store_2d(tmD, stg_f32, col0, row0);
       tma_store_2d(tmD2, stg_bf16, col0, row0);
     } else {
       tma_store_2d(tmD, e.d_dtype == TPS_F32 ? stg_f32 : stg_bf16, col0, row0);
     }
+    bulk_commit();
+  }
+}
+
+// EPI_GLU_BWD chunk through TMA stores, double-buffered like
+// tc_store_chunk<1>: dHg = v * U * phi'(Hg) leaves from the bf16 slot and
+// dU = v * phi(Hg) from the start of the fp32 slot, both as bf16 boxes.
+// `u` is overwritten with dU.
+__device__ __forceinline__ void tc_store_glu_bwd_chunk(const Epilogue& e, const CUtensorMap* tmD,
+                                                       const CUtensorMap* tmD2, uint8_t* stg_f32, uint8_t* stg_bf16,
+                                                       int lane, int row0, int col0, float (&v)[32],
+                                                       const float (&hg)[32], float (&u)[32]) {
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float f, g;
+    act_fwd_grad(e.act, hg[i], f, g);
+    const float da = v[i];
+    v[i] = da * u[i] * g;
+    u[i] = da * f;
+  }
+  stage_bf16_sw64(stg_bf16, lane, v);
+  stage_bf16_sw64(stg_f32, lane, u);
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmD, stg_bf16, col0, row0);
+    tma_store_2d(tmD2, stg_f32, col0, row0);
+    bulk_commit();
+  }
+}
+
+// EPI_GLU_FWD chunk through TMA stores from one 10 KB staging buffer: Hg
+// (fp32) at +0, U (fp32) at +4 KB, A = phi(Hg) * U (bf16) at +8 KB.  The
+// buffer is reused only after this warp's earlier stores have read it.
+__device__ __forceinline__ void tc_store_glu_chunk(const Epilogue& e, const CUtensorMap* tmHg, const CUtensorMap* tmA,
+                                                   const CUtensorMap* tmU, uint8_t* stg, int lane, int row0,
+                                                   int col0, const float (&hg)[32], float (&u)[32]) {
+  if (lane == 0) bulk_wait_read0();
+  __syncwarp();
+  stage_f32_sw128(stg, lane, hg);
+  stage_f32_sw128(stg + TC_STG_F32_BYTES, lane, u);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) u[i] *= act_fwd(e.act, hg[i]);
+  stage_bf16_sw64(stg + 2 * TC_STG_F32_BYTES, lane, u);
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmHg, stg, col0, row0);
+    tma_store_2d(tmU, stg + TC_STG_F32_BYTES, col0, row0);
+    tma_store_2d(tmA, stg + 2 * TC_STG_F32_BYTES, col0, row0);
     bulk_commit();
   }
 }

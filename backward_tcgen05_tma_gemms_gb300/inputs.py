@@ -109,6 +109,23 @@ def mlp_case(seed: int, T: int, d: int, F: int, dtype=torch.bfloat16, w_std: flo
 
 LLAMA_MLP = dict(T=8192, d=4096, F=14336, tp=8)
 
+
+def glu_case(seed: int, T: int, d: int, F: int, dtype=torch.bfloat16, w_std: float = 0.02,
+             layout: str = "in_out"):
+    """X (T x d), Wg, Wu, W2, G_Y (T x d) for the gated MLP, drawn in that
+    order.  Wg and Wu are d x F and W2 F x d for layout "in_out", or their
+    transposes for "out_in".  Weights N(0, w_std^2), X and G_Y N(0, 1)."""
+    rng = np.random.default_rng(seed)
+    X = normal(rng, (T, d))
+    Wg = normal(rng, (d, F), w_std)
+    Wu = normal(rng, (d, F), w_std)
+    W2 = normal(rng, (F, d), w_std)
+    GY = normal(rng, (T, d))
+    if layout == "out_in":
+        Wg, Wu, W2 = (np.ascontiguousarray(w.T) for w in (Wg, Wu, W2))
+    conv = to_bf16 if dtype == torch.bfloat16 else torch.from_numpy
+    return conv(X), conv(Wg), conv(Wu), conv(W2), conv(GY)
+
 # ---------------------------------------------------------------------------
 # vocabulary cross-entropy
 

@@ -3,6 +3,7 @@ profilers (ncu) and quick timing.  Prints per-launch device times from the
 library's own launch profiler.
 
     python -m backward_tcgen05_tma_gemms_gb300.profile_case mlp --T 2048 --reps 2
+    python -m backward_tcgen05_tma_gemms_gb300.profile_case glu --T 2048 --reps 1
     python -m backward_tcgen05_tma_gemms_gb300.profile_case ce --T 1024 --reps 2
     python -m backward_tcgen05_tma_gemms_gb300.profile_case matmul --M 4096 --K 4096 --N 4096
 
@@ -18,7 +19,7 @@ from . import api, inputs
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["mlp", "ce", "matmul"])
+    ap.add_argument("op", choices=["mlp", "glu", "ce", "matmul"])
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--d", type=int, default=4096)
     ap.add_argument("--F", type=int, default=14336)
@@ -34,6 +35,9 @@ def main():
     if a.op == "mlp":
         X, W1, W2, GY = (t.to(dev) for t in inputs.mlp_case(0, a.T, a.d, a.F, torch.bfloat16))
         call = lambda: api.mlp_fwd_bwd(X, W1, W2, GY, a.tp, "gelu_tanh", "in_out")
+    elif a.op == "glu":
+        X, Wg, Wu, W2, GY = (t.to(dev) for t in inputs.glu_case(0, a.T, a.d, a.F, torch.bfloat16))
+        call = lambda: api.glu_mlp_fwd_bwd(X, Wg, Wu, W2, GY, a.tp, "silu", "in_out")
     elif a.op == "ce":
         h, W, labels = (t.to(dev) for t in inputs.ce_case(0, a.T, a.d, a.V, torch.bfloat16))
         call = lambda: api.vocab_ce_fwd_bwd(h, W, labels, a.tp)

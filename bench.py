@@ -333,8 +333,66 @@ def run_gpu(args, rank, world, local_rank):
     # max over ranks
     if world > 1:
         ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
+    widened = None if args.no_widened else run_widened(args, dev, d)
     return dict(ms=ms, e2e_ms=e2e_ms, prof=prof.summary, launches=launches, clocks=clk.summary(), h2d=h2d, d2h=d2h,
-                host=host)
+                host=host, widened=widened)
+
+
+# ----------------------------------------------------------------- widened rows
+GLU_FLOPS = 9 * 2.0 * MLP["T"] * MLP["d"] * MLP["F"]          # gate+up (2), down, dA, dW2, dWg, dWu, dX (2)
+CE_EX_FLOPS = 3 * 2.0 * CE["T"] * CE["d"] * CE["V"]           # logits, dHidden, dWhead
+
+
+def run_widened(args, dev, d):
+    """Time, apart from the step, the rows built beyond it at the same
+    sizes: the gated (SwiGLU) MLP and the extended cross-entropy (every
+    eighth label ignored, job-wide mean, head gradient).  Device-resident
+    inputs, CUDA events on the launching stream."""
+    from backward_tcgen05_tma_gemms_gb300 import api
+    T, dm, F, V = MLP["T"], MLP["d"], MLP["F"], CE["V"]
+    stream = torch.cuda.current_stream(dev)
+    X, Wg, Wu, W2, GY = (t.to(dev) for t in inputs.glu_case(0, T, dm, F, torch.bfloat16))
+    f32 = dict(device=dev, dtype=torch.float32)
+    glu_out = (torch.empty(T, dm, **f32), torch.empty(T, dm, **f32), torch.empty(dm, F, **f32),
+               torch.empty(dm, F, **f32), torch.empty(F, dm, **f32))
+    glu_ws = torch.empty(api.glu_mlp_workspace_bytes(T, dm, F, MLP["tp"], torch.bfloat16), dtype=torch.uint8,
+                         device=dev)
+    labels = d["labels"].clone()
+    labels[::8] = -100
+    ce_ws = torch.empty(api.ce_workspace_bytes(T, V, CE["tp"]), dtype=torch.uint8, device=dev)
+    denom = float((labels != -100).sum().item())
+
+    def glu():
+        api.glu_mlp_fwd_bwd(X, Wg, Wu, W2, GY, MLP["tp"], "silu", workspace=glu_ws, out=glu_out)
+
+    def ce_ex():
+        api.vocab_ce_fwd_bwd_ex(d["h"], d["W"], labels, CE["tp"], ignore_index=-100, reduction="mean",
+                                denominator=denom, want_dwhead=True, workspace=ce_ws)
+
+    res = {}
+    for name, fn, flops, what in (
+            ("swiglu_mlp", glu, GLU_FLOPS,
+             "gated TP-MLP fwd+bwd, SiLU gate (T=8192, d=4096, F=14336, tp=8), gate and up fused in one GEMM"),
+            ("vocab_ce_ex", ce_ex, CE_EX_FLOPS,
+             "vocab CE fwd+bwd with ignore_index on 1/8 of labels, job-wide mean, dWhead (T=8192, d=4096, "
+             "V=128256, tp=8)")):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        n = max(3, args.steps // 3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with api.profile() as prof:
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        if api.last_device_error() != 0:
+            raise RuntimeError(f"device error in {name}")
+        ms = e0.elapsed_time(e1) / n
+        res[name] = {"workload": what, "ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12, "steps": n,
+                     "per_kernel_ms_per_step": {k: v["ms"] / n for k, v in prof.summary.items()}}
+    return res
 
 
 # ----------------------------------------------------------------- oracle (CPU) arm
@@ -374,6 +432,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["tps", "reference"], default="tps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-widened", action="store_true", help="skip timing the rows beyond the step")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -448,6 +507,8 @@ def main():
         "e2e": {"value": STEP_FLOPS * world / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
     }
+    if r["widened"] is not None:
+        line["widened_rows"] = r["widened"]
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         f, s, threads, desc = oracle_sample(host=r["host"])
         line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",

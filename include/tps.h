@@ -81,11 +81,13 @@ enum {
 /* Split axes of tps_matmul_fwd_bwd ([SG] "解题路线" steps 2-4). */
 enum { TPS_AXIS_ROWS = 0, TPS_AXIS_COLUMNS = 1, TPS_AXIS_INNER = 2 };
 
-/* Element-wise activation phi of the MLP.
+/* Element-wise activation phi of the MLP (and the gate of the gated MLP).
  *   GELU_ERF : x * Phi(x) -- torch's default gelu used by [TP] "参考答案".
  *   GELU_TANH: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
- *   TANH     : tanh, with phi' = 1 - H^2 as [MC] "02 / BACKWARD" writes. */
-enum { TPS_ACT_GELU_ERF = 0, TPS_ACT_GELU_TANH = 1, TPS_ACT_TANH = 2 };
+ *   TANH     : tanh, with phi' = 1 - H^2 as [MC] "02 / BACKWARD" writes.
+ *   SILU     : x sigma(x), one of the element-wise activations [TP] core
+ *              concept 2.A step 3 names (SwiGLU's gate). */
+enum { TPS_ACT_GELU_ERF = 0, TPS_ACT_GELU_TANH = 1, TPS_ACT_TANH = 2, TPS_ACT_SILU = 3 };
 
 /* Weight layouts.  IN_OUT: W1 is d x F and W2 is F x d (math notation
  * Y = phi(X W1) W2 of [MC] "01 / COLUMN THEN ROW").  OUT_IN: torch
@@ -176,6 +178,35 @@ size_t tps_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int3
 int tps_mlp_fwd_bwd_noalloc(const tps_tensor* X, const tps_tensor* W1, const tps_tensor* W2, const tps_tensor* GY,
                             int32_t tp, int32_t act, int32_t weight_layout, const tps_tensor* Y,
                             const tps_tensor* dX, const tps_tensor* dW1, const tps_tensor* dW2, void* cuda_stream);
+
+/* ------------------------------------------------------------------------
+ * tps_glu_mlp_fwd_bwd -- the gated column-then-row MLP (SwiGLU for
+ * act = TPS_ACT_SILU), forward and backward, split over `tp` logical ranks
+ * along the hidden width F.  [TP] reference answer Q1 puts the gate/up
+ * projections and the activation in the column-parallel layer and the down
+ * projection in the row-parallel one; both Wg and Wu are split along F by
+ * the same array_split plan, so the gating is shard-local ([TP] core
+ * concept 2.A step 3) and only the outputs Y and dX are rank sums:
+ *   Hg = X Wg, U = X Wu, A = phi(Hg) * U, Y = sum_r A_r W2_r;
+ *   dA = GY W2^T, dU = dA * phi(Hg), dHg = dA * U * phi'(Hg),
+ *   dWg = X^T dHg, dWu = X^T dU, dW2 = A^T GY,
+ *   dX = sum_r (dHg_r Wg_r^T + dU_r Wu_r^T).
+ * The pages give no gating formula; this is the usual gated linear unit.
+ * X, GY (..., d); Wg, Wu: d x F (TPS_W_IN_OUT) or F x d (TPS_W_OUT_IN),
+ * W2: F x d or d x F; all F32 or all BF16.  Outputs Y, dX (..., d) and
+ * dWg, dWu, dW2 (their weights' shapes) are F32.  For bf16 operands the
+ * gate and up projections run as one tensor-core GEMM whose epilogue forms
+ * A; A, dHg and dU are bf16 GEMM operands, Hg and U stay fp32.
+ * `workspace` >= tps_glu_mlp_workspace_bytes bytes, 256-byte aligned.
+ * ---------------------------------------------------------------------- */
+int tps_glu_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* Wg, const tps_tensor* Wu, const tps_tensor* W2,
+                        const tps_tensor* GY, int32_t tp, int32_t act, int32_t weight_layout, const tps_tensor* Y,
+                        const tps_tensor* dX, const tps_tensor* dWg, const tps_tensor* dWu, const tps_tensor* dW2,
+                        void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Workspace bytes tps_glu_mlp_fwd_bwd needs: 8 T F + 3 T F x (operand
+ * element size), each part rounded up to 256 bytes. */
+size_t tps_glu_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int32_t dtype);
 
 /* ------------------------------------------------------------------------
  * tps_vocab_ce_fwd_bwd -- cross-entropy over a vocabulary split into `tp`

@@ -16,7 +16,8 @@ from parity import assert_close
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-ACTS = {"gelu_erf": oracle.ACT_GELU_ERF, "gelu_tanh": oracle.ACT_GELU_TANH, "tanh": oracle.ACT_TANH}
+ACTS = {"gelu_erf": oracle.ACT_GELU_ERF, "gelu_tanh": oracle.ACT_GELU_TANH, "tanh": oracle.ACT_TANH,
+        "silu": oracle.ACT_SILU}
 
 
 def oracle_io(W, layout):
