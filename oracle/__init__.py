@@ -18,6 +18,10 @@ Parity status per function (what pins it is in ``tests/test_oracle_*.py``):
   glu_rows, glu_cols          pinned (torch autograd, finite differences,
                               reduction to mlp_* when U = 1, the lesson's
                               per-rank sum)
+  plan_heads                  pinned (the lesson's Llama-3-8B head counts
+                              for TP = 8 and 16, brute-force invariants)
+  attn_qkv, attn_out          pinned (torch autograd, finite differences,
+                              the lesson's per-rank column / row split)
   ce_tokens, ce_sharded_one   pinned (closed-form softmax on the worked
                               example's logits, torch cross_entropy, FD)
   ce_ex                       pinned (torch cross_entropy with ignore_index
@@ -78,6 +82,12 @@ def _declare(lib):
     lib.orc_glu_cols.argtypes = ([ctypes.c_int64] * 3 + [_dp] * 5 + [ctypes.c_int, ctypes.c_int64, _i64p, _dp, _dp,
                                  _dp])
     lib.orc_glu_cols.restype = None
+    lib.orc_plan_heads.argtypes = [ctypes.c_int32] * 3 + [_i64p, _i64p, _i32p, _i32p]
+    lib.orc_plan_heads.restype = ctypes.c_int
+    lib.orc_attn_qkv.argtypes = [ctypes.c_int64] * 4 + [_dp] * 14
+    lib.orc_attn_qkv.restype = None
+    lib.orc_attn_out.argtypes = [ctypes.c_int64] * 3 + [_dp] * 6
+    lib.orc_attn_out.restype = None
     lib.orc_ce_tokens.argtypes = ([ctypes.c_int64] * 3 + [_dp, _dp, _i64p, ctypes.c_int32, ctypes.c_int64, _i64p,
                                   _dp, _dp, _dp, _i32p])
     lib.orc_ce_tokens.restype = ctypes.c_int
@@ -220,6 +230,38 @@ class Oracle:
         Y, dX = self.glu_rows(X, Wg, Wu, W2, GY, act)
         dWg, dWu, dW2 = self.glu_cols(X, Wg, Wu, W2, GY, act)
         return Y, dX, dWg, dWu, dW2
+
+    # -- attention projections (weights (in, out)) -------------------------
+    def plan_heads(self, n_heads: int, n_kv_heads: int, tp: int):
+        """(q_off [tp+1], kv_first [tp], kv_count, kv_replicas)."""
+        q_off = np.zeros(max(tp, 0) + 1, dtype=np.int64)
+        kv_first = np.zeros(max(tp, 1), dtype=np.int64)
+        cnt, rep = ctypes.c_int32(0), ctypes.c_int32(0)
+        rc = self.lib.orc_plan_heads(n_heads, n_kv_heads, tp, self._p(q_off, _i64p), self._p(kv_first, _i64p),
+                                     ctypes.byref(cnt), ctypes.byref(rep))
+        if rc != 0:
+            raise ValueError("partition")
+        return q_off, kv_first[:tp], int(cnt.value), int(rep.value)
+
+    def attn_qkv(self, X, Wq, Wk, Wv, dQ, dK, dV):
+        """(Q, K, V, dX, dWq, dWk, dWv)."""
+        X, Wq, Wk, Wv, dQ, dK, dV = map(self._f64, (X, Wq, Wk, Wv, dQ, dK, dV))
+        T, d = X.shape
+        nq, nkv = Wq.shape[1], Wk.shape[1]
+        out = [np.empty((T, nq)), np.empty((T, nkv)), np.empty((T, nkv)), np.empty((T, d)),
+               np.empty((d, nq)), np.empty((d, nkv)), np.empty((d, nkv))]
+        self.lib.orc_attn_qkv(T, d, nq, nkv, *[self._p(a) for a in (X, Wq, Wk, Wv, dQ, dK, dV)],
+                              *[self._p(a) for a in out])
+        return tuple(out)
+
+    def attn_out(self, C, Wo, GY):
+        """(Y, dC, dWo)."""
+        C, Wo, GY = map(self._f64, (C, Wo, GY))
+        T, nq = C.shape
+        d = Wo.shape[1]
+        out = [np.empty((T, d)), np.empty((T, nq)), np.empty((nq, d))]
+        self.lib.orc_attn_out(T, d, nq, self._p(C), self._p(Wo), self._p(GY), *[self._p(a) for a in out])
+        return tuple(out)
 
     # -- cross-entropy ---------------------------------------------------
     def ce_tokens(self, h, W, labels, parts: int, toks=None):

@@ -1,6 +1,7 @@
 /*
  * oracle.c -- plain float64 CPU oracle for the sharded GEMM forward/backward,
- * the column-then-row tensor-parallel MLP and the vocabulary-sharded
+ * the column-then-row tensor-parallel MLP (plain and gated), the attention
+ * projections with their head-aligned plan, and the vocabulary-sharded
  * cross-entropy.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
@@ -367,6 +368,130 @@ void orc_glu_cols(int64_t T, int64_t d, int64_t F,
         free(a);
         free(dhg);
         free(du);
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * Head-aligned shard plan of the attention projections.
+ * [TP] core concept 2.B: W_Q, W_K, W_V are split along the output head
+ * dimension, each rank owning H / TP heads; W_O is split along its input
+ * head dimension.  [TP] core concept 3.4: H must be divisible by TP; with
+ * grouped-query attention (H_kv key/value heads, each shared by H / H_kv
+ * query heads) TP = 8 for H = 32, H_kv = 8 gives every rank 4 query heads
+ * and 1 KV head, while TP = 16 leaves the 8 KV heads indivisible and they
+ * must be shared or replicated across ranks.  Reading taken: the KV heads
+ * are split evenly when H_kv mod TP = 0, and each KV head is replicated on
+ * TP / H_kv ranks when TP mod H_kv = 0; other combinations are rejected,
+ * as is H mod H_kv != 0.
+ * Outputs: q_off[0..tp] (query-head offsets, rank r owns heads
+ * [q_off[r], q_off[r+1])), kv_first[0..tp-1] (first KV head of rank r),
+ * *kv_count (KV heads per rank), *kv_replicas (ranks holding each KV head).
+ * ---------------------------------------------------------------------- */
+int orc_plan_heads(int32_t n_heads, int32_t n_kv_heads, int32_t tp, int64_t* q_off, int64_t* kv_first,
+                   int32_t* kv_count, int32_t* kv_replicas) {
+    if (tp < 1 || n_heads < 1 || n_kv_heads < 1) return ORC_ERR_PARTITION;
+    if (n_heads % tp != 0) return ORC_ERR_PARTITION;          /* H mod TP = 0 */
+    if (n_heads % n_kv_heads != 0) return ORC_ERR_PARTITION;  /* whole query groups */
+    int32_t per_rank = n_heads / tp;
+    for (int32_t r = 0; r <= tp; ++r) q_off[r] = (int64_t)r * per_rank;
+    if (n_kv_heads % tp == 0) {
+        *kv_count = n_kv_heads / tp;
+        *kv_replicas = 1;
+        for (int32_t r = 0; r < tp; ++r) kv_first[r] = (int64_t)r * (n_kv_heads / tp);
+    } else if (tp % n_kv_heads == 0) {
+        int32_t rep = tp / n_kv_heads;
+        *kv_count = 1;
+        *kv_replicas = rep;
+        for (int32_t r = 0; r < tp; ++r) kv_first[r] = r / rep;
+    } else {
+        return ORC_ERR_PARTITION;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Attention projections, unsharded definitions ([TP] core concept 2.B; the
+ * attention core between them is not part of this computation: its
+ * outputs and gradients are inputs here).
+ * QKV projections (column-parallel):  Q = X Wq, K = X Wk, V = X Wv;
+ * given the upstream dQ, dK, dV:       dWq = X^T dQ, dWk = X^T dK,
+ *                                      dWv = X^T dV,
+ *                                      dX = dQ Wq^T + dK Wk^T + dV Wv^T.
+ * X T x d; Wq d x nq; Wk, Wv d x nkv (in,out); nq = H dh, nkv = H_kv dh.
+ * Any output may be NULL.
+ * ---------------------------------------------------------------------- */
+void orc_attn_qkv(int64_t T, int64_t d, int64_t nq, int64_t nkv,
+                  const double* X, const double* Wq, const double* Wk, const double* Wv,
+                  const double* dQ, const double* dK, const double* dV,
+                  double* Q, double* K, double* V, double* dX, double* dWq, double* dWk, double* dWv) {
+    const double* W[3] = {Wq, Wk, Wv};
+    const double* G[3] = {dQ, dK, dV};
+    double* O[3] = {Q, K, V};
+    double* dW[3] = {dWq, dWk, dWv};
+    const int64_t n[3] = {nq, nkv, nkv};
+    for (int p = 0; p < 3; ++p) {
+        if (O[p]) {
+            #pragma omp parallel for schedule(static)
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t j = 0; j < n[p]; ++j) {
+                    double s = 0.0;
+                    for (int64_t c = 0; c < d; ++c) s += X[t * d + c] * W[p][c * n[p] + j];
+                    O[p][t * n[p] + j] = s;
+                }
+        }
+        if (dW[p]) {
+            #pragma omp parallel for schedule(static)
+            for (int64_t c = 0; c < d; ++c)
+                for (int64_t j = 0; j < n[p]; ++j) {
+                    double s = 0.0;
+                    for (int64_t t = 0; t < T; ++t) s += X[t * d + c] * G[p][t * n[p] + j];
+                    dW[p][c * n[p] + j] = s;
+                }
+        }
+    }
+    if (dX) {
+        #pragma omp parallel for schedule(static)
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t c = 0; c < d; ++c) {
+                double s = 0.0;
+                for (int p = 0; p < 3; ++p)
+                    for (int64_t j = 0; j < n[p]; ++j) s += G[p][t * n[p] + j] * W[p][c * n[p] + j];
+                dX[t * d + c] = s;
+            }
+    }
+}
+
+/* Output projection (row-parallel):    Y = C Wo;
+ * given the upstream G_Y:              dC = G_Y Wo^T, dWo = C^T G_Y.
+ * C T x nq (the attention core's context), Wo nq x d (in,out). */
+void orc_attn_out(int64_t T, int64_t d, int64_t nq, const double* C, const double* Wo, const double* GY,
+                  double* Y, double* dC, double* dWo) {
+    if (Y) {
+        #pragma omp parallel for schedule(static)
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t c = 0; c < d; ++c) {
+                double s = 0.0;
+                for (int64_t j = 0; j < nq; ++j) s += C[t * nq + j] * Wo[j * d + c];
+                Y[t * d + c] = s;
+            }
+    }
+    if (dC) {
+        #pragma omp parallel for schedule(static)
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t j = 0; j < nq; ++j) {
+                double s = 0.0;
+                for (int64_t c = 0; c < d; ++c) s += GY[t * d + c] * Wo[j * d + c];
+                dC[t * nq + j] = s;
+            }
+    }
+    if (dWo) {
+        #pragma omp parallel for schedule(static)
+        for (int64_t j = 0; j < nq; ++j)
+            for (int64_t c = 0; c < d; ++c) {
+                double s = 0.0;
+                for (int64_t t = 0; t < T; ++t) s += C[t * nq + j] * GY[t * d + c];
+                dWo[j * d + c] = s;
+            }
     }
 }
 

@@ -53,6 +53,14 @@ MUTANTS = [
     ("glu_dHg_missing_up_factor", "dhg[t] = da * u * orc_act_grad(act, hg);", "dhg[t] = da * orc_act_grad(act, hg);",
      "test_oracle_glu.py"),
     ("glu_dWu_wrong_operand", "su += X[t * d + c] * du[t];", "su += X[t * d + c] * dhg[t];", "test_oracle_glu.py"),
+    ("heads_replica_index", "for (int32_t r = 0; r < tp; ++r) kv_first[r] = r / rep;",
+     "for (int32_t r = 0; r < tp; ++r) kv_first[r] = r % n_kv_heads;", "test_oracle_attn.py"),
+    ("heads_uneven_accepted", "if (n_heads % tp != 0) return ORC_ERR_PARTITION;", "", "test_oracle_attn.py"),
+    ("attn_dX_missing_branch", "for (int64_t j = 0; j < n[p]; ++j) s += G[p][t * n[p] + j] * W[p][c * n[p] + j];",
+     "for (int64_t j = 0; j < n[p] && p < 2; ++j) s += G[p][t * n[p] + j] * W[p][c * n[p] + j];",
+     "test_oracle_attn.py"),
+    ("attn_dWo_wrong_index", "for (int64_t t = 0; t < T; ++t) s += C[t * nq + j] * GY[t * d + c];",
+     "for (int64_t t = 0; t < T; ++t) s += C[t * nq + j] * GY[t * d + (c + 1) % d];", "test_oracle_attn.py"),
     ("ce_sharded_local_max", "for (int64_t j = off[r]; j < off[r + 1]; ++j) sr += exp(z[j] - m);",
      "for (int64_t j = off[r]; j < off[r + 1]; ++j) sr += exp(z[j] - m_r[r]);", "test_oracle_ce.py"),
 ]
