@@ -68,6 +68,11 @@ def library():
     lib.tps_glu_mlp_fwd_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P, P, P, vp, sz, vp]
     lib.tps_glu_mlp_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     lib.tps_glu_mlp_workspace_bytes.restype = sz
+    lib.tps_plan_heads.argtypes = [i32, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i32),
+                                   ctypes.POINTER(i32)]
+    lib.tps_attn_qkv_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, vp]
+    lib.tps_attn_qkv_bwd.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, P, P, P, P, vp]
+    lib.tps_attn_out_fwd_bwd.argtypes = [P, P, P, i32, i32, i32, P, P, P, vp]
     lib.tps_mlp_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     lib.tps_mlp_workspace_bytes.restype = sz
     lib.tps_vocab_ce_fwd_bwd.argtypes = [P, P, P, i32, i32, P, P, P, P, vp, sz, vp]
@@ -259,6 +264,68 @@ def glu_mlp_fwd_bwd(X: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, W2: tor
     _check(library().tps_glu_mlp_fwd_bwd(*[_ref(a) for a in args[:5]], tp, ACTS[act], LAYOUTS[weight_layout],
                                          *[_ref(a) for a in args[5:]], ctypes.c_void_p(workspace.data_ptr()),
                                          workspace.numel() * workspace.element_size(), _stream(dev)))
+    return tuple(out)
+
+
+def plan_heads(n_heads: int, n_kv_heads: int, tp: int):
+    """Head-aligned plan: (q_off [tp+1], kv_first [tp], kv_count, kv_replicas)."""
+    _parts(tp, "tp")
+    q_off = (ctypes.c_int64 * (tp + 1))()
+    kv_first = (ctypes.c_int64 * tp)()
+    cnt, rep = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(library().tps_plan_heads(n_heads, n_kv_heads, tp, q_off, kv_first, ctypes.byref(cnt), ctypes.byref(rep)))
+    return list(q_off), list(kv_first), int(cnt.value), int(rep.value)
+
+
+def attn_qkv_fwd(X, Wq, Wk, Wv, n_heads: int, n_kv_heads: int, tp: int, weight_layout: str = "in_out",
+                 out_dtype: Optional[torch.dtype] = None, out: Optional[Sequence[torch.Tensor]] = None):
+    """(Q, K, V) of the head-split column-parallel projections."""
+    _parts(tp, "tp")
+    if weight_layout not in LAYOUTS:
+        raise ValueError("argument")
+    d = X.shape[-1]
+    T = X.numel() // d if d else 0
+    nq = Wq.shape[1] if weight_layout == "in_out" else Wq.shape[0]
+    nkv = Wk.shape[1] if weight_layout == "in_out" else Wk.shape[0]
+    dt = out_dtype or X.dtype
+    if out is None:
+        out = tuple(torch.empty(T, n, device=X.device, dtype=dt) for n in (nq, nkv, nkv))
+    args = [_tt(t) for t in (X, Wq, Wk, Wv, *out)]
+    _check(library().tps_attn_qkv_fwd(*[_ref(a) for a in args[:4]], n_heads, n_kv_heads, tp, LAYOUTS[weight_layout],
+                                      *[_ref(a) for a in args[4:]], _stream(X.device)))
+    return tuple(out)
+
+
+def attn_qkv_bwd(X, Wq, Wk, Wv, dQ, dK, dV, n_heads: int, n_kv_heads: int, tp: int, weight_layout: str = "in_out",
+                 out: Optional[Sequence[torch.Tensor]] = None):
+    """fp32 (dX, dWq, dWk, dWv)."""
+    _parts(tp, "tp")
+    if weight_layout not in LAYOUTS:
+        raise ValueError("argument")
+    dev = X.device
+    if out is None:
+        out = (torch.empty(X.shape, device=dev, dtype=torch.float32),
+               *(torch.empty(w.shape, device=dev, dtype=torch.float32) for w in (Wq, Wk, Wv)))
+    args = [_tt(t) for t in (X, Wq, Wk, Wv, dQ, dK, dV, *out)]
+    _check(library().tps_attn_qkv_bwd(*[_ref(a) for a in args[:7]], n_heads, n_kv_heads, tp, LAYOUTS[weight_layout],
+                                      *[_ref(a) for a in args[7:]], _stream(dev)))
+    return tuple(out)
+
+
+def attn_out_fwd_bwd(C, Wo, GY, n_heads: int, tp: int, weight_layout: str = "in_out",
+                     dC_dtype: Optional[torch.dtype] = None, out: Optional[Sequence[torch.Tensor]] = None):
+    """(Y fp32, dC, dWo fp32) of the row-parallel output projection."""
+    _parts(tp, "tp")
+    if weight_layout not in LAYOUTS:
+        raise ValueError("argument")
+    dev = C.device
+    if out is None:
+        out = (torch.empty(GY.shape, device=dev, dtype=torch.float32),
+               torch.empty(C.shape, device=dev, dtype=dC_dtype or C.dtype),
+               torch.empty(Wo.shape, device=dev, dtype=torch.float32))
+    args = [_tt(t) for t in (C, Wo, GY, *out)]
+    _check(library().tps_attn_out_fwd_bwd(*[_ref(a) for a in args[:3]], n_heads, tp, LAYOUTS[weight_layout],
+                                          *[_ref(a) for a in args[3:]], _stream(dev)))
     return tuple(out)
 
 

@@ -196,10 +196,49 @@ static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream)
   if (g.M == 0 || g.N == 0) return TPS_OK;
   uint32_t* err = dev_err_ptr();
   if (err == nullptr) return fail(TPS_ERR_CUDA, "cannot resolve the device error word");
-  if (g.K == 0 && g.K2 > 0) {  // only the second segment has terms
-    g.a = g.a2; g.a_sm = g.a2_sm; g.a_sk = g.a2_sk;
-    g.b = g.b2; g.b_sk = g.b2_sk; g.b_sn = g.b2_sn;
-    g.K = g.K2; g.K2 = 0;
+  // Drop empty contraction segments (the first non-empty one moves to the front).
+  for (int pass = 0; pass < 2; ++pass) {
+    if (g.K == 0 && (g.K2 > 0 || g.K3 > 0)) {
+      g.a = g.a2; g.a_sm = g.a2_sm; g.a_sk = g.a2_sk;
+      g.b = g.b2; g.b_sk = g.b2_sk; g.b_sn = g.b2_sn;
+      g.K = g.K2;
+      g.a2 = g.a3; g.a2_sm = g.a3_sm; g.a2_sk = g.a3_sk;
+      g.b2 = g.b3; g.b2_sk = g.b3_sk; g.b2_sn = g.b3_sn;
+      g.K2 = g.K3;
+      g.K3 = 0;
+    }
+  }
+  if (g.K2 == 0 && g.K3 > 0) {
+    g.a2 = g.a3; g.a2_sm = g.a3_sm; g.a2_sk = g.a3_sk;
+    g.b2 = g.b3; g.b2_sk = g.b3_sk; g.b2_sn = g.b3_sn;
+    g.K2 = g.K3;
+    g.K3 = 0;
+  }
+  if (g.n_segs > 1) {  // column segments: each output on its own
+    if (g.K == 0) {
+      for (int s = 0; s < g.n_segs; ++s) {
+        const int rc = launch_fill(g.nd[s], g.epi.d_dtype, g.M, g.n_cols[s], g.nldd[s], 1, stream);
+        if (rc) return rc;
+      }
+      return TPS_OK;
+    }
+    if (!gemm_tc_supported(g)) {  // one GEMM per segment
+      for (int s = 0; s < g.n_segs; ++s) {
+        GemmDesc t = g;
+        t.n_segs = 1;
+        t.N = g.n_cols[s];
+        t.b = g.nb[s];
+        t.b_sk = g.nb_sk[s];
+        t.b_sn = g.nb_sn[s];
+        t.epi.d = g.nd[s];
+        const int rc = run_gemm(t, g.nldd[s], 1, stream);
+        if (rc) return rc;
+      }
+      return TPS_OK;
+    }
+    const int rc = launch_gemm_tc(g, err, stream);
+    if (rc == TPS_ERR_CUDA) return fail(rc, "%s: launch failed: %s", g.name, cudaGetErrorString(cudaGetLastError()));
+    return rc;
   }
   if (g.K == 0) {
     // An empty contraction is the zero matrix; phi(0) = 0 and 0 * phi' = 0
@@ -230,6 +269,12 @@ static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream)
     t.b2 = g.a2;
     t.b2_sk = g.a2_sk;
     t.b2_sn = g.a2_sm;
+    t.a3 = g.b3;
+    t.a3_sm = g.b3_sn;
+    t.a3_sk = g.b3_sk;
+    t.b3 = g.a3;
+    t.b3_sk = g.a3_sk;
+    t.b3_sn = g.a3_sm;
     t.epi.ldd = d_sn;
     g = t;
   } else {
@@ -607,6 +652,227 @@ extern "C" int tps_glu_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* Wg, co
     g.epi.d = dx.data; g.epi.d_dtype = TPS_F32;
     g.kparts = tp;
     if ((rc = run_gemm(g, dx.sr, dx.sc, s))) return rc;
+  }
+  return TPS_OK;
+}
+
+// ------------------------------------------------------------ attention projections
+// Head-aligned plan: query heads split evenly (H mod tp = 0); KV heads
+// split evenly when H_kv mod tp = 0, else each replicated on tp / H_kv ranks
+// (tp mod H_kv = 0); H mod H_kv = 0 (whole query groups per KV head).
+static int plan_heads(int32_t H, int32_t Hkv, int32_t tp, int64_t* q_off, int64_t* kv_first, int32_t* kv_count,
+                      int32_t* replicas) {
+  if (tp < 1 || H < 1 || Hkv < 1) return fail(TPS_ERR_PARTITION, "heads and tp must be >= 1");
+  if (H % tp != 0) return fail(TPS_ERR_PARTITION, "%d query heads do not split over tp=%d", H, tp);
+  if (H % Hkv != 0) return fail(TPS_ERR_PARTITION, "%d query heads do not group over %d KV heads", H, Hkv);
+  int32_t cnt, rep;
+  if (Hkv % tp == 0) {
+    cnt = Hkv / tp;
+    rep = 1;
+  } else if (tp % Hkv == 0) {
+    cnt = 1;
+    rep = tp / Hkv;
+  } else {
+    return fail(TPS_ERR_PARTITION, "%d KV heads neither split nor replicate evenly over tp=%d", Hkv, tp);
+  }
+  for (int32_t r = 0; r <= tp && q_off; ++r) q_off[r] = static_cast<int64_t>(r) * (H / tp);
+  for (int32_t r = 0; r < tp && kv_first; ++r) kv_first[r] = rep > 1 ? r / rep : static_cast<int64_t>(r) * cnt;
+  if (kv_count) *kv_count = cnt;
+  if (replicas) *replicas = rep;
+  return TPS_OK;
+}
+
+extern "C" int tps_plan_heads(int32_t n_heads, int32_t n_kv_heads, int32_t tp, int64_t* q_off, int64_t* kv_first,
+                              int32_t* kv_count, int32_t* kv_replicas) {
+  t_detail.clear();
+  return plan_heads(n_heads, n_kv_heads, tp, q_off, kv_first, kv_count, kv_replicas);
+}
+
+// Shapes of the QKV weights: nq = H dh columns for Wq, nkv = H_kv dh for Wk
+// and Wv, in either layout.
+struct QkvShapes {
+  int64_t T, d, nq, nkv;
+  Mat x, wq, wk, wv;
+};
+static int qkv_shapes(const tps_tensor* X, const tps_tensor* Wq, const tps_tensor* Wk, const tps_tensor* Wv,
+                      int32_t H, int32_t Hkv, int32_t tp, int32_t layout, QkvShapes* q) {
+  int rc;
+  if ((rc = as_mat(X, "X", true, &q->x)) || (rc = as_mat(Wq, "Wq", false, &q->wq)) ||
+      (rc = as_mat(Wk, "Wk", false, &q->wk)) || (rc = as_mat(Wv, "Wv", false, &q->wv)))
+    return rc;
+  if (layout != TPS_W_IN_OUT && layout != TPS_W_OUT_IN) return fail(TPS_ERR_ARG, "unknown weight layout %d", layout);
+  if ((rc = plan_heads(H, Hkv, tp, nullptr, nullptr, nullptr, nullptr))) return rc;
+  const bool io = layout == TPS_W_IN_OUT;
+  q->T = q->x.rows;
+  q->d = q->x.cols;
+  q->nq = io ? q->wq.cols : q->wq.rows;
+  if ((io ? q->wq.rows : q->wq.cols) != q->d) return fail(TPS_ERR_SHAPE, "Wq does not match X's width");
+  if (q->nq % H != 0) return fail(TPS_ERR_SHAPE, "Wq's %lld outputs are not %d whole heads", (long long)q->nq, H);
+  q->nkv = (q->nq / H) * Hkv;
+  if ((rc = expect(q->wk, "Wk", io ? q->d : q->nkv, io ? q->nkv : q->d)) ||
+      (rc = expect(q->wv, "Wv", io ? q->d : q->nkv, io ? q->nkv : q->d)))
+    return rc;
+  const int dt = q->x.dtype;
+  if ((dt != TPS_F32 && dt != TPS_BF16) || q->wq.dtype != dt || q->wk.dtype != dt || q->wv.dtype != dt)
+    return fail(TPS_ERR_DTYPE, "X, Wq, Wk, Wv must all be f32 or all bf16");
+  return TPS_OK;
+}
+
+extern "C" int tps_attn_qkv_fwd(const tps_tensor* X, const tps_tensor* Wq, const tps_tensor* Wk,
+                                const tps_tensor* Wv, int32_t n_heads, int32_t n_kv_heads, int32_t tp,
+                                int32_t weight_layout, const tps_tensor* Q, const tps_tensor* K, const tps_tensor* V,
+                                void* cuda_stream) {
+  t_detail.clear();
+  QkvShapes a;
+  int rc;
+  if ((rc = qkv_shapes(X, Wq, Wk, Wv, n_heads, n_kv_heads, tp, weight_layout, &a))) return rc;
+  Mat q, k, v;
+  if ((rc = as_mat(Q, "Q", true, &q)) || (rc = expect(q, "Q", a.T, a.nq)) || (rc = as_mat(K, "K", true, &k)) ||
+      (rc = expect(k, "K", a.T, a.nkv)) || (rc = as_mat(V, "V", true, &v)) || (rc = expect(v, "V", a.T, a.nkv)))
+    return rc;
+  if ((q.dtype != TPS_F32 && q.dtype != TPS_BF16) || k.dtype != q.dtype || v.dtype != q.dtype)
+    return fail(TPS_ERR_DTYPE, "Q, K, V must share f32 or bf16");
+  if ((q.sc != 1 && a.nq > 1) || (k.sc != 1 && a.nkv > 1) || (v.sc != 1 && a.nkv > 1))
+    return fail(TPS_ERR_LAYOUT, "Q, K, V rows must be contiguous");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const Mat* w[3] = {&a.wq, &a.wk, &a.wv};
+  const Mat* o[3] = {&q, &k, &v};
+  GemmDesc g;  // Q | K | V = X [Wq | Wk | Wv]: one launch over the three column ranges
+  g.name = "attn_qkv";
+  g.M = a.T; g.N = a.nq + 2 * a.nkv; g.K = a.d; g.in_dtype = a.x.dtype;
+  g.a = a.x.data; g.a_sm = a.x.sr; g.a_sk = a.x.sc;
+  g.n_segs = 3;
+  for (int i = 0; i < 3; ++i) {
+    int64_t w_in, w_out;
+    weight_strides(*w[i], weight_layout, &w_in, &w_out);
+    g.n_cols[i] = i == 0 ? a.nq : a.nkv;
+    g.nb[i] = w[i]->data; g.nb_sk[i] = w_in; g.nb_sn[i] = w_out;
+    g.nd[i] = o[i]->data; g.nldd[i] = o[i]->sr;
+  }
+  g.b = g.nb[0]; g.b_sk = g.nb_sk[0]; g.b_sn = g.nb_sn[0];
+  g.epi.d_dtype = q.dtype;
+  return run_gemm(g, 0, 1, s);
+}
+
+extern "C" int tps_attn_qkv_bwd(const tps_tensor* X, const tps_tensor* Wq, const tps_tensor* Wk,
+                                const tps_tensor* Wv, const tps_tensor* dQ, const tps_tensor* dK, const tps_tensor* dV,
+                                int32_t n_heads, int32_t n_kv_heads, int32_t tp, int32_t weight_layout,
+                                const tps_tensor* dX, const tps_tensor* dWq, const tps_tensor* dWk,
+                                const tps_tensor* dWv, void* cuda_stream) {
+  t_detail.clear();
+  QkvShapes a;
+  int rc;
+  if ((rc = qkv_shapes(X, Wq, Wk, Wv, n_heads, n_kv_heads, tp, weight_layout, &a))) return rc;
+  Mat dq, dk, dv, dx, dwq, dwk, dwv;
+  if ((rc = as_mat(dQ, "dQ", true, &dq)) || (rc = expect(dq, "dQ", a.T, a.nq)) ||
+      (rc = as_mat(dK, "dK", true, &dk)) || (rc = expect(dk, "dK", a.T, a.nkv)) ||
+      (rc = as_mat(dV, "dV", true, &dv)) || (rc = expect(dv, "dV", a.T, a.nkv)) ||
+      (rc = as_mat(dX, "dX", true, &dx)) || (rc = expect(dx, "dX", a.T, a.d)) ||
+      (rc = as_mat(dWq, "dWq", false, &dwq)) || (rc = expect(dwq, "dWq", a.wq.rows, a.wq.cols)) ||
+      (rc = as_mat(dWk, "dWk", false, &dwk)) || (rc = expect(dwk, "dWk", a.wk.rows, a.wk.cols)) ||
+      (rc = as_mat(dWv, "dWv", false, &dwv)) || (rc = expect(dwv, "dWv", a.wv.rows, a.wv.cols)))
+    return rc;
+  const int dt = a.x.dtype;
+  if (dq.dtype != dt || dk.dtype != dt || dv.dtype != dt)
+    return fail(TPS_ERR_DTYPE, "dQ, dK, dV must have the operand dtype (%s)", dtname(dt));
+  for (const Mat* m : {&dx, &dwq, &dwk, &dwv})
+    if (m->dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "projection gradients must be f32");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const Mat* w[3] = {&a.wq, &a.wk, &a.wv};
+  const Mat* gr[3] = {&dq, &dk, &dv};
+  const Mat* dw[3] = {&dwq, &dwk, &dwv};
+  int64_t w_in[3], w_out[3];
+  for (int i = 0; i < 3; ++i) weight_strides(*w[i], weight_layout, &w_in[i], &w_out[i]);
+  {  // dX = sum_r (dQ_r Wq_r^T + dK_r Wk_r^T + dV_r Wv_r^T): three K segments, one K loop
+    GemmDesc g;
+    g.name = "attn_dX";
+    g.M = a.T; g.N = a.d; g.in_dtype = dt;
+    g.K = a.nq;
+    g.a = dq.data; g.a_sm = dq.sr; g.a_sk = dq.sc;
+    g.b = a.wq.data; g.b_sk = w_out[0]; g.b_sn = w_in[0];
+    g.K2 = a.nkv;
+    g.a2 = dk.data; g.a2_sm = dk.sr; g.a2_sk = dk.sc;
+    g.b2 = a.wk.data; g.b2_sk = w_out[1]; g.b2_sn = w_in[1];
+    g.K3 = a.nkv;
+    g.a3 = dv.data; g.a3_sm = dv.sr; g.a3_sk = dv.sc;
+    g.b3 = a.wv.data; g.b3_sk = w_out[2]; g.b3_sn = w_in[2];
+    g.epi.d = dx.data; g.epi.d_dtype = TPS_F32;
+    g.kparts = tp;
+    if ((rc = run_gemm(g, dx.sr, dx.sc, s))) return rc;
+  }
+  static const char* names[3] = {"attn_dWq", "attn_dWk", "attn_dWv"};
+  for (int i = 0; i < 3; ++i) {  // dW(dd, j) = sum_t X[t, dd] dProj[t, j]: shard-local columns
+    int64_t o_in, o_out;
+    weight_strides(*dw[i], weight_layout, &o_in, &o_out);
+    GemmDesc g;
+    g.name = names[i];
+    g.M = a.d; g.N = i == 0 ? a.nq : a.nkv; g.K = a.T; g.in_dtype = dt;
+    g.a = a.x.data; g.a_sm = a.x.sc; g.a_sk = a.x.sr;
+    g.b = gr[i]->data; g.b_sk = gr[i]->sr; g.b_sn = gr[i]->sc;
+    g.epi.d = dw[i]->data; g.epi.d_dtype = TPS_F32;
+    if ((rc = run_gemm(g, o_in, o_out, s))) return rc;
+  }
+  return TPS_OK;
+}
+
+extern "C" int tps_attn_out_fwd_bwd(const tps_tensor* C, const tps_tensor* Wo, const tps_tensor* GY, int32_t n_heads,
+                                    int32_t tp, int32_t weight_layout, const tps_tensor* Y, const tps_tensor* dC,
+                                    const tps_tensor* dWo, void* cuda_stream) {
+  t_detail.clear();
+  Mat c, wo, gy, y, dc, dwo;
+  int rc;
+  if ((rc = as_mat(C, "C", true, &c)) || (rc = as_mat(Wo, "Wo", false, &wo)) || (rc = as_mat(GY, "GY", true, &gy)))
+    return rc;
+  if (weight_layout != TPS_W_IN_OUT && weight_layout != TPS_W_OUT_IN)
+    return fail(TPS_ERR_ARG, "unknown weight layout %d", weight_layout);
+  if (tp < 1 || n_heads < 1 || n_heads % tp != 0)
+    return fail(TPS_ERR_PARTITION, "%d heads do not split over tp=%d", n_heads, tp);
+  const bool io = weight_layout == TPS_W_IN_OUT;
+  const int64_t T = c.rows, nq = c.cols;
+  const int64_t d = io ? wo.cols : wo.rows;
+  if (nq % n_heads != 0) return fail(TPS_ERR_SHAPE, "C's %lld columns are not %d whole heads", (long long)nq, n_heads);
+  if ((io ? wo.rows : wo.cols) != nq) return fail(TPS_ERR_SHAPE, "Wo does not match C's width");
+  if ((rc = expect(gy, "GY", T, d))) return rc;
+  const int dt = c.dtype;
+  if ((dt != TPS_F32 && dt != TPS_BF16) || wo.dtype != dt || gy.dtype != dt)
+    return fail(TPS_ERR_DTYPE, "C, Wo, GY must all be f32 or all bf16");
+  if ((rc = as_mat(Y, "Y", true, &y)) || (rc = expect(y, "Y", T, d)) || (rc = as_mat(dC, "dC", true, &dc)) ||
+      (rc = expect(dc, "dC", T, nq)) || (rc = as_mat(dWo, "dWo", false, &dwo)) ||
+      (rc = expect(dwo, "dWo", wo.rows, wo.cols)))
+    return rc;
+  if (y.dtype != TPS_F32 || dwo.dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "Y and dWo must be f32");
+  if (dc.dtype != TPS_F32 && dc.dtype != TPS_BF16) return fail(TPS_ERR_DTYPE, "dC must be f32 or bf16");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  int64_t w_in, w_out, o_in, o_out;
+  weight_strides(wo, weight_layout, &w_in, &w_out);  // Wo(j, dd)
+  weight_strides(dwo, weight_layout, &o_in, &o_out);
+  {  // Y = sum_r C_r Wo_r: row-parallel over the heads, rank sum in the K loop
+    GemmDesc g;
+    g.name = "attn_out";
+    g.M = T; g.N = d; g.K = nq; g.in_dtype = dt;
+    g.a = c.data; g.a_sm = c.sr; g.a_sk = c.sc;
+    g.b = wo.data; g.b_sk = w_in; g.b_sn = w_out;
+    g.epi.d = y.data; g.epi.d_dtype = TPS_F32;
+    g.kparts = tp;
+    if ((rc = run_gemm(g, y.sr, y.sc, s))) return rc;
+  }
+  {  // dC = GY Wo^T: each rank's head columns
+    GemmDesc g;
+    g.name = "attn_dC";
+    g.M = T; g.N = nq; g.K = d; g.in_dtype = dt;
+    g.a = gy.data; g.a_sm = gy.sr; g.a_sk = gy.sc;
+    g.b = wo.data; g.b_sk = w_out; g.b_sn = w_in;
+    g.epi.d = dc.data; g.epi.d_dtype = dc.dtype;
+    if ((rc = run_gemm(g, dc.sr, dc.sc, s))) return rc;
+  }
+  {  // dWo(j, dd) = sum_t C[t, j] GY[t, dd]
+    GemmDesc g;
+    g.name = "attn_dWo";
+    g.M = nq; g.N = d; g.K = T; g.in_dtype = dt;
+    g.a = c.data; g.a_sm = c.sc; g.a_sk = c.sr;
+    g.b = gy.data; g.b_sk = gy.sr; g.b_sn = gy.sc;
+    g.epi.d = dwo.data; g.epi.d_dtype = TPS_F32;
+    if ((rc = run_gemm(g, o_in, o_out, s))) return rc;
   }
   return TPS_OK;
 }

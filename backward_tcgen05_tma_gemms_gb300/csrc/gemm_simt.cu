@@ -7,9 +7,9 @@
 // ("Sharded GEMM与Backprop：行、列、内维三种切分", 解题路线 steps 2-4: a
 // result that needs sum/all-reduce), each rank's partial product over its
 // array_split segment of K is accumulated separately and the partials are
-// then added in rank order, inside the kernel.  A second contraction
-// segment (D = A B + A2 B2) adds each rank's segment of the second pair to
-// the same rank partial.
+// then added in rank order, inside the kernel.  Further contraction
+// segments (D = A B + A2 B2 + A3 B3) add each rank's segment of every
+// further pair to the same rank partial.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,7 +21,7 @@ namespace tps {
 constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16, SG_THREADS = 256;
 
 struct SimtParams {
-  int64_t M, N, K, K2;
+  int64_t M, N, K, K2, K3;
   const void* a;
   int64_t a_sm, a_sk;
   const void* b;
@@ -30,6 +30,10 @@ struct SimtParams {
   int64_t a2_sm, a2_sk;
   const void* b2;
   int64_t b2_sk, b2_sn;
+  const void* a3;
+  int64_t a3_sm, a3_sk;
+  const void* b3;
+  int64_t b3_sk, b3_sn;
   int32_t kparts;
   Epilogue epi;
 };
@@ -118,6 +122,9 @@ __global__ void __launch_bounds__(SG_THREADS) gemm_simt_kernel(const SimtParams 
     if (p.K2 > 0)
       simt_segment<T>(p.a2, p.a2_sm, p.a2_sk, p.b2, p.b2_sk, p.b2_sn, p.M, p.N, m0, n0,
                       shard_offset(p.K2, p.kparts, r), shard_offset(p.K2, p.kparts, r + 1), As, Bs, part);
+    if (p.K3 > 0)
+      simt_segment<T>(p.a3, p.a3_sm, p.a3_sk, p.b3, p.b3_sk, p.b3_sn, p.M, p.N, m0, n0,
+                      shard_offset(p.K3, p.kparts, r), shard_offset(p.K3, p.kparts, r + 1), As, Bs, part);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -154,13 +161,21 @@ int launch_gemm_simt(const GemmDesc& g, uint32_t* /*dev_err*/, cudaStream_t stre
   p.b2 = g.b2;
   p.b2_sk = g.b2_sk;
   p.b2_sn = g.b2_sn;
+  p.K3 = g.K3;
+  p.a3 = g.a3;
+  p.a3_sm = g.a3_sm;
+  p.a3_sk = g.a3_sk;
+  p.b3 = g.b3;
+  p.b3_sk = g.b3_sk;
+  p.b3_sn = g.b3_sn;
   p.kparts = g.kparts < 1 ? 1 : g.kparts;
-  if (g.epi.mode == EPI_GLU_FWD) return TPS_ERR_ARG;  // the fused gate/up form is tensor-core only
+  // the fused gate/up form and column segments are tensor-core only
+  if (g.epi.mode == EPI_GLU_FWD || g.n_segs > 1) return TPS_ERR_ARG;
   p.epi = g.epi;
   const int64_t gx = (g.N + SG_BN - 1) / SG_BN, gy = (g.M + SG_BM - 1) / SG_BM;
   if (gx > 0x7FFFFFFF || gy > 65535) return TPS_ERR_SHAPE;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
-  ProfScope prof("gemm_simt", g.name, 2.0 * double(g.M) * double(g.N) * (double(g.K) + double(g.K2)), 0.0, stream);
+  ProfScope prof("gemm_simt", g.name, 2.0 * double(g.M) * double(g.N) * double(g.K + g.K2 + g.K3), 0.0, stream);
   if (g.in_dtype == TPS_F32)
     gemm_simt_kernel<float><<<grid, SG_THREADS, 0, stream>>>(p);
   else

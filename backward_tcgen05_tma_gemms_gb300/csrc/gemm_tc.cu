@@ -354,9 +354,12 @@ void tc_raster_choice(int m_tiles, int* raster_n, int* group, int* pol_a, int* p
 // contiguous dimension.
 bool gemm_tc_supported(const GemmDesc& g) {
   if (g.in_dtype != TPS_BF16) return false;
-  if (g.M < 1 || g.N < 1 || g.K < 1 || g.K2 < 0) return false;
-  if (g.M >= (1ll << 31) || g.N >= (1ll << 31) || g.K >= (1ll << 31) || g.K2 >= (1ll << 31)) return false;
-  if (g.epi.mode == EPI_GLU_FWD && (g.b_up == nullptr || g.K2 > 0)) return false;
+  if (g.M < 1 || g.N < 1 || g.K < 1 || g.K2 < 0 || g.K3 < 0) return false;
+  if (g.M >= (1ll << 31) || g.N >= (1ll << 31) || g.K + g.K2 + g.K3 >= (1ll << 31)) return false;
+  const bool k_segs = g.K2 > 0 || g.K3 > 0;
+  if (g.epi.mode == EPI_GLU_FWD && (g.b_up == nullptr || k_segs || g.n_segs > 1)) return false;
+  if (g.n_segs < 1 || g.n_segs > 3 || (g.n_segs > 1 && k_segs)) return false;
+  if ((g.n_segs > 1 || k_segs) && g.epi.mode != EPI_STORE) return false;  // segments: plain stores only
   auto ok_operand = [](const void* ptr, int64_t s_outer, int64_t s_inner, int64_t inner_extent) {
     if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return false;
     if (s_inner != 1) return false;
@@ -364,18 +367,37 @@ bool gemm_tc_supported(const GemmDesc& g) {
     return s_outer * 2 < (1ll << 40);
   };
   const bool a_ok = (g.a_sk == 1) ? ok_operand(g.a, g.a_sm, g.a_sk, g.K) : ok_operand(g.a, g.a_sk, g.a_sm, g.M);
+  if (!a_ok) return false;
+  if (g.n_segs > 1) {  // each segment's B and output, boundaries on 128-column blocks
+    int64_t n = 0;
+    for (int s = 0; s < g.n_segs; ++s) {
+      const int64_t c = g.n_cols[s];
+      if (c < 1 || (s + 1 < g.n_segs && c % 128 != 0)) return false;
+      if ((g.nb_sk[s] == 1) != (g.b_sk == 1)) return false;
+      if (!((g.nb_sk[s] == 1) ? ok_operand(g.nb[s], g.nb_sn[s], 1, g.K) : ok_operand(g.nb[s], g.nb_sk[s], g.nb_sn[s], c)))
+        return false;
+      const int es = g.epi.d_dtype == TPS_F32 ? 4 : 2;
+      if ((reinterpret_cast<uintptr_t>(g.nd[s]) & 15u) != 0 || (g.nldd[s] * es) % 16 != 0 || g.nldd[s] < c)
+        return false;
+      n += c;
+    }
+    return n == g.N;
+  }
   const bool b_ok = (g.b_sk == 1) ? ok_operand(g.b, g.b_sn, g.b_sk, g.K) : ok_operand(g.b, g.b_sk, g.b_sn, g.N);
-  if (!a_ok || !b_ok) return false;
+  if (!b_ok) return false;
   if (g.epi.mode == EPI_GLU_FWD &&
       !((g.b_sk == 1) ? ok_operand(g.b_up, g.b_sn, g.b_sk, g.K) : ok_operand(g.b_up, g.b_sk, g.b_sn, g.N)))
     return false;
-  if (g.K2 > 0) {
-    if ((g.a2_sk == 1) != (g.a_sk == 1) || (g.b2_sk == 1) != (g.b_sk == 1)) return false;
-    const bool a2_ok =
-        (g.a2_sk == 1) ? ok_operand(g.a2, g.a2_sm, g.a2_sk, g.K2) : ok_operand(g.a2, g.a2_sk, g.a2_sm, g.M);
-    const bool b2_ok =
-        (g.b2_sk == 1) ? ok_operand(g.b2, g.b2_sn, g.b2_sk, g.K2) : ok_operand(g.b2, g.b2_sk, g.b2_sn, g.N);
-    if (!a2_ok || !b2_ok) return false;
+  const void* as[2] = {g.a2, g.a3};
+  const void* bs[2] = {g.b2, g.b3};
+  const int64_t ks[2] = {g.K2, g.K3}, asm_[2] = {g.a2_sm, g.a3_sm}, ask[2] = {g.a2_sk, g.a3_sk};
+  const int64_t bsk[2] = {g.b2_sk, g.b3_sk}, bsn[2] = {g.b2_sn, g.b3_sn};
+  for (int s = 0; s < 2; ++s) {
+    if (ks[s] == 0) continue;
+    if ((ask[s] == 1) != (g.a_sk == 1) || (bsk[s] == 1) != (g.b_sk == 1)) return false;
+    const bool ao = (ask[s] == 1) ? ok_operand(as[s], asm_[s], 1, ks[s]) : ok_operand(as[s], ask[s], asm_[s], g.M);
+    const bool bo = (bsk[s] == 1) ? ok_operand(bs[s], bsn[s], 1, ks[s]) : ok_operand(bs[s], bsk[s], bsn[s], g.N);
+    if (!ao || !bo) return false;
   }
   return true;
 }
@@ -387,6 +409,13 @@ bool tc_make_output_maps(const GemmDesc& g, CUtensorMap* td, CUtensorMap* td2, C
   memset(td, 0, sizeof(*td));
   memset(td2, 0, sizeof(*td2));
   if (td3) memset(td3, 0, sizeof(*td3));
+  if (g.n_segs > 1) {  // one map per column segment, in td, td2, td3
+    CUtensorMap* maps[3] = {td, td2, td3};
+    for (int s = 0; s < g.n_segs; ++s)
+      if (maps[s] == nullptr || !tc_make_out_map(maps[s], g.nd[s], g.M, g.n_cols[s], g.nldd[s], g.epi.d_dtype))
+        return false;
+    return true;
+  }
   if (g.epi.mode == EPI_GLU_FWD) {  // Hg and U fp32, A bf16, 128-wide hidden-unit tiles
     return td3 != nullptr && g.epi.d2_dtype == TPS_BF16 &&
            tc_make_out_map(td, g.epi.d, g.M, g.N, g.epi.ldd, TPS_F32) &&
@@ -424,7 +453,8 @@ static int launch_typed(const GemmDesc& g, const CUtensorMap& ta, const CUtensor
 
 int launch_gemm_tc1(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   // the gated forms and a second K segment exist on CTA pairs only
-  if (g.epi.mode == EPI_GLU_FWD || g.epi.mode == EPI_GLU_BWD || g.K2 > 0) return TPS_ERR_ARG;
+  if (g.epi.mode == EPI_GLU_FWD || g.epi.mode == EPI_GLU_BWD || g.K2 > 0 || g.K3 > 0 || g.n_segs > 1)
+    return TPS_ERR_ARG;
   const bool a_mn = (g.a_sk != 1);
   const bool b_mn = (g.b_sk != 1);
   CUtensorMap ta, tb;
@@ -458,11 +488,13 @@ int launch_gemm_tc1(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
 
 // Kernel choice: CTA pairs (gemm_tc2.cu) when M spans at least one 256-row
 // pair tile, else single CTAs.  TPS_GEMM_KERNEL=1 or 2 forces one, except
-// that the gated forms and a second K segment always run on CTA pairs.
+// that the gated forms and contraction or column segments always run on
+// CTA pairs.
 int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   const char* kv = getenv("TPS_GEMM_KERNEL");
   const int forced = kv ? atoi(kv) : 0;
-  const bool pair_only = g.epi.mode == EPI_GLU_FWD || g.epi.mode == EPI_GLU_BWD || g.K2 > 0;
+  const bool pair_only =
+      g.epi.mode == EPI_GLU_FWD || g.epi.mode == EPI_GLU_BWD || g.K2 > 0 || g.K3 > 0 || g.n_segs > 1;
   const bool pair = pair_only || forced == 2 || (forced != 1 && g.M >= 256);
   return pair ? launch_gemm_tc2(g, dev_err, stream) : launch_gemm_tc1(g, dev_err, stream);
 }

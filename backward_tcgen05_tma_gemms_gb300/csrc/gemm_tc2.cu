@@ -25,8 +25,12 @@
 // epilogue forms phi(gate) * up without leaving the SM.  A pair tile then
 // covers 128 hidden units.
 //
-// A second contraction segment (GemmDesc::K2) continues the K loop with the
-// operands A2 and B2 into the same accumulator: D = A B + A2 B2.
+// Further contraction segments (GemmDesc::K2, K3) continue the K loop with
+// the operands A2, B2 (and A3, B3) into the same accumulator:
+// D = A B + A2 B2 + A3 B3.  Column segments (GemmDesc::n_segs) run up to
+// three GEMMs that share A as one launch over their concatenated columns:
+// each CTA's 128 B columns, and each epilogue warp's 128 output columns,
+// lie in one segment, whose own B and output maps they use.
 //
 // Warp roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one thread)
@@ -71,11 +75,20 @@ struct T2Barriers {
 constexpr size_t T2_SMEM_BYTES = 1024 + T2_STAGES * T2_STAGE_BYTES + T2_STAGING_BYTES + sizeof(T2Barriers);
 static_assert(T2_SMEM_BYTES <= 232448, "exceeds the opt-in shared memory per block");
 
+// Tensor maps of one launch: a[s], b[s] are the operands of contraction
+// segment s (b[1] is the up weight of the gated forward); with column
+// segments b[s] and d[s] belong to column segment s; otherwise d[0], d[1],
+// d[2] are the outputs D, D2 and D3.
+struct T2Maps {
+  CUtensorMap a[3], b[3], d[3];
+};
+
 struct T2Params {
   int M, N, K;
   int m_tiles, n_tiles, k_tiles, num_tiles;  // m_tiles counts 256-row pair tiles
-  int k_tiles1;                              // K tiles of the first segment
-  int glu;                                   // EPI_GLU_FWD: B2 is the up weight
+  int k_end[3];                              // cumulative K tiles of the contraction segments
+  int n_segs, n_end[3];                      // column segments: cumulative column ends
+  int glu;                                   // EPI_GLU_FWD: b[1] is the up weight
   int raster_n, group;
   int tma_store;
   Epilogue epi;
@@ -84,14 +97,12 @@ struct T2Params {
 
 // Epilogue families, compiled as separate kernels so that the gated forms'
 // extra live registers do not cost the plain ones a spill.
-enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2 };
+// T2_SEG: plain stores with contraction or column segments.
+enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2, T2_SEG = 3 };
 
 template <bool A_MN, bool B_MN, int FAM>
 __global__ void __launch_bounds__(T2_THREADS, 1)
-    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
-                    const __grid_constant__ CUtensorMap tmD3, const T2Params p) {
+    gemm_tc2_kernel(const __grid_constant__ T2Maps m, const T2Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -119,10 +130,11 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    if (p.k_tiles1 < p.k_tiles) tma_prefetch_desc(&tmA2);
-    if (p.glu || p.k_tiles1 < p.k_tiles) tma_prefetch_desc(&tmB2);
+    for (int s = 0; s < 3; ++s) {
+      const bool k_used = s == 0 || p.k_end[s] > p.k_end[s - 1];
+      if (k_used) tma_prefetch_desc(&m.a[s]);
+      if (k_used || s < p.n_segs || (s == 1 && p.glu)) tma_prefetch_desc(&m.b[s]);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(&bars->tmem_slot, T2_TMEM_COLS);
@@ -146,8 +158,13 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
         const int m0 = mt * 2 * T2_BM + static_cast<int>(rank) * T2_BM;
         // gated: both CTAs stage the same 128 hidden units, gate or up
-        const int nb0 = p.glu ? nt * T2_BN_CTA : nt * T2_BN + static_cast<int>(rank) * T2_BN_CTA;
-        const CUtensorMap* mb1 = (p.glu && rank == 1) ? &tmB2 : &tmB;
+        int nb0 = p.glu ? nt * T2_BN_CTA : nt * T2_BN + static_cast<int>(rank) * T2_BN_CTA;
+        int nseg = 0;  // column segment of this CTA's 128 B columns
+        if constexpr (FAM == T2_SEG) {
+          while (nseg < p.n_segs - 1 && nb0 >= p.n_end[nseg]) ++nseg;
+          if (nseg > 0) nb0 -= p.n_end[nseg - 1];
+        }
+        const CUtensorMap* mb0 = (p.glu && rank == 1) ? &m.b[1] : &m.b[nseg];
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -157,10 +174,12 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
           uint8_t* sb = sa + T2_A_BYTES;
           if (rank == 0) mbar_expect_tx(&bars->full[stage], 2 * T2_STAGE_BYTES);
           const uint32_t fb = full0_leader + stage * static_cast<uint32_t>(sizeof(uint64_t));
-          const bool seg2 = kt >= p.k_tiles1;
-          const CUtensorMap* ma = seg2 ? &tmA2 : &tmA;
-          const CUtensorMap* mb = seg2 ? &tmB2 : mb1;
-          const int k0 = (seg2 ? kt - p.k_tiles1 : kt) * TC_BK;
+          int ks = 0;  // contraction segment of this K tile
+          if constexpr (FAM == T2_SEG)
+            while (ks < 2 && kt >= p.k_end[ks]) ++ks;
+          const CUtensorMap* ma = &m.a[ks];
+          const CUtensorMap* mb = ks > 0 ? &m.b[ks] : mb0;
+          const int k0 = (kt - (ks > 0 ? p.k_end[ks - 1] : 0)) * TC_BK;
           if (!A_MN) {
             tma_load_2d_pair(sa, ma, fb, k0, m0);
           } else {
@@ -235,8 +254,9 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     const int h = ew >> 2;         // column half of the 256-column tile
     uint8_t* stg = staging + ew * 2 * T2_STG_BUF;
     const Epilogue& e = p.epi;
-    const bool ce = (e.mode == EPI_CE_STATS);
-    const bool bwd = p.tma_store && (e.mode == EPI_ACT_BWD || e.mode == EPI_GLU_UP);  // AUX prefetch
+    // segmented launches are plain stores: no statistics, no AUX
+    const bool ce = FAM == T2_PLAIN && e.mode == EPI_CE_STATS;
+    const bool bwd = FAM == T2_PLAIN && p.tma_store && (e.mode == EPI_ACT_BWD || e.mode == EPI_GLU_UP);
     constexpr bool glu = FAM == T2_GLU_FWD;
     constexpr bool gbwd = FAM == T2_GLU_BWD;
     // accumulator columns this warp drains: 128 (gated: 64 gate + 64 up)
@@ -248,6 +268,11 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       const int m0 = mt * 2 * T2_BM + static_cast<int>(rank) * T2_BM;
       // first output column of this warp's part of the tile
       const int nh0 = glu ? nt * T2_BN_CTA + h * warp_cols : nt * T2_BN + h * warp_cols;
+      int oseg = 0, ocol0 = 0;  // column segment of these columns: its output map and first column
+      if constexpr (FAM == T2_SEG) {
+        while (oseg < p.n_segs - 1 && nh0 >= p.n_end[oseg]) ++oseg;
+        ocol0 = oseg > 0 ? p.n_end[oseg - 1] : 0;
+      }
       if (!mbar_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const int row0 = m0 + q * 32;
@@ -282,7 +307,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
           if (!p.tma_store) {
             if (row < p.M) epilogue_glu_run32(e, row, col0, min(32, p.N - col0), hg, u);
           } else {
-            tc_store_glu_chunk(e, &tmD, &tmD2, &tmD3, stg, lane, row0, col0, hg, u);
+            tc_store_glu_chunk(e, &m.d[0], &m.d[1], &m.d[2], stg, lane, row0, col0, hg, u);
           }
           continue;
         }
@@ -301,7 +326,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
             uint8_t* buf = stg + (chunk & 1u) * T2_STG_BUF;
-            tc_store_glu_bwd_chunk(e, &tmD, &tmD2, buf, buf + TC_STG_F32_BYTES, lane, row0, col0, v, hg, u);
+            tc_store_glu_bwd_chunk(e, &m.d[0], &m.d[1], buf, buf + TC_STG_F32_BYTES, lane, row0, col0, v, hg, u);
             ++chunk;
           } else {
             tmem_ld_wait();
@@ -335,7 +360,8 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
           continue;
         }
         uint8_t* buf = stg + (chunk & 1u) * T2_STG_BUF;
-        tc_store_chunk<1>(e, &tmD, &tmD2, buf, buf + TC_STG_F32_BYTES, lane, row0, col0, v, a);
+        tc_store_chunk<1, FAM == T2_SEG>(e, &m.d[oseg], &m.d[1], buf, buf + TC_STG_F32_BYTES, lane, row0,
+                                         col0 - ocol0, v, a);
         ++chunk;
       }
       tc_fence_before();
@@ -356,10 +382,6 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
 // ------------------------------------------------------------------ host
 
 bool tc_make_output_maps(const GemmDesc& g, CUtensorMap* td, CUtensorMap* td2, CUtensorMap* td3);
-
-struct T2Maps {
-  CUtensorMap a, b, a2, b2, d, d2, d3;
-};
 
 template <bool A_MN, bool B_MN, int FAM>
 static int launch_pair_typed(const GemmDesc& g, const T2Maps& m, const T2Params& p, int pairs,
@@ -383,10 +405,10 @@ static int launch_pair_typed(const GemmDesc& g, const T2Maps& m, const T2Params&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const double flops = 2.0 * double(g.M) * double(g.N) * (double(g.K) + double(g.K2)) * (p.glu ? 2.0 : 1.0);
+  const double flops = 2.0 * double(g.M) * double(g.N) * double(g.K + g.K2 + g.K3) * (p.glu ? 2.0 : 1.0);
   ProfScope prof("gemm_tc", g.name, flops, 0.0, stream);
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN, FAM>, m.a, m.b, m.a2, m.b2, m.d, m.d2, m.d3, p);
+      cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN, FAM>, m, p);
   note_launch();
   return e == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
 }
@@ -404,6 +426,10 @@ static int launch_pair_family(const GemmDesc& g, const T2Maps& m, const T2Params
                               bool b_mn, cudaStream_t stream) {
   if (g.epi.mode == EPI_GLU_FWD) return launch_pair_majors<T2_GLU_FWD>(g, m, p, pairs, a_mn, b_mn, stream);
   if (g.epi.mode == EPI_GLU_BWD) return launch_pair_majors<T2_GLU_BWD>(g, m, p, pairs, a_mn, b_mn, stream);
+  if (g.n_segs > 1 || g.K2 > 0 || g.K3 > 0) {
+    if (g.epi.mode != EPI_STORE) return TPS_ERR_ARG;
+    return launch_pair_majors<T2_SEG>(g, m, p, pairs, a_mn, b_mn, stream);
+  }
   return launch_pair_majors<T2_PLAIN>(g, m, p, pairs, a_mn, b_mn, stream);
 }
 
@@ -417,18 +443,32 @@ int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   const bool a_mn = (g.a_sk != 1);
   const bool b_mn = (g.b_sk != 1);
   const bool glu = g.epi.mode == EPI_GLU_FWD;
-  const bool seg2 = g.K2 > 0;
-  if (glu && (seg2 || g.b_up == nullptr)) return TPS_ERR_ARG;
-  if (seg2 && ((g.a2_sk != 1) != a_mn || (g.b2_sk != 1) != b_mn)) return TPS_ERR_LAYOUT;
+  const int64_t ks[3] = {g.K, g.K2, g.K3};
+  const void* as[3] = {g.a, g.a2, g.a3};
+  const void* bs[3] = {g.b, g.b2, g.b3};
+  const int64_t a_sm[3] = {g.a_sm, g.a2_sm, g.a3_sm}, a_sk[3] = {g.a_sk, g.a2_sk, g.a3_sk};
+  const int64_t b_sk[3] = {g.b_sk, g.b2_sk, g.b3_sk}, b_sn[3] = {g.b_sn, g.b2_sn, g.b3_sn};
+  const bool k_segs = g.K2 > 0 || g.K3 > 0;
+  const bool n_segs = g.n_segs > 1;
+  if (g.n_segs < 1 || g.n_segs > 3) return TPS_ERR_ARG;
+  if (glu && (k_segs || n_segs || g.b_up == nullptr)) return TPS_ERR_ARG;
+  if ((n_segs || k_segs) && g.epi.mode != EPI_STORE) return TPS_ERR_ARG;  // segments: plain stores only
+  if (n_segs && k_segs) return TPS_ERR_ARG;
+  for (int s = 1; s < 3; ++s)
+    if (ks[s] > 0 && ((a_sk[s] != 1) != a_mn || (b_sk[s] != 1) != b_mn)) return TPS_ERR_LAYOUT;
   T2Maps m;
   memset(&m, 0, sizeof(m));
-  bool ok = pair_operand_map(&m.a, g.a, a_mn, g.K, g.M, a_mn ? g.a_sk : g.a_sm, T2_BM);
-  ok = ok && pair_operand_map(&m.b, g.b, b_mn, g.K, g.N, b_mn ? g.b_sk : g.b_sn, T2_BN_CTA);
-  if (glu) ok = ok && pair_operand_map(&m.b2, g.b_up, b_mn, g.K, g.N, b_mn ? g.b_sk : g.b_sn, T2_BN_CTA);
-  if (seg2) {
-    ok = ok && pair_operand_map(&m.a2, g.a2, a_mn, g.K2, g.M, a_mn ? g.a2_sk : g.a2_sm, T2_BM);
-    ok = ok && pair_operand_map(&m.b2, g.b2, b_mn, g.K2, g.N, b_mn ? g.b2_sk : g.b2_sn, T2_BN_CTA);
+  bool ok = true;
+  for (int s = 0; s < 3; ++s) {
+    if (s > 0 && ks[s] == 0) continue;
+    ok = ok && pair_operand_map(&m.a[s], as[s], a_mn, ks[s], g.M, a_mn ? a_sk[s] : a_sm[s], T2_BM);
+    if (!n_segs) ok = ok && pair_operand_map(&m.b[s], bs[s], b_mn, ks[s], g.N, b_mn ? b_sk[s] : b_sn[s], T2_BN_CTA);
   }
+  if (glu) ok = ok && pair_operand_map(&m.b[1], g.b_up, b_mn, g.K, g.N, b_mn ? g.b_sk : g.b_sn, T2_BN_CTA);
+  if (n_segs)
+    for (int s = 0; s < g.n_segs; ++s)
+      ok = ok && ((g.nb_sk[s] != 1) == b_mn) &&
+           pair_operand_map(&m.b[s], g.nb[s], b_mn, g.K, g.n_cols[s], b_mn ? g.nb_sk[s] : g.nb_sn[s], T2_BN_CTA);
   if (!ok) return TPS_ERR_CUDA;
 
   T2Params p;
@@ -438,8 +478,24 @@ int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   p.glu = glu ? 1 : 0;
   p.m_tiles = static_cast<int>((g.M + 2 * T2_BM - 1) / (2 * T2_BM));
   p.n_tiles = static_cast<int>(glu ? (g.N + T2_BN_CTA - 1) / T2_BN_CTA : (g.N + T2_BN - 1) / T2_BN);
-  p.k_tiles1 = static_cast<int>((g.K + TC_BK - 1) / TC_BK);
-  p.k_tiles = p.k_tiles1 + static_cast<int>((g.K2 + TC_BK - 1) / TC_BK);
+  int kt = 0;
+  for (int s = 0; s < 3; ++s) {
+    kt += static_cast<int>((ks[s] + TC_BK - 1) / TC_BK);
+    p.k_end[s] = kt;
+  }
+  p.k_tiles = kt;
+  p.n_segs = g.n_segs;
+  int64_t nc = 0;
+  for (int s = 0; s < 3; ++s) {
+    if (s < g.n_segs && n_segs) {
+      if (s + 1 < g.n_segs && g.n_cols[s] % T2_BN_CTA != 0) return TPS_ERR_ARG;
+      nc += g.n_cols[s];
+    } else {
+      nc = g.N;
+    }
+    p.n_end[s] = static_cast<int>(nc);
+  }
+  if (n_segs && nc != g.N) return TPS_ERR_ARG;
   p.num_tiles = p.m_tiles * p.n_tiles;
   int pol_a = 0, pol_b = 0;
   // groups of pair tiles cover the same rows as twice as many single tiles
@@ -449,7 +505,8 @@ int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   if (p.group > p.m_tiles) p.group = p.m_tiles;
   p.epi = g.epi;
   p.err = dev_err;
-  p.tma_store = tc_make_output_maps(g, &m.d, &m.d2, &m.d3) ? 1 : 0;
+  p.tma_store = tc_make_output_maps(g, &m.d[0], &m.d[1], &m.d[2]) ? 1 : 0;
+  if (n_segs && !p.tma_store) return TPS_ERR_LAYOUT;  // column segments leave through TMA stores only
   const int max_pairs = tc_num_sms() / 2;
   const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
 

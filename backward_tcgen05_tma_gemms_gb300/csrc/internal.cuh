@@ -87,14 +87,32 @@ struct GemmDesc {
   // EPI_GLU_FWD: the up projection's weight, with b's strides (b is the
   // gate's); N counts gate (= up) columns.
   const void* b_up = nullptr;
-  // Optional second contraction segment: D = A B + A2 B2 over K2 more terms
-  // (same operand dtype and contiguous dimensions as A and B).  Under a
-  // K split each logical rank owns its array_split segment of both.
+  // Optional further contraction segments: D = A B + A2 B2 + A3 B3 over K2
+  // and K3 more terms (same operand dtype and contiguous dimensions as A
+  // and B).  Under a K split each logical rank owns its array_split segment
+  // of every one.
   const void* a2 = nullptr;
   int64_t a2_sm = 0, a2_sk = 0;
   const void* b2 = nullptr;
   int64_t b2_sk = 0, b2_sn = 0;
   int64_t K2 = 0;
+  const void* a3 = nullptr;
+  int64_t a3_sm = 0, a3_sk = 0;
+  const void* b3 = nullptr;
+  int64_t b3_sk = 0, b3_sn = 0;
+  int64_t K3 = 0;
+  // Column segments (EPI_STORE, CTA-pair kernel): the N columns are up to
+  // three GEMMs that share A, segment s being n_cols[s] wide (every
+  // segment but the last a multiple of 128), with its own B (base nb[s],
+  // strides nb_sk[s], nb_sn[s], the same dimension contiguous in every
+  // segment) and its own row-major output (base nd[s], leading dimension
+  // nldd[s], dtype epi.d_dtype).  b, b_sk, b_sn describe segment 0.
+  int n_segs = 1;
+  int64_t n_cols[3] = {0, 0, 0};
+  const void* nb[3] = {nullptr, nullptr, nullptr};
+  int64_t nb_sk[3] = {0, 0, 0}, nb_sn[3] = {0, 0, 0};
+  void* nd[3] = {nullptr, nullptr, nullptr};
+  int64_t nldd[3] = {0, 0, 0};
   const char* name = "gemm";  // label used by the launch profiler
 };
 

@@ -53,7 +53,8 @@ __device__ __forceinline__ void stage_bf16_sw64(uint8_t* buf, int r, const float
 // for EPI_GLU_UP).  PENDING is the number of this warp's earlier
 // bulk-store groups that may still be reading staging when the buffers are
 // overwritten (0 for one staging buffer, 1 when the caller alternates two).
-template <int PENDING>
+// STORE_ONLY: the caller guarantees EPI_STORE.
+template <int PENDING, bool STORE_ONLY = false>
 __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensorMap* tmD, const CUtensorMap* tmD2,
                                                uint8_t* stg_f32, uint8_t* stg_bf16, int lane, int row0, int col0,
                                                float (&v)[32], const float (&a)[32]) {
@@ -64,7 +65,7 @@ __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensor
       asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
   }
   __syncwarp();
-  if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
+  if (STORE_ONLY || e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
     if (e.d_dtype == TPS_F32)
       stage_f32_sw128(stg_f32, lane, v);
     else
@@ -90,7 +91,7 @@ __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensor
   fence_async_smem();
   __syncwarp();
   if (lane == 0) {
-    if (e.mode == EPI_ACT_FWD || e.mode == EPI_GLU_UP) {
+    if (!STORE_ONLY && (e.mode == EPI_ACT_FWD || e.mode == EPI_GLU_UP)) {
       if (e.d != nullptr) tma_store_2d(tmD, stg_f32, col0, row0);
       tma_store_2d(tmD2, stg_bf16, col0, row0);
     } else {

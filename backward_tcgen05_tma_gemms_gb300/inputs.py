@@ -127,6 +127,38 @@ def glu_case(seed: int, T: int, d: int, F: int, dtype=torch.bfloat16, w_std: flo
     return conv(X), conv(Wg), conv(Wu), conv(W2), conv(GY)
 
 # ---------------------------------------------------------------------------
+# attention projections
+
+
+def attn_case(seed: int, T: int, d: int, H: int, Hkv: int, dh: int, dtype=torch.bfloat16, w_std: float = 0.02,
+              layout: str = "in_out"):
+    """X (T x d); Wq (d x H dh), Wk, Wv (d x Hkv dh), Wo (H dh x d) for
+    layout "in_out" or their transposes for "out_in"; the attention core's
+    gradients dQ (T x H dh), dK, dV (T x Hkv dh), its context C (T x H dh),
+    and G_Y (T x d), drawn in that order.  Weights N(0, w_std^2), the rest
+    N(0, 1)."""
+    rng = np.random.default_rng(seed)
+    nq, nkv = H * dh, Hkv * dh
+    X = normal(rng, (T, d))
+    Wq = normal(rng, (d, nq), w_std)
+    Wk = normal(rng, (d, nkv), w_std)
+    Wv = normal(rng, (d, nkv), w_std)
+    Wo = normal(rng, (nq, d), w_std)
+    dQ = normal(rng, (T, nq))
+    dK = normal(rng, (T, nkv))
+    dV = normal(rng, (T, nkv))
+    C = normal(rng, (T, nq))
+    GY = normal(rng, (T, d))
+    if layout == "out_in":
+        Wq, Wk, Wv, Wo = (np.ascontiguousarray(w.T) for w in (Wq, Wk, Wv, Wo))
+    conv = to_bf16 if dtype == torch.bfloat16 else torch.from_numpy
+    return dict(X=conv(X), Wq=conv(Wq), Wk=conv(Wk), Wv=conv(Wv), Wo=conv(Wo), dQ=conv(dQ), dK=conv(dK),
+                dV=conv(dV), C=conv(C), GY=conv(GY))
+
+
+LLAMA_ATTN = dict(T=8192, d=4096, H=32, Hkv=8, dh=128, tp=8)
+
+# ---------------------------------------------------------------------------
 # vocabulary cross-entropy
 
 

@@ -341,12 +341,17 @@ def run_gpu(args, rank, world, local_rank):
 # ----------------------------------------------------------------- widened rows
 GLU_FLOPS = 9 * 2.0 * MLP["T"] * MLP["d"] * MLP["F"]          # gate+up (2), down, dA, dW2, dWg, dWu, dX (2)
 CE_EX_FLOPS = 3 * 2.0 * CE["T"] * CE["d"] * CE["V"]           # logits, dHidden, dWhead
+ATT = inputs.LLAMA_ATTN
+_NQ, _NKV = ATT["H"] * ATT["dh"], ATT["Hkv"] * ATT["dh"]
+# QKV forward, dX and the three weight gradients; the output projection, dC, dWo
+ATTN_FLOPS = 3 * 2.0 * ATT["T"] * ATT["d"] * (_NQ + 2 * _NKV) + 3 * 2.0 * ATT["T"] * _NQ * ATT["d"]
 
 
 def run_widened(args, dev, d):
     """Time, apart from the step, the rows built beyond it at the same
-    sizes: the gated (SwiGLU) MLP and the extended cross-entropy (every
-    eighth label ignored, job-wide mean, head gradient).  Device-resident
+    sizes: the gated (SwiGLU) MLP, the extended cross-entropy (every
+    eighth label ignored, job-wide mean, head gradient) and the attention
+    projections.  Device-resident
     inputs, CUDA events on the launching stream."""
     from backward_tcgen05_tma_gemms_gb300 import api
     T, dm, F, V = MLP["T"], MLP["d"], MLP["F"], CE["V"]
@@ -369,13 +374,32 @@ def run_widened(args, dev, d):
         api.vocab_ce_fwd_bwd_ex(d["h"], d["W"], labels, CE["tp"], ignore_index=-100, reduction="mean",
                                 denominator=denom, want_dwhead=True, workspace=ce_ws)
 
+    a = {k: v.to(dev) for k, v in inputs.attn_case(0, ATT["T"], ATT["d"], ATT["H"], ATT["Hkv"], ATT["dh"],
+                                                    torch.bfloat16).items()}
+    bf = dict(device=dev, dtype=torch.bfloat16)
+    qkv_out = (torch.empty(ATT["T"], _NQ, **bf), torch.empty(ATT["T"], _NKV, **bf), torch.empty(ATT["T"], _NKV, **bf))
+    qkv_grads = (torch.empty(ATT["T"], ATT["d"], **f32), torch.empty(ATT["d"], _NQ, **f32),
+                 torch.empty(ATT["d"], _NKV, **f32), torch.empty(ATT["d"], _NKV, **f32))
+    o_out = (torch.empty(ATT["T"], ATT["d"], **f32), torch.empty(ATT["T"], _NQ, **bf),
+             torch.empty(_NQ, ATT["d"], **f32))
+
+    def attn():
+        hq, hkv, tpa = ATT["H"], ATT["Hkv"], ATT["tp"]
+        api.attn_qkv_fwd(a["X"], a["Wq"], a["Wk"], a["Wv"], hq, hkv, tpa, out=qkv_out)
+        api.attn_out_fwd_bwd(a["C"], a["Wo"], a["GY"], hq, tpa, out=o_out)
+        api.attn_qkv_bwd(a["X"], a["Wq"], a["Wk"], a["Wv"], a["dQ"], a["dK"], a["dV"], hq, hkv, tpa, out=qkv_grads)
+
     res = {}
     for name, fn, flops, what in (
             ("swiglu_mlp", glu, GLU_FLOPS,
              "gated TP-MLP fwd+bwd, SiLU gate (T=8192, d=4096, F=14336, tp=8), gate and up fused in one GEMM"),
             ("vocab_ce_ex", ce_ex, CE_EX_FLOPS,
              "vocab CE fwd+bwd with ignore_index on 1/8 of labels, job-wide mean, dWhead (T=8192, d=4096, "
-             "V=128256, tp=8)")):
+             "V=128256, tp=8)"),
+            ("attn_projections", attn, ATTN_FLOPS,
+             "TP attention projections fwd+bwd, Llama-3-8B heads (T=8192, d=4096, 32 query / 8 KV heads of 128, "
+             "tp=8): fused QKV, W_O with its rank sum, dX over the three branches, four weight gradients; the "
+             "attention core's context and gradients are synthetic inputs")):
         for _ in range(args.warmup):
             fn()
         torch.cuda.synchronize(dev)

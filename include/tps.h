@@ -209,6 +209,57 @@ int tps_glu_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* Wg, const tps_ten
 size_t tps_glu_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int32_t dtype);
 
 /* ------------------------------------------------------------------------
+ * Attention projections, split over `tp` logical ranks by heads
+ * ([TP] core concept 2.B: W_Q, W_K, W_V column-parallel along the output
+ * heads, W_O row-parallel along its input heads, one sum at the output).
+ * The attention core between them is not part of this library: its context
+ * C and its gradients dQ, dK, dV are inputs.
+ *
+ * tps_plan_heads -- the head-aligned plan ([TP] core concept 3 item 4).
+ * Query heads split evenly: n_heads mod tp must be 0.  KV heads (grouped
+ * query attention, n_heads mod n_kv_heads = 0) split evenly when
+ * n_kv_heads mod tp = 0, else each KV head is replicated on tp / n_kv_heads
+ * ranks (tp mod n_kv_heads = 0); other counts return TPS_ERR_PARTITION.
+ * Writes q_off[0..tp] (rank r owns query heads [q_off[r], q_off[r+1])),
+ * kv_first[0..tp-1] (first KV head of rank r), *kv_count (KV heads per
+ * rank) and *kv_replicas (ranks holding each KV head).  Any output may be
+ * NULL.  Host only; no device work.
+ * ---------------------------------------------------------------------- */
+int tps_plan_heads(int32_t n_heads, int32_t n_kv_heads, int32_t tp, int64_t* q_off, int64_t* kv_first,
+                   int32_t* kv_count, int32_t* kv_replicas);
+
+/* tps_attn_qkv_fwd -- Q = X Wq, K = X Wk, V = X Wv.  X (..., d); Wq d x nq
+ * and Wk, Wv d x nkv (TPS_W_IN_OUT) or their transposes (TPS_W_OUT_IN),
+ * with nq = n_heads * dh and nkv = n_kv_heads * dh; all F32 or all BF16.
+ * Q (T x nq), K, V (T x nkv): F32 or BF16 (one dtype for all three), rows
+ * contiguous.  Rank r's heads are a column range of each output.  For bf16
+ * the three projections run as one tensor-core launch over their
+ * concatenated columns when every boundary falls on 128 columns. */
+int tps_attn_qkv_fwd(const tps_tensor* X, const tps_tensor* Wq, const tps_tensor* Wk, const tps_tensor* Wv,
+                     int32_t n_heads, int32_t n_kv_heads, int32_t tp, int32_t weight_layout, const tps_tensor* Q,
+                     const tps_tensor* K, const tps_tensor* V, void* cuda_stream);
+
+/* tps_attn_qkv_bwd -- given dQ, dK, dV (the operand dtype; with replicated
+ * KV heads dK and dV summed over the replicas): dWq = X^T dQ,
+ * dWk = X^T dK, dWv = X^T dV (each rank's head columns) and
+ * dX = sum_r (dQ_r Wq_r^T + dK_r Wk_r^T + dV_r Wv_r^T), one GEMM whose K
+ * loop runs over the three branches.  dX (..., d) and the weight
+ * gradients (their weights' shapes) are F32. */
+int tps_attn_qkv_bwd(const tps_tensor* X, const tps_tensor* Wq, const tps_tensor* Wk, const tps_tensor* Wv,
+                     const tps_tensor* dQ, const tps_tensor* dK, const tps_tensor* dV, int32_t n_heads,
+                     int32_t n_kv_heads, int32_t tp, int32_t weight_layout, const tps_tensor* dX,
+                     const tps_tensor* dWq, const tps_tensor* dWk, const tps_tensor* dWv, void* cuda_stream);
+
+/* tps_attn_out_fwd_bwd -- the output projection: Y = sum_r C_r Wo_r (the
+ * row-parallel sum over the ranks' heads), dC = GY Wo^T, dWo = C^T GY.
+ * C (T x nq) and GY (..., d) in the operand dtype, Wo nq x d (IN_OUT) or
+ * d x nq (OUT_IN); n_heads mod tp must be 0.  Y and dWo F32; dC F32 or
+ * BF16 (the attention core's backward input). */
+int tps_attn_out_fwd_bwd(const tps_tensor* C, const tps_tensor* Wo, const tps_tensor* GY, int32_t n_heads,
+                         int32_t tp, int32_t weight_layout, const tps_tensor* Y, const tps_tensor* dC,
+                         const tps_tensor* dWo, void* cuda_stream);
+
+/* ------------------------------------------------------------------------
  * tps_vocab_ce_fwd_bwd -- cross-entropy over a vocabulary split into `tp`
  * contiguous shards (array_split of V), forward and backward
  * ([MC] "04 / VOCABULARY SHARDS"; single supervised position per token, no

@@ -131,3 +131,21 @@ def test_no_cpu_path():
     from backward_tcgen05_tma_gemms_gb300 import api
     with pytest.raises(ValueError, match="GPU"):
         api.matmul_fwd_bwd(torch.zeros(3, 5), torch.zeros(5, 4), torch.zeros(3, 4), 2, "inner")
+
+
+def test_plan_heads_matches_oracle(orc):
+    """The library's head plan (host code, no device work) against the
+    oracle's, bit for bit, over a grid of head counts and tp."""
+    from backward_tcgen05_tma_gemms_gb300 import api
+    for H in (1, 4, 6, 8, 12, 32, 64):
+        for Hkv in (1, 2, 4, 8, 32):
+            for tp in range(1, 70):
+                try:
+                    want = orc.plan_heads(H, Hkv, tp)
+                except ValueError:
+                    with pytest.raises(ValueError, match="partition"):
+                        api.plan_heads(H, Hkv, tp)
+                    continue
+                q_off, kv_first, cnt, rep = api.plan_heads(H, Hkv, tp)
+                assert q_off == want[0].tolist() and kv_first == want[1].tolist(), (H, Hkv, tp)
+                assert (cnt, rep) == (want[2], want[3]), (H, Hkv, tp)
