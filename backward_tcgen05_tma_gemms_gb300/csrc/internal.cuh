@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "tps.h"
 
@@ -220,6 +221,21 @@ __device__ __forceinline__ float act_grad(int act, float x) {
   const float h = tanhf(x);
   return 1.0f - h * h;
 }
+// Compile-time forms: act_dispatch calls f with the activation as a type,
+// once per chunk, so the unrolled element loops carry no activation branch.
+template <int ACT>
+__device__ __forceinline__ float act_fwd_c(float x) { return act_fwd(ACT, x); }
+template <int ACT>
+__device__ __forceinline__ float act_grad_c(float x) { return act_grad(ACT, x); }
+template <typename F>
+__device__ __forceinline__ void act_dispatch(int act, F&& f) {
+  switch (act) {
+    case TPS_ACT_GELU_ERF: f(std::integral_constant<int, TPS_ACT_GELU_ERF>()); break;
+    case TPS_ACT_GELU_TANH: f(std::integral_constant<int, TPS_ACT_GELU_TANH>()); break;
+    case TPS_ACT_SILU: f(std::integral_constant<int, TPS_ACT_SILU>()); break;
+    default: f(std::integral_constant<int, TPS_ACT_TANH>()); break;
+  }
+}
 // phi(x) and phi'(x) together (one exponential for SiLU).
 __device__ __forceinline__ void act_fwd_grad(int act, float x, float& f, float& g) {
   if (act == TPS_ACT_SILU) {
@@ -231,5 +247,7 @@ __device__ __forceinline__ void act_fwd_grad(int act, float x, float& f, float& 
     g = act_grad(act, x);
   }
 }
+template <int ACT>
+__device__ __forceinline__ void act_fwd_grad_c(float x, float& f, float& g) { act_fwd_grad(ACT, x, f, g); }
 
 }  // namespace tps

@@ -72,17 +72,23 @@ __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensor
       stage_bf16_sw64(stg_bf16, lane, v);
   } else if (e.mode == EPI_ACT_FWD) {
     if (e.d != nullptr) stage_f32_sw128(stg_f32, lane, v);
+    act_dispatch(e.act, [&](auto A) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = act_fwd(e.act, v[i]);
+      for (int i = 0; i < 32; ++i) v[i] = act_fwd_c<decltype(A)::value>(v[i]);
+    });
     stage_bf16_sw64(stg_bf16, lane, v);
   } else if (e.mode == EPI_GLU_UP) {
     if (e.d != nullptr) stage_f32_sw128(stg_f32, lane, v);
+    act_dispatch(e.act, [&](auto A) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= act_fwd(e.act, a[i]);
+      for (int i = 0; i < 32; ++i) v[i] *= act_fwd_c<decltype(A)::value>(a[i]);
+    });
     stage_bf16_sw64(stg_bf16, lane, v);
   } else {
+    act_dispatch(e.act, [&](auto A) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= act_grad(e.act, a[i]);
+      for (int i = 0; i < 32; ++i) v[i] *= act_grad_c<decltype(A)::value>(a[i]);
+    });
     if (e.d_dtype == TPS_F32)
       stage_f32_sw128(stg_f32, lane, v);
     else
@@ -111,14 +117,16 @@ __device__ __forceinline__ void tc_store_glu_bwd_chunk(const Epilogue& e, const 
                                                        const float (&hg)[32], float (&u)[32]) {
   if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
   __syncwarp();
+  act_dispatch(e.act, [&](auto A) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float f, g;
-    act_fwd_grad(e.act, hg[i], f, g);
-    const float da = v[i];
-    v[i] = da * u[i] * g;
-    u[i] = da * f;
-  }
+    for (int i = 0; i < 32; ++i) {
+      float f, g;
+      act_fwd_grad_c<decltype(A)::value>(hg[i], f, g);
+      const float da = v[i];
+      v[i] = da * u[i] * g;
+      u[i] = da * f;
+    }
+  });
   stage_bf16_sw64(stg_bf16, lane, v);
   stage_bf16_sw64(stg_f32, lane, u);
   fence_async_smem();
@@ -140,8 +148,10 @@ __device__ __forceinline__ void tc_store_glu_chunk(const Epilogue& e, const CUte
   __syncwarp();
   stage_f32_sw128(stg, lane, hg);
   stage_f32_sw128(stg + TC_STG_F32_BYTES, lane, u);
+  act_dispatch(e.act, [&](auto A) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) u[i] *= act_fwd(e.act, hg[i]);
+    for (int i = 0; i < 32; ++i) u[i] *= act_fwd_c<decltype(A)::value>(hg[i]);
+  });
   stage_bf16_sw64(stg + 2 * TC_STG_F32_BYTES, lane, u);
   fence_async_smem();
   __syncwarp();
