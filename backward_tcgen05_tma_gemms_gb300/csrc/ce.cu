@@ -842,7 +842,10 @@ constexpr int CEF_VEC = 4;                                 // float4 loads per t
 constexpr int64_t CEF_ITEM = CEF_THREADS * 4 * CEF_VEC;   // 4096 elements
 
 // dlogits = e^{z - m}/s - 1[j = y], streamed over (token, 4096-column item)
-// work items by a persistent grid; all loads of an item are issued first.
+// work items by a persistent grid sized to the blocks that fit at once.
+// The loads are software-pipelined: each thread issues the next item's
+// 16-byte loads before the exponentials and stores of the current one, so
+// HBM reads stay in flight through the arithmetic.
 template <typename TOut>
 __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CeParams p, const float* ms) {
   const int64_t per_row = (p.V + CEF_ITEM - 1) / CEF_ITEM;
@@ -851,6 +854,24 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
                    ((reinterpret_cast<uintptr_t>(p.z) & 15u) == 0) &&
                    ((reinterpret_cast<uintptr_t>(p.dlog) & (4 * sizeof(TOut) - 1)) == 0);
   const float sc = grad_scale(p);
+  auto load_item = [&](int64_t it, float4 (&w)[CEF_VEC]) {
+    const int64_t t = it / per_row;
+    const int64_t c0 = (it - t * per_row) * CEF_ITEM;
+    const float* zrow = p.z + t * p.ldz;
+#pragma unroll
+    for (int k = 0; k < CEF_VEC; ++k) {
+      const int64_t e = c0 + 4 * (threadIdx.x + k * CEF_THREADS);
+      if (vec && e + 3 < p.V) w[k] = __ldcs(reinterpret_cast<const float4*>(zrow + e));
+      else {
+        w[k].x = (e + 0 < p.V) ? zrow[e + 0] : 0.0f;
+        w[k].y = (e + 1 < p.V) ? zrow[e + 1] : 0.0f;
+        w[k].z = (e + 2 < p.V) ? zrow[e + 2] : 0.0f;
+        w[k].w = (e + 3 < p.V) ? zrow[e + 3] : 0.0f;
+      }
+    }
+  };
+  float4 v[CEF_VEC];
+  if (blockIdx.x < items) load_item(blockIdx.x, v);
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
     const int64_t t = it / per_row;
     const int64_t c0 = (it - t * per_row) * CEF_ITEM;
@@ -858,20 +879,9 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
     const float ml = mi.x * kLog2e, inv = mi.y * sc;
     const int64_t y0 = load_label(p, t);
     const int64_t y = label_kind(p, y0) == 1 ? -1 : y0;  // an ignored row has no one-hot
-    const float* zrow = p.z + t * p.ldz;
     TOut* grow = static_cast<TOut*>(p.dlog) + t * p.ldg;
-    float4 v[CEF_VEC];
-#pragma unroll
-    for (int k = 0; k < CEF_VEC; ++k) {
-      const int64_t e = c0 + 4 * (threadIdx.x + k * CEF_THREADS);
-      if (vec && e + 3 < p.V) v[k] = __ldcs(reinterpret_cast<const float4*>(zrow + e));
-      else {
-        v[k].x = (e + 0 < p.V) ? zrow[e + 0] : 0.0f;
-        v[k].y = (e + 1 < p.V) ? zrow[e + 1] : 0.0f;
-        v[k].z = (e + 2 < p.V) ? zrow[e + 2] : 0.0f;
-        v[k].w = (e + 3 < p.V) ? zrow[e + 3] : 0.0f;
-      }
-    }
+    float4 nv[CEF_VEC];
+    if (it + gridDim.x < items) load_item(it + gridDim.x, nv);
 #pragma unroll
     for (int k = 0; k < CEF_VEC; ++k) {
       const int64_t e = c0 + 4 * (threadIdx.x + k * CEF_THREADS);
@@ -907,6 +917,8 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
         if (e + 3 < p.V) store_grad(grow + e + 3, g3);
       }
     }
+#pragma unroll
+    for (int k = 0; k < CEF_VEC; ++k) v[k] = nv[k];
   }
 }
 
@@ -969,7 +981,16 @@ int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t 
   int dev = 0, sms = 1;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const unsigned grid = static_cast<unsigned>(sms * 8);
+  // exactly the blocks that fit at once: a larger grid would run as a
+  // second, partial wave
+  static int occ_f = 0, occ_b = 0;
+  static std::once_flag occ_once;
+  std::call_once(occ_once, [] {
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_f, ce_grad_stream_kernel<float>, CEF_THREADS, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_b, ce_grad_stream_kernel<__nv_bfloat16>, CEF_THREADS, 0);
+  });
+  const int occ = (c.dlogits_dtype == TPS_F32 ? occ_f : occ_b);
+  const unsigned grid = static_cast<unsigned>(sms * (occ > 0 ? occ : 1));
   if (c.dlogits_dtype == TPS_F32)
     ce_grad_stream_kernel<float><<<grid, CEF_THREADS, 0, stream>>>(p, ms);
   else
