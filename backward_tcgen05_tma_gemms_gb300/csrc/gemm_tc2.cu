@@ -51,7 +51,7 @@ namespace tps {
 constexpr int T2_BM = 128;      // rows per CTA (256 per pair)
 constexpr int T2_BN = 256;      // columns per pair tile
 constexpr int T2_BN_CTA = 128;  // B columns staged by each CTA
-constexpr int T2_STAGES = 4;
+constexpr int T2_MAX_STAGES = 5;
 constexpr int T2_A_BYTES = T2_BM * TC_BK * 2;      // 16 KB
 constexpr int T2_B_BYTES = T2_BN_CTA * TC_BK * 2;  // 16 KB
 constexpr int T2_STAGE_BYTES = T2_A_BYTES + T2_B_BYTES;
@@ -59,12 +59,11 @@ constexpr int T2_THREADS = 320;
 constexpr int T2_EPI_WARPS = 8;
 constexpr uint32_t T2_TMEM_COLS = 2 * T2_BN;  // two fp32 accumulators
 constexpr int T2_STG_BUF = TC_STG_F32_BYTES + TC_STG_BF16_BYTES;  // 6 KB, one buffer
-constexpr int T2_STAGING_BYTES = T2_EPI_WARPS * 2 * T2_STG_BUF;   // 96 KB
 static_assert(T2_BN / 2 == kStatsTileN, "each epilogue warp covers one CE statistics tile");
 
 struct T2Barriers {
-  uint64_t full[T2_STAGES];
-  uint64_t empty[T2_STAGES];
+  uint64_t full[T2_MAX_STAGES];
+  uint64_t empty[T2_MAX_STAGES];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
@@ -72,8 +71,6 @@ struct T2Barriers {
   uint32_t abort;
 };
 
-constexpr size_t T2_SMEM_BYTES = 1024 + T2_STAGES * T2_STAGE_BYTES + T2_STAGING_BYTES + sizeof(T2Barriers);
-static_assert(T2_SMEM_BYTES <= 232448, "exceeds the opt-in shared memory per block");
 
 // Tensor maps of one launch: a[s], b[s] are the operands of contraction
 // segment s (b[1] is the up weight of the gated forward); with column
@@ -95,10 +92,37 @@ struct T2Params {
   uint32_t* err;
 };
 
-// Epilogue families, compiled as separate kernels so that the gated forms'
-// extra live registers do not cost the plain ones a spill.
-// T2_SEG: plain stores with contraction or column segments.
-enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2, T2_SEG = 3 };
+// Epilogue families, compiled as separate kernels so that one form's extra
+// live registers and staging do not cost another its registers or stages.
+//   T2_PLAIN    EPI_STORE, EPI_CE_STATS (one output box per chunk)
+//   T2_ACT      EPI_ACT_FWD, EPI_ACT_BWD, EPI_GLU_UP
+//   T2_GLU_FWD  EPI_GLU_FWD
+//   T2_GLU_BWD  EPI_GLU_BWD
+//   T2_SEG      EPI_STORE with contraction or column segments
+enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2, T2_SEG = 3, T2_ACT = 4 };
+
+// Shared-memory layout per family: operand stages of 32 KB and the
+// epilogue's staging.  With four stages the mainloop measured latency-bound
+// (the MLP GEMMs ran 8 % and the CE GEMMs 4-5 % slower than with five at
+// the Llama shapes); a sixth stage, where it fits, measured slower again.
+//   plain, segmented  one 4 KB box per warp (fp32 and bf16 share it),
+//                     double-buffered                       -> 5 stages
+//   act               fp32 + bf16 boxes (6 KB), single       -> 5 stages
+//   gated backward    two bf16 boxes (4 KB), double-buffered -> 5 stages
+//   gated forward     Hg, U (fp32) + A (bf16): 10 KB         -> 4 stages
+template <int FAM>
+struct T2Layout {
+  static constexpr bool kStoreOnly = FAM == T2_PLAIN || FAM == T2_SEG;
+  static constexpr int kStages = FAM == T2_GLU_FWD ? 4 : 5;
+  static constexpr int kBufBytes =
+      kStoreOnly ? TC_STG_F32_BYTES : (FAM == T2_GLU_BWD ? 2 * TC_STG_BF16_BYTES : T2_STG_BUF);
+  static constexpr int kBufs = (FAM == T2_GLU_BWD || kStoreOnly) ? 2 : 1;
+  static constexpr int kWarpStaging = FAM == T2_GLU_FWD ? 2 * T2_STG_BUF : kBufs * kBufBytes;
+  static constexpr size_t kSmem =
+      1024 + kStages * T2_STAGE_BYTES + T2_EPI_WARPS * kWarpStaging + sizeof(T2Barriers);
+  static_assert(kStages <= T2_MAX_STAGES, "barrier arrays hold T2_MAX_STAGES stages");
+  static_assert(kSmem <= 232448, "exceeds the opt-in shared memory per block");
+};
 
 template <bool A_MN, bool B_MN, int FAM>
 __global__ void __launch_bounds__(T2_THREADS, 1)
@@ -106,8 +130,10 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  using L = T2Layout<FAM>;
+  constexpr int T2_STAGES = L::kStages;
   uint8_t* staging = smem + T2_STAGES * T2_STAGE_BYTES;  // 1024-aligned
-  T2Barriers* bars = reinterpret_cast<T2Barriers*>(staging + T2_STAGING_BYTES);
+  T2Barriers* bars = reinterpret_cast<T2Barriers*>(staging + T2_EPI_WARPS * L::kWarpStaging);
   volatile uint32_t* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -252,11 +278,10 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     const int ew = warp - 2;       // 0..7
     const int q = warp & 3;        // TMEM lane quadrant
     const int h = ew >> 2;         // column half of the 256-column tile
-    uint8_t* stg = staging + ew * 2 * T2_STG_BUF;
+    uint8_t* stg = staging + ew * L::kWarpStaging;
     const Epilogue& e = p.epi;
-    // segmented launches are plain stores: no statistics, no AUX
     const bool ce = FAM == T2_PLAIN && e.mode == EPI_CE_STATS;
-    const bool bwd = FAM == T2_PLAIN && p.tma_store && (e.mode == EPI_ACT_BWD || e.mode == EPI_GLU_UP);
+    const bool bwd = FAM == T2_ACT && p.tma_store && (e.mode == EPI_ACT_BWD || e.mode == EPI_GLU_UP);  // AUX prefetch
     constexpr bool glu = FAM == T2_GLU_FWD;
     constexpr bool gbwd = FAM == T2_GLU_BWD;
     // accumulator columns this warp drains: 128 (gated: 64 gate + 64 up)
@@ -325,8 +350,8 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-            uint8_t* buf = stg + (chunk & 1u) * T2_STG_BUF;
-            tc_store_glu_bwd_chunk(e, &m.d[0], &m.d[1], buf, buf + TC_STG_F32_BYTES, lane, row0, col0, v, hg, u);
+            uint8_t* buf = stg + (chunk & 1u) * L::kBufBytes;  // dU box, then the dHg box
+            tc_store_glu_bwd_chunk(e, &m.d[0], &m.d[1], buf, buf + TC_STG_BF16_BYTES, lane, row0, col0, v, hg, u);
             ++chunk;
           } else {
             tmem_ld_wait();
@@ -359,8 +384,10 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
           if (row < p.M) epilogue_run32(e, row, col0, n, v);
           continue;
         }
-        uint8_t* buf = stg + (chunk & 1u) * T2_STG_BUF;
-        tc_store_chunk<1, FAM == T2_SEG>(e, &m.d[oseg], &m.d[1], buf, buf + TC_STG_F32_BYTES, lane, row0,
+        // the fp32 and bf16 slots (store-only: one shared box), single- or double-buffered
+        uint8_t* buf = stg + (L::kBufs == 2 ? (chunk & 1u) * L::kBufBytes : 0u);
+        tc_store_chunk<L::kBufs - 1, L::kStoreOnly>(e, &m.d[oseg], &m.d[1], buf,
+                                                    L::kStoreOnly ? buf : buf + TC_STG_F32_BYTES, lane, row0,
                                          col0 - ocol0, v, a);
         ++chunk;
       }
@@ -390,13 +417,13 @@ static int launch_pair_typed(const GemmDesc& g, const T2Maps& m, const T2Params&
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN, FAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(T2_SMEM_BYTES));
+                                    static_cast<int>(T2Layout<FAM>::kSmem));
   });
   if (attr_err != cudaSuccess) return TPS_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
   cfg.blockDim = dim3(T2_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = T2_SMEM_BYTES;
+  cfg.dynamicSmemBytes = T2Layout<FAM>::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -430,6 +457,8 @@ static int launch_pair_family(const GemmDesc& g, const T2Maps& m, const T2Params
     if (g.epi.mode != EPI_STORE) return TPS_ERR_ARG;
     return launch_pair_majors<T2_SEG>(g, m, p, pairs, a_mn, b_mn, stream);
   }
+  if (g.epi.mode == EPI_ACT_FWD || g.epi.mode == EPI_ACT_BWD || g.epi.mode == EPI_GLU_UP)
+    return launch_pair_majors<T2_ACT>(g, m, p, pairs, a_mn, b_mn, stream);
   return launch_pair_majors<T2_PLAIN>(g, m, p, pairs, a_mn, b_mn, stream);
 }
 
