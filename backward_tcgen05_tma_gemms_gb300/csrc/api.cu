@@ -1009,7 +1009,7 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
   weight_strides(w, weight_layout, &w_in, &w_out);  // W(dd, v)
 
   // z = h Whead: vocabulary shards are column ranges of z.  On the tensor
-  // cores (shards of at least one 256-column tile) the epilogue also leaves
+  // cores (shards of at least one 128-column statistics tile) the epilogue also leaves
   // each shard's partial softmax statistics per tile.
   GemmDesc g;
   g.name = "ce_logits";

@@ -785,7 +785,7 @@ __global__ void __launch_bounds__(1024) ce_finalize_kernel(const float* loss, in
 }
 
 // ------------------------------------------------------------ from tile statistics
-// The logits GEMM's epilogue left, per (token, 256-column tile), the
+// The logits GEMM's epilogue left, per (token, 128-column tile), the
 // statistics of the tile's columns split at the shard boundary.  Shard r's
 // (m_r, s_r) combines the tiles whose first column lies in r (their first
 // part) and, when r starts inside a tile, that tile's second part.

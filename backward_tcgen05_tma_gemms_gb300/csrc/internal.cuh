@@ -19,7 +19,7 @@ constexpr uint32_t TPS_DEVERR_LABEL = 2u;
 // EPI_ACT_BWD  D = acc * phi'(AUX), AUX the fp32 pre-activation
 // EPI_CE_STATS D = acc (fp32 logits), and per (row, 128-column tile) the
 //              softmax statistics of the tile's columns, split at the
-//              vocabulary-shard boundary (see CeTileStats)
+//              vocabulary-shard boundary (see CeTileAcc)
 // Gated MLP (Hg = X Wg, U = X Wu, A = phi(Hg) * U):
 // EPI_GLU_FWD  CTA-pair kernel only: each pair tile holds 128 gate columns
 //              (from B) and the same 128 up columns (from the up operand);
