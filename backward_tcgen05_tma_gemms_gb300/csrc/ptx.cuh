@@ -52,6 +52,21 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity
   return ok;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` (it returns as
+// soon as the phase completes), so waiting warps stop polling.
+__device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok;
+}
+constexpr uint32_t kWaitSuspendNs = 100000;
+
 // Bounded wait for the phase with the given parity.  `abort_flag` (shared
 // memory) lets one role tell the others to stop waiting after a timeout.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
@@ -59,7 +74,7 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, vo
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSuspendNs)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
@@ -77,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // MMAs before a CTA exits); still bounded in time.
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* err) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSuspendNs)) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       atomicOr(err, TPS_DEVERR_TIMEOUT);
       return;

@@ -255,6 +255,23 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device error {rc} in the timed region")
     launches = prof.launches
 
+    # ---- the same step captured once in a CUDA graph and replayed
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(d)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    graph_ms = g0.elapsed_time(g1) / args.steps
+    if api.last_device_error() != 0:
+        raise RuntimeError("device error in the graph replays")
+    del graph
+
     # ---- end-to-end: pinned host inputs in, results out, every step.
     # Three streams pipeline consecutive steps: host->device copies of step
     # i+1's inputs and device->host copies of step i-1's results overlap the
@@ -332,9 +349,9 @@ def run_gpu(args, rank, world, local_rank):
 
     # max over ranks
     if world > 1:
-        ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
+        ms, e2e_ms, graph_ms = max_over_ranks([ms, e2e_ms, graph_ms], dev)
     widened = None if args.no_widened else run_widened(args, dev, d)
-    return dict(ms=ms, e2e_ms=e2e_ms, prof=prof.summary, launches=launches, clocks=clk.summary(), h2d=h2d, d2h=d2h,
+    return dict(ms=ms, e2e_ms=e2e_ms, graph_ms=graph_ms, prof=prof.summary, launches=launches, clocks=clk.summary(), h2d=h2d, d2h=d2h,
                 host=host, widened=widened)
 
 
@@ -527,6 +544,8 @@ def main():
                "hbm_peak_gbs": hbm_peak, "peak_source": peak_src},
         "per_kernel_ms_per_step": {k: v["ms"] / args.steps for k, v in r["prof"].items()},
         "gpu_launches": r["launches"],
+        "graph": {"ms_per_step": r["graph_ms"], "value": STEP_FLOPS * world / (r["graph_ms"] * 1e-3) / 1e12,
+                  "what": "the same step captured once in a CUDA graph and replayed (inputs resident)"},
         "clocks": r["clocks"],
         "e2e": {"value": STEP_FLOPS * world / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
