@@ -3,8 +3,9 @@
  * (sm_103a).  Built as libtps.so from backward_tcgen05_tma_gemms_gb300/csrc.
  *
  * The library computes the forward and backward of a matrix product split
- * over P logical ranks, the column-then-row tensor-parallel MLP and the
- * vocabulary-sharded cross-entropy.  On one GPU the logical ranks are shard
+ * over P logical ranks, the column-then-row tensor-parallel MLP (plain and
+ * gated), the head-split attention projections and the vocabulary-sharded
+ * cross-entropy.  On one GPU the logical ranks are shard
  * partitions of the same device buffers: a result the pages concatenate is a
  * range of one output buffer, and a result the pages sum over ranks is
  * accumulated inside the producing kernel (the contraction loop runs over
@@ -38,6 +39,13 @@
  *     cores).  Results named "fp32" are always TPS_F32.
  *   - Thread safety.  Entry points may be called from several host threads;
  *     launches on one stream execute in issue order.
+ *   - CUDA graphs.  tps_matmul_fwd_bwd, tps_mlp_fwd_bwd, tps_glu_mlp_fwd_bwd,
+ *     tps_attn_qkv_fwd, tps_attn_qkv_bwd, tps_attn_out_fwd_bwd,
+ *     tps_vocab_ce_fwd_bwd and tps_vocab_ce_fwd_bwd_ex enqueue only kernel
+ *     launches and memsets on `cuda_stream`; their one-time set-up runs on
+ *     the first call on a device.  After one such call they may be captured
+ *     into a CUDA graph; a replay reads and writes the buffers given at
+ *     capture.  tps_last_device_error synchronizes and must not be captured.
  */
 #ifndef TPS_H_
 #define TPS_H_
