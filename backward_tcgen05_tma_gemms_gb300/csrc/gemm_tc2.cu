@@ -101,7 +101,7 @@ struct T2Params {
 //   T2_SEG      EPI_STORE with contraction or column segments
 enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2, T2_SEG = 3, T2_ACT = 4 };
 
-// Shared-memory layout per family: operand stages of 32 KB and the
+// Shared-memory layout per family: five operand stages of 32 KB and the
 // epilogue's staging.  With four stages the mainloop measured latency-bound
 // (the MLP GEMMs ran 8 % and the CE GEMMs 4-5 % slower than with five at
 // the Llama shapes); a sixth stage, where it fits, measured slower again.
@@ -109,15 +109,16 @@ enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2, T2_SEG = 3, 
 //                     double-buffered                       -> 5 stages
 //   act               fp32 + bf16 boxes (6 KB), single       -> 5 stages
 //   gated backward    two bf16 boxes (4 KB), double-buffered -> 5 stages
-//   gated forward     Hg, U (fp32) + A (bf16): 10 KB         -> 4 stages
+//   gated forward     Hg then U through one fp32 box, A bf16
+//                     (6 KB), single-buffered                -> 5 stages
 template <int FAM>
 struct T2Layout {
   static constexpr bool kStoreOnly = FAM == T2_PLAIN || FAM == T2_SEG;
-  static constexpr int kStages = FAM == T2_GLU_FWD ? 4 : 5;
+  static constexpr int kStages = 5;
   static constexpr int kBufBytes =
       kStoreOnly ? TC_STG_F32_BYTES : (FAM == T2_GLU_BWD ? 2 * TC_STG_BF16_BYTES : T2_STG_BUF);
   static constexpr int kBufs = (FAM == T2_GLU_BWD || kStoreOnly) ? 2 : 1;
-  static constexpr int kWarpStaging = FAM == T2_GLU_FWD ? 2 * T2_STG_BUF : kBufs * kBufBytes;
+  static constexpr int kWarpStaging = kBufs * kBufBytes;
   static constexpr size_t kSmem =
       1024 + kStages * T2_STAGE_BYTES + T2_EPI_WARPS * kWarpStaging + sizeof(T2Barriers);
   static_assert(kStages <= T2_MAX_STAGES, "barrier arrays hold T2_MAX_STAGES stages");

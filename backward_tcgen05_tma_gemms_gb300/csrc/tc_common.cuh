@@ -138,27 +138,37 @@ __device__ __forceinline__ void tc_store_glu_bwd_chunk(const Epilogue& e, const 
   }
 }
 
-// EPI_GLU_FWD chunk through TMA stores from one 10 KB staging buffer: Hg
-// (fp32) at +0, U (fp32) at +4 KB, A = phi(Hg) * U (bf16) at +8 KB.  The
-// buffer is reused only after this warp's earlier stores have read it.
+// EPI_GLU_FWD chunk through TMA stores from a 6 KB staging buffer: Hg and
+// then U (fp32) pass through the same 4 KB box at +0 -- U is staged once
+// the Hg store has read the box -- and A = phi(Hg) * U (bf16) through the
+// 2 KB box at +4 KB.  The buffer is reused only after this warp's earlier
+// stores have read it.
 __device__ __forceinline__ void tc_store_glu_chunk(const Epilogue& e, const CUtensorMap* tmHg, const CUtensorMap* tmA,
                                                    const CUtensorMap* tmU, uint8_t* stg, int lane, int row0,
                                                    int col0, const float (&hg)[32], float (&u)[32]) {
   if (lane == 0) bulk_wait_read0();
   __syncwarp();
   stage_f32_sw128(stg, lane, hg);
-  stage_f32_sw128(stg + TC_STG_F32_BYTES, lane, u);
-  act_dispatch(e.act, [&](auto A) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) u[i] *= act_fwd_c<decltype(A)::value>(hg[i]);
-  });
-  stage_bf16_sw64(stg + 2 * TC_STG_F32_BYTES, lane, u);
   fence_async_smem();
   __syncwarp();
   if (lane == 0) {
     tma_store_2d(tmHg, stg, col0, row0);
-    tma_store_2d(tmU, stg + TC_STG_F32_BYTES, col0, row0);
-    tma_store_2d(tmA, stg + 2 * TC_STG_F32_BYTES, col0, row0);
+    bulk_commit();
+  }
+  float a[32];
+  act_dispatch(e.act, [&](auto A) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a[i] = u[i] * act_fwd_c<decltype(A)::value>(hg[i]);
+  });
+  stage_bf16_sw64(stg + TC_STG_F32_BYTES, lane, a);
+  if (lane == 0) bulk_wait_read0();  // the Hg store has read the fp32 box
+  __syncwarp();
+  stage_f32_sw128(stg, lane, u);
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmU, stg, col0, row0);
+    tma_store_2d(tmA, stg + TC_STG_F32_BYTES, col0, row0);
     bulk_commit();
   }
 }
