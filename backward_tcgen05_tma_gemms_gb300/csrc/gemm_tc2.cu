@@ -299,12 +299,10 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         while (oseg < p.n_segs - 1 && nh0 >= p.n_end[oseg]) ++oseg;
         ocol0 = oseg > 0 ? p.n_end[oseg - 1] : 0;
       }
-      if (!mbar_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.err)) break;
-      tc_fence_after();
       const int row0 = m0 + q * 32;
       const int64_t row = row0 + lane;
-      const uint32_t t_row =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * T2_BN + static_cast<uint32_t>(h * warp_cols);
+      // The first chunk's AUX input does not depend on the accumulator: it
+      // is loaded before waiting for it.
       float a_next[32];
       if (bwd) {
         if (row < p.M && nh0 < p.N) {
@@ -314,6 +312,10 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
           for (int i = 0; i < 32; ++i) a_next[i] = 0.0f;
         }
       }
+      if (!mbar_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * T2_BN + static_cast<uint32_t>(h * warp_cols);
       CeTileAcc st;
       for (int c = 0; c < warp_cols / 32; ++c) {
         const int col0 = nh0 + c * 32;
