@@ -149,3 +149,55 @@ def test_plan_heads_matches_oracle(orc):
                 q_off, kv_first, cnt, rep = api.plan_heads(H, Hkv, tp)
                 assert q_off == want[0].tolist() and kv_first == want[1].tolist(), (H, Hkv, tp)
                 assert (cnt, rep) == (want[2], want[3]), (H, Hkv, tp)
+
+
+def test_widened_rows_validation_codes(lib):
+    """The gated MLP, attention projections and extended CE reject bad
+    arguments with the documented codes before anything is launched."""
+    from backward_tcgen05_tma_gemms_gb300.api import TpsCeOptions, NO_IGNORE
+    r = ctypes.byref
+    ws = ctypes.c_void_p(0x100000)
+    # gated MLP: X 16x64, Wg/Wu 64x96, W2 96x64
+    X, Wg, Wu, W2, GY = _fake([16, 64]), _fake([64, 96]), _fake([64, 96]), _fake([96, 64]), _fake([16, 64])
+    outs = [_fake([16, 64]), _fake([16, 64]), _fake([64, 96]), _fake([64, 96]), _fake([96, 64])]
+    glu = lambda tp=4, act=3, wu=Wu, size=1 << 30, x=X: lib.tps_glu_mlp_fwd_bwd(
+        r(x), r(Wg), r(wu), r(W2), r(GY), tp, act, 0, *[r(o) for o in outs], ws, size, None)
+    assert glu(tp=0) == 2
+    assert glu(act=9) == 9
+    assert glu(wu=_fake([64, 95])) == 1
+    assert glu(x=_fake([16, 64], dtype=1)) == 3
+    assert glu(size=64) == 6
+    # attention: 6 query heads of 16, 2 KV heads
+    Xa, Wq, Wk, Wv = _fake([8, 32]), _fake([32, 96]), _fake([32, 32]), _fake([32, 32])
+    Q, K, V = _fake([8, 96]), _fake([8, 32]), _fake([8, 32])
+    qkv = lambda H=6, Hkv=2, tp=2, wk=Wk, q=Q, k=K: lib.tps_attn_qkv_fwd(
+        r(Xa), r(Wq), r(wk), r(Wv), H, Hkv, tp, 0, r(q), r(k), r(V), None)
+    assert qkv(tp=4) == 2                       # 6 heads do not split over 4 ranks
+    assert qkv(H=4, Hkv=3) == 2                 # 4 query heads do not group over 3 KV heads
+    assert qkv(H=5, Hkv=1, tp=1) == 1           # 96 columns are not 5 whole heads
+    assert qkv(wk=_fake([32, 48])) == 1         # Wk not H_kv heads wide
+    assert qkv(q=_fake([8, 95])) == 1
+    assert qkv(k=_fake([8, 32], dtype=1)) == 3  # Q, K, V dtypes differ
+    C, Wo, G = _fake([8, 96]), _fake([96, 32]), _fake([8, 32])
+    out = lambda H=6, tp=2, dc=_fake([8, 96]): lib.tps_attn_out_fwd_bwd(
+        r(C), r(Wo), r(G), H, tp, 0, r(_fake([8, 32])), r(dc), r(_fake([96, 32])), None)
+    assert out(tp=4) == 2
+    assert out(dc=_fake([8, 96], dtype=3)) == 3
+    # extended CE: vocabulary 100, 4 tokens
+    h, W, lab = _fake([4, 16]), _fake([16, 100]), _fake([4], dtype=3)
+    loss, dl, dh = _fake([4]), _fake([4, 100]), _fake([4, 16])
+
+    def ce(ignore=NO_IGNORE, vocab=0, red=0, den=0.0, reserved=0, lred=None, dw=None):
+        o = TpsCeOptions(ignore, vocab, red, reserved, den)
+        return lib.tps_vocab_ce_fwd_bwd_ex(r(h), r(W), r(lab), 2, 0, r(o), r(loss),
+                                           r(lred) if lred is not None else None, r(dl), r(dh),
+                                           r(dw) if dw is not None else None, None, ws, 1 << 30, None)
+    assert ce(vocab=101) == 1
+    assert ce(vocab=-1) == 1
+    assert ce(red=3) == 9
+    assert ce(red=2, den=-1.0) == 9
+    assert ce(red=2, den=float("nan")) == 9
+    assert ce(reserved=1) == 9
+    assert ce(red=1, lred=_fake([2])) == 1      # loss_reduced holds one float
+    assert ce(dw=_fake([16, 99])) == 1          # dWhead must match Whead
+    assert ce(dw=_fake([16, 100], dtype=1)) == 3
