@@ -201,3 +201,25 @@ def test_widened_rows_validation_codes(lib):
     assert ce(red=1, lred=_fake([2])) == 1      # loss_reduced holds one float
     assert ce(dw=_fake([16, 99])) == 1          # dWhead must match Whead
     assert ce(dw=_fake([16, 100], dtype=1)) == 3
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/tps.h is a C ABI: it compiles as strict C99 and as C++."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "use_tps.c"
+    src.write_text('#include "tps.h"\n'
+                   'int main(void) {\n'
+                   '  tps_ce_options o = {TPS_NO_IGNORE, 0, TPS_REDUCE_MEAN, 0, 0.0};\n'
+                   '  tps_tensor t;\n'
+                   '  (void)o; (void)t;\n'
+                   '  return TPS_OK;\n'
+                   '}\n')
+    inc = os.path.join(ROOT, "include")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, "-c", str(src), "-o",
+                    str(tmp_path / "c.o")], check=True)
+    if shutil.which("g++"):
+        subprocess.run(["g++", "-std=c++11", "-Wall", "-Werror", "-I", inc, "-x", "c++", "-c", str(src), "-o",
+                        str(tmp_path / "cpp.o")], check=True)
