@@ -100,3 +100,11 @@ def test_llama_shape_sampled(orc):
     assert_close(dWv[:, kc].cpu(), rdwv, True, "dWv cols")
     _, _, rdwo = orc.attn_out(f["C"][:, qc], f["Wo"][qc], f["GY"])
     assert_close(dWo[qc].cpu(), rdwo, True, "dWo rows")
+
+
+@pytest.mark.parametrize("T", [0, 3])
+def test_bf16_few_tokens(orc, T):
+    c = inputs.attn_case(40 + T, max(T, 1), 128, 4, 2, 64, torch.bfloat16, w_std=0.1)
+    for k in ("X", "dQ", "dK", "dV", "C", "GY"):
+        c[k] = c[k][:T].contiguous()
+    check(orc, c, 4, 2, 2, "in_out", True, f"T={T}")

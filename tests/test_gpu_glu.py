@@ -104,3 +104,12 @@ def test_llama_shape_sampled(orc):
     assert_close(dW2[cols].cpu(), rdW2, True, "dW2 rows")
     for t in out:
         assert torch.isfinite(t).all()
+
+
+@pytest.mark.parametrize("T", [0, 1, 5])
+def test_bf16_few_tokens(orc, T):
+    """A single pair tile that is almost (or wholly) outside the token range;
+    with no tokens every weight gradient is an exact zero."""
+    X, Wg, Wu, W2, GY = inputs.glu_case(31 + T, max(T, 1), 64, 256, torch.bfloat16, w_std=0.1)
+    X, GY = X[:T].contiguous(), GY[:T].contiguous()
+    run_and_check(orc, X, Wg, Wu, W2, GY, 2, "silu", "in_out", True, f"T={T}")
