@@ -334,17 +334,26 @@ int tc_num_sms() {
 // Tile order and L2 policy.  Consecutive tiles walk groups of 16 M-tiles
 // (M fastest), so a wave of tiles touches a compact block of A rows and B
 // columns and consecutive waves share the group's A slabs.
-// TPS_GEMM_GROUP overrides the group size; TPS_GEMM_L2_HINTS=1 marks A (the
-// operand a group revisits) evict-last and B evict-first.
+// TPS_GEMM_GROUP overrides the group size.  TPS_GEMM_L2_HINTS=1 marks A (the
+// operand a group revisits) evict-last and B evict-first; two digits "ab"
+// choose each operand's policy (0 none, 1 evict-first, 2 evict-last).  The
+// default carries no hint: every hinted form measured slower.
 void tc_raster_choice(int m_tiles, int* raster_n, int* group, int* pol_a, int* pol_b) {
   const char* gv = getenv("TPS_GEMM_GROUP");
   const char* hv = getenv("TPS_GEMM_L2_HINTS");
   const int g = (gv && atoi(gv) > 0) ? atoi(gv) : TC_GROUP_M;
-  const int hints = hv ? atoi(hv) : 0;
   *raster_n = 0;
   *group = g < m_tiles ? g : m_tiles;
-  *pol_a = hints ? 2 : 0;
-  *pol_b = hints ? 1 : 0;
+  *pol_a = 0;
+  *pol_b = 0;
+  if (hv == nullptr) return;
+  if (hv[0] >= '0' && hv[0] <= '2' && hv[1] >= '0' && hv[1] <= '2' && hv[2] == '\0') {
+    *pol_a = hv[0] - '0';
+    *pol_b = hv[1] - '0';
+  } else if (atoi(hv) != 0) {
+    *pol_a = 2;
+    *pol_b = 1;
+  }
 }
 
 // The tensor-core path needs bf16 operands that TMA can describe: 16-byte

@@ -87,6 +87,7 @@ struct T2Params {
   int n_segs, n_end[3];                      // column segments: cumulative column ends
   int glu;                                   // EPI_GLU_FWD: b[1] is the up weight
   int raster_n, group;
+  int pol_a, pol_b;  // L2 policy kinds of the operand loads (0 none, 1 evict-first, 2 evict-last)
   int tma_store;
   Epilogue epi;
   uint32_t* err;
@@ -124,6 +125,15 @@ struct T2Layout {
   static_assert(kStages <= T2_MAX_STAGES, "barrier arrays hold T2_MAX_STAGES stages");
   static_assert(kSmem <= 232448, "exceeds the opt-in shared memory per block");
 };
+
+// A paired operand load that carries an L2 policy only when one was chosen.
+__device__ __forceinline__ void pair_load(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int32_t c0,
+                                          int32_t c1, int kind, uint64_t policy) {
+  if (kind != 0)
+    tma_load_2d_pair_hint(dst, map, bar_cluster, c0, c1, policy);
+  else
+    tma_load_2d_pair(dst, map, bar_cluster, c0, c1);
+}
 
 template <bool A_MN, bool B_MN, int FAM>
 __global__ void __launch_bounds__(T2_THREADS, 1)
@@ -180,6 +190,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
+      const uint64_t pa = tc_policy(p.pol_a), pb = tc_policy(p.pol_b);
       for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
         int mt, nt;
         tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
@@ -208,17 +219,18 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
           const CUtensorMap* mb = ks > 0 ? &m.b[ks] : mb0;
           const int k0 = (kt - (ks > 0 ? p.k_end[ks - 1] : 0)) * TC_BK;
           if (!A_MN) {
-            tma_load_2d_pair(sa, ma, fb, k0, m0);
+            pair_load(sa, ma, fb, k0, m0, p.pol_a, pa);
           } else {
 #pragma unroll
-            for (int j = 0; j < T2_BM / 64; ++j) tma_load_2d_pair(sa + j * TC_MN_BOX_BYTES, ma, fb, m0 + 64 * j, k0);
+            for (int j = 0; j < T2_BM / 64; ++j)
+              pair_load(sa + j * TC_MN_BOX_BYTES, ma, fb, m0 + 64 * j, k0, p.pol_a, pa);
           }
           if (!B_MN) {
-            tma_load_2d_pair(sb, mb, fb, k0, nb0);
+            pair_load(sb, mb, fb, k0, nb0, p.pol_b, pb);
           } else {
 #pragma unroll
             for (int j = 0; j < T2_BN_CTA / 64; ++j)
-              tma_load_2d_pair(sb + j * TC_MN_BOX_BYTES, mb, fb, nb0 + 64 * j, k0);
+              pair_load(sb + j * TC_MN_BOX_BYTES, mb, fb, nb0 + 64 * j, k0, p.pol_b, pb);
           }
           ++issued;
           if (++stage == T2_STAGES) {
@@ -529,9 +541,8 @@ int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   }
   if (n_segs && nc != g.N) return TPS_ERR_ARG;
   p.num_tiles = p.m_tiles * p.n_tiles;
-  int pol_a = 0, pol_b = 0;
   // groups of pair tiles cover the same rows as twice as many single tiles
-  tc_raster_choice(2 * p.m_tiles, &p.raster_n, &p.group, &pol_a, &pol_b);
+  tc_raster_choice(2 * p.m_tiles, &p.raster_n, &p.group, &p.pol_a, &p.pol_b);
   p.group = (p.group + 1) / 2;
   if (p.group < 1) p.group = 1;
   if (p.group > p.m_tiles) p.group = p.m_tiles;
