@@ -882,7 +882,7 @@ extern "C" int tps_attn_out_fwd_bwd(const tps_tensor* C, const tps_tensor* Wo, c
 // combined (m, 1/s) per token (T x 2) | 256 bytes of scalars (the count of
 // supervised labels, int32 at +0, and the gradient scale, f32 at +16).
 struct CeWs {
-  size_t z, stats, zy, tiles, ms, scal, total;
+  size_t z, stats, zy, tiles, shift, ms, scal, total;
 };
 static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp) {
   const size_t t = static_cast<size_t>(T);
@@ -892,7 +892,8 @@ static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp) {
   w.stats = w.z + align256(t * static_cast<size_t>(V) * 4);
   w.zy = w.stats + align256(t * static_cast<size_t>(tp) * 2 * 4);
   w.tiles = w.zy + align256(t * 4);
-  w.ms = w.tiles + align256(t * n_tiles * 4 * 4);
+  w.shift = w.tiles + align256(t * n_tiles * 4 * 4);
+  w.ms = w.shift + align256(t * n_tiles * 4);
   w.scal = w.ms + align256(t * 2 * 4);
   w.total = w.scal + 256;
   return w;
@@ -1002,6 +1003,7 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
   float* stats = reinterpret_cast<float*>(ws + lay.stats);
   float* zy = reinterpret_cast<float*>(ws + lay.zy);
   float* tile_stats = reinterpret_cast<float*>(ws + lay.tiles);
+  float* shift = reinterpret_cast<float*>(ws + lay.shift);
   float* ms = reinterpret_cast<float*>(ws + lay.ms);
   char* scal = ws + lay.scal;
   const int64_t n_tiles = (V + kStatsTileN - 1) / kStatsTileN;
@@ -1009,8 +1011,10 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
   weight_strides(w, weight_layout, &w_in, &w_out);  // W(dd, v)
 
   // z = h Whead: vocabulary shards are column ranges of z.  On the tensor
-  // cores (shards of at least one 128-column statistics tile) the epilogue also leaves
-  // each shard's partial softmax statistics per tile.
+  // cores (shards of at least one 128-column statistics tile) the epilogue
+  // also leaves each shard's partial softmax statistics per tile, and stores
+  // z as bf16 relative to each tile's max, with the shifts and the fp32
+  // logit at each label beside it; otherwise z is fp32.
   GemmDesc g;
   g.name = "ce_logits";
   g.M = T; g.N = V; g.K = d; g.in_dtype = dt;
@@ -1020,16 +1024,25 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
   const bool fused = gemm_tc_supported(g) && ce_tile_stats_supported(V, tp);
   if (fused) {
     g.epi.mode = EPI_CE_STATS;
+    g.epi.d_dtype = TPS_BF16;
     g.epi.stats = tile_stats;
     g.epi.n_tiles = n_tiles;
     g.epi.ce_parts = tp;
     g.epi.ce_vreal = vreal;
+    g.epi.ce_shift = shift;
+    g.epi.ce_labels = labels->data;
+    g.epi.ce_label_i64 = labels->dtype == TPS_I64 ? 1 : 0;
+    g.epi.ce_zy = zy;
   }
   if ((rc = run_gemm(g, V, 1, s))) return rc;
   {
     CeDesc c;
     c.T = T; c.V = V; c.parts = tp;
     c.logits = z; c.ldz = V;
+    if (fused) {
+      c.logits16 = z;
+      c.shift = shift;
+    }
     c.labels = labels->data; c.label_dtype = labels->dtype;
     c.loss = static_cast<float*>(loss->data);
     c.dlogits = dl.data; c.ldg = dl.sr; c.dlogits_dtype = dt;

@@ -44,6 +44,12 @@ struct CeParams {
   int32_t parts;
   const float* z;
   int64_t ldz;
+  // the logits GEMM's CE-statistics epilogue: bf16 logits relative to the
+  // shift of their 128-column tile (leading dimension ldz), the shifts
+  // (T x n_tiles) and, in zy, the fp32 logit at each label
+  const __nv_bfloat16* z16;
+  const float* zshift;
+  int64_t n_tiles;
   const void* labels;
   int label_is_i64;
   float* loss;
@@ -822,7 +828,7 @@ __global__ void __launch_bounds__(32 * CEF_TOK_PER_BLOCK) ce_combine_kernel(cons
       p.loss[t] = 0.0f;
       if (p.owner) p.owner[t] = -1;
     } else if (kind == 0) {
-      p.loss[t] = logf(s) + m - p.z[t * p.ldz + y];
+      p.loss[t] = logf(s) + m - p.zy[t];
       if (p.owner) {
         int32_t r = 0;
         while (r + 1 < p.parts && shard_offset(p.V, p.parts, r + 1) <= y) ++r;
@@ -838,39 +844,58 @@ __global__ void __launch_bounds__(32 * CEF_TOK_PER_BLOCK) ce_combine_kernel(cons
 }
 
 constexpr int CEF_THREADS = 256;
-constexpr int CEF_VEC = 4;                                 // float4 loads per thread per item
-constexpr int64_t CEF_ITEM = CEF_THREADS * 4 * CEF_VEC;   // 4096 elements
+constexpr int CEF_VEC = 4;                                 // 16-byte loads (8 logits) per thread per item
+constexpr int64_t CEF_ITEM = CEF_THREADS * 8 * CEF_VEC;   // 8192 columns
 
-// dlogits = e^{z - m}/s - 1[j = y], streamed over (token, 4096-column item)
+// The two bf16 values packed in a 32-bit word, low half first, as floats.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// dlogits = e^{z - m}/s - 1[j = y], streamed over (token, 8192-column item)
 // work items by a persistent grid sized to the blocks that fit at once.
-// The loads are software-pipelined: each thread issues the next item's
-// 16-byte loads before the exponentials and stores of the current one, so
-// HBM reads stay in flight through the arithmetic.
+// The logits arrive as bf16 z~ = z - c, relative to the shift c of their
+// 128-column statistics tile, so e^{z - m} = 2^{z~ log2(e) + (c - m) log2(e)}
+// (one FMA and one ex2 per element).  The loads are software-pipelined:
+// each thread issues the next item's 16-byte loads before the exponentials
+// and stores of the current one, so HBM reads stay in flight through the
+// arithmetic.
 template <typename TOut>
 __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CeParams p, const float* ms) {
   const int64_t per_row = (p.V + CEF_ITEM - 1) / CEF_ITEM;
   const int64_t items = p.T * per_row;
-  const bool vec = ((p.ldz & 3) == 0) && ((p.ldg & 3) == 0) &&
-                   ((reinterpret_cast<uintptr_t>(p.z) & 15u) == 0) &&
-                   ((reinterpret_cast<uintptr_t>(p.dlog) & (4 * sizeof(TOut) - 1)) == 0);
+  const bool vec = ((p.ldz & 7) == 0) && ((p.ldg & 7) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(p.z16) & 15u) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(p.dlog) & 15u) == 0);
   const float sc = grad_scale(p);
-  auto load_item = [&](int64_t it, float4 (&w)[CEF_VEC]) {
+  struct Item {
+    uint4 z[CEF_VEC];   // 8 bf16 logits (relative to their tile's shift) per load
+    float c[CEF_VEC];   // the shift of each load's tile
+  };
+  auto load_item = [&](int64_t it, Item& w) {
     const int64_t t = it / per_row;
     const int64_t c0 = (it - t * per_row) * CEF_ITEM;
-    const float* zrow = p.z + t * p.ldz;
+    const __nv_bfloat16* zrow = p.z16 + t * p.ldz;
+    const unsigned short* zbits = reinterpret_cast<const unsigned short*>(zrow);
+    const float* crow = p.zshift + t * p.n_tiles;
 #pragma unroll
     for (int k = 0; k < CEF_VEC; ++k) {
-      const int64_t e = c0 + 4 * (threadIdx.x + k * CEF_THREADS);
-      if (vec && e + 3 < p.V) w[k] = __ldcs(reinterpret_cast<const float4*>(zrow + e));
-      else {
-        w[k].x = (e + 0 < p.V) ? zrow[e + 0] : 0.0f;
-        w[k].y = (e + 1 < p.V) ? zrow[e + 1] : 0.0f;
-        w[k].z = (e + 2 < p.V) ? zrow[e + 2] : 0.0f;
-        w[k].w = (e + 3 < p.V) ? zrow[e + 3] : 0.0f;
+      const int64_t e = c0 + 8 * (threadIdx.x + k * CEF_THREADS);
+      w.c[k] = (e < p.V) ? crow[e / kStatsTileN] : 0.0f;
+      if (vec && e + 7 < p.V) {
+        w.z[k] = __ldcs(reinterpret_cast<const uint4*>(zrow + e));
+      } else {
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t lo = (e + 2 * j < p.V) ? zbits[e + 2 * j] : 0u;
+          const uint32_t hi = (e + 2 * j + 1 < p.V) ? zbits[e + 2 * j + 1] : 0u;
+          q[j] = lo | (hi << 16);
+        }
+        w.z[k] = make_uint4(q[0], q[1], q[2], q[3]);
       }
     }
   };
-  float4 v[CEF_VEC];
+  Item v;
   if (blockIdx.x < items) load_item(blockIdx.x, v);
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
     const int64_t t = it / per_row;
@@ -880,45 +905,48 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
     const int64_t y0 = load_label(p, t);
     const int64_t y = label_kind(p, y0) == 1 ? -1 : y0;  // an ignored row has no one-hot
     TOut* grow = static_cast<TOut*>(p.dlog) + t * p.ldg;
-    float4 nv[CEF_VEC];
+    Item nv;
     if (it + gridDim.x < items) load_item(it + gridDim.x, nv);
 #pragma unroll
     for (int k = 0; k < CEF_VEC; ++k) {
-      const int64_t e = c0 + 4 * (threadIdx.x + k * CEF_THREADS);
-      float g0 = exp_shift(v[k].x, ml) * inv, g1 = exp_shift(v[k].y, ml) * inv;
-      float g2 = exp_shift(v[k].z, ml) * inv, g3 = exp_shift(v[k].w, ml) * inv;
-      if (y >= e && y < e + 4) {
-        const int64_t d = y - e;
-        g0 -= (d == 0) ? sc : 0.0f;
-        g1 -= (d == 1) ? sc : 0.0f;
-        g2 -= (d == 2) ? sc : 0.0f;
-        g3 -= (d == 3) ? sc : 0.0f;
+      const int64_t e = c0 + 8 * (threadIdx.x + k * CEF_THREADS);
+      if (e >= p.V) continue;
+      const float adj = fmaf(v.c[k], kLog2e, -ml);  // (c - m) log2(e)
+      const uint32_t wd[4] = {v.z[k].x, v.z[k].y, v.z[k].z, v.z[k].w};
+      float g[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        g[2 * j] = ex2_approx(fmaf(bf16_lo(wd[j]), kLog2e, adj)) * inv;
+        g[2 * j + 1] = ex2_approx(fmaf(bf16_hi(wd[j]), kLog2e, adj)) * inv;
       }
-      if (e + 3 >= p.vreal) {  // vocabulary padding
-        g0 = (e + 0 < p.vreal) ? g0 : 0.0f;
-        g1 = (e + 1 < p.vreal) ? g1 : 0.0f;
-        g2 = (e + 2 < p.vreal) ? g2 : 0.0f;
-        g3 = (e + 3 < p.vreal) ? g3 : 0.0f;
+      if (y >= e && y < e + 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] -= (y == e + j) ? sc : 0.0f;
       }
-      if (vec && e + 3 < p.V) {
+      if (e + 7 >= p.vreal) {  // vocabulary padding
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = (e + j < p.vreal) ? g[j] : 0.0f;
+      }
+      if (vec && e + 7 < p.V) {
         if constexpr (sizeof(TOut) == 2) {
-          __nv_bfloat162 a = __floats2bfloat162_rn(g0, g1), b = __floats2bfloat162_rn(g2, g3);
-          uint2 w;
-          w.x = *reinterpret_cast<uint32_t*>(&a);
-          w.y = *reinterpret_cast<uint32_t*>(&b);
-          __stcs(reinterpret_cast<uint2*>(grow + e), w);
+          uint32_t q[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(g[2 * j], g[2 * j + 1]);
+            q[j] = *reinterpret_cast<uint32_t*>(&b);
+          }
+          __stcs(reinterpret_cast<uint4*>(grow + e), make_uint4(q[0], q[1], q[2], q[3]));
         } else {
-          __stcs(reinterpret_cast<float4*>(grow + e), make_float4(g0, g1, g2, g3));
+          __stcs(reinterpret_cast<float4*>(grow + e), make_float4(g[0], g[1], g[2], g[3]));
+          __stcs(reinterpret_cast<float4*>(grow + e + 4), make_float4(g[4], g[5], g[6], g[7]));
         }
       } else {
-        if (e + 0 < p.V) store_grad(grow + e + 0, g0);
-        if (e + 1 < p.V) store_grad(grow + e + 1, g1);
-        if (e + 2 < p.V) store_grad(grow + e + 2, g2);
-        if (e + 3 < p.V) store_grad(grow + e + 3, g3);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (e + j < p.V) store_grad(grow + e + j, g[j]);
       }
     }
-#pragma unroll
-    for (int k = 0; k < CEF_VEC; ++k) v[k] = nv[k];
+    v = nv;
   }
 }
 
@@ -931,6 +959,9 @@ static CeParams make_params(const CeDesc& c, uint32_t* dev_err) {
   p.parts = c.parts;
   p.z = c.logits;
   p.ldz = c.ldz;
+  p.z16 = static_cast<const __nv_bfloat16*>(c.logits16);
+  p.zshift = c.shift;
+  p.n_tiles = 0;
   p.labels = c.labels;
   p.label_is_i64 = (c.label_dtype == TPS_I64);
   p.loss = c.loss;
@@ -962,11 +993,13 @@ static int launch_finalize(const CeDesc& c, bool want_scale, bool want_reduced, 
 int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,
                               uint32_t* dev_err, cudaStream_t stream) {
   if (c.T == 0) return TPS_OK;
+  if (c.logits16 == nullptr || c.shift == nullptr || c.zy == nullptr) return TPS_ERR_ARG;
   CeParams p = make_params(c, dev_err);
   p.stats = nullptr;
-  p.zy = nullptr;
+  p.n_tiles = n_tiles;
   const int64_t gsize = c.dlogits_dtype == TPS_F32 ? 4 : 2;
-  const double bytes = double(c.T) * double(c.V) * (4.0 + gsize) + double(c.T) * (8.0 + 4.0);
+  const double bytes = double(c.T) * double(c.V) * (2.0 + gsize) + double(c.T) * double(n_tiles) * 4.0 +
+                       double(c.T) * (8.0 + 4.0);
   ProfScope prof("ce_stream", "ce_core", 0.0, bytes, stream);
   const int64_t nb = (c.T + CEF_TOK_PER_BLOCK - 1) / CEF_TOK_PER_BLOCK;
   if (nb > 0x7FFFFFFF) return TPS_ERR_SHAPE;

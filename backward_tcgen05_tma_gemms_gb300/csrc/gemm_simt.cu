@@ -169,8 +169,9 @@ int launch_gemm_simt(const GemmDesc& g, uint32_t* /*dev_err*/, cudaStream_t stre
   p.b3_sk = g.b3_sk;
   p.b3_sn = g.b3_sn;
   p.kparts = g.kparts < 1 ? 1 : g.kparts;
-  // the fused gate/up form and column segments are tensor-core only
-  if (g.epi.mode == EPI_GLU_FWD || g.n_segs > 1) return TPS_ERR_ARG;
+  // the fused gate/up form, the CE statistics form and column segments are
+  // tensor-core only
+  if (g.epi.mode == EPI_GLU_FWD || g.epi.mode == EPI_CE_STATS || g.n_segs > 1) return TPS_ERR_ARG;
   p.epi = g.epi;
   const int64_t gx = (g.N + SG_BN - 1) / SG_BN, gy = (g.M + SG_BM - 1) / SG_BM;
   if (gx > 0x7FFFFFFF || gy > 65535) return TPS_ERR_SHAPE;

@@ -229,8 +229,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int i = 0; i < 32; ++i) a_next[i] = 0.0f;
         }
       }
-      CeTileAcc st;
-      for (int c = 0; c < TC_BN / 32; ++c) {
+      if (ce) {  // the warp's 256 columns are two statistics tiles
+        const int64_t y = row < p.M ? ce_row_label(e, row) : -1;
+        float zy = 0.0f, a[32];
+        bool have = false;
+        for (int tt = 0; tt < TC_BN / kStatsTileN; ++tt) {
+          const int tc0 = n0 + tt * kStatsTileN;
+          if (tc0 >= p.N) break;  // warp-uniform
+          ce_stats_tile(e, t_row + tt * kStatsTileN, tc0, p.N, row < p.M, row, y, zy, have,
+                        [&](int64_t col0, int n, float(&v)[32]) {
+                          if (!p.tma_store) {
+                            if (row < p.M) epilogue_run32(e, row, col0, n, v);
+                            return;
+                          }
+                          tc_store_chunk<0>(e, &tmD, &tmD2, stg_f32, stg_bf16, lane, row0, static_cast<int>(col0), v,
+                                            a);
+                        });
+        }
+        if (have) e.ce_zy[row] = zy;
+      }
+      for (int c = 0; !ce && c < TC_BN / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= p.N) break;  // warp-uniform
         uint32_t r[32];
@@ -247,13 +265,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         const int n = min(32, p.N - col0);
-        if (ce) {
-          constexpr int kChunks = kStatsTileN / 32;
-          if (c % kChunks == 0) st.reset(e, p.N, col0);
-          st.fold(v, col0, n, e.ce_vreal);
-          if ((c % kChunks == kChunks - 1 || col0 + 32 >= p.N) && row < p.M)
-            st.flush(e, row, static_cast<int64_t>(col0) / kStatsTileN);
-        }
         if (!p.tma_store) {
           if (row < p.M) epilogue_run32(e, row, col0, n, v);
           continue;
@@ -367,6 +378,9 @@ bool gemm_tc_supported(const GemmDesc& g) {
   if (g.M >= (1ll << 31) || g.N >= (1ll << 31) || g.K + g.K2 + g.K3 >= (1ll << 31)) return false;
   const bool k_segs = g.K2 > 0 || g.K3 > 0;
   if (g.epi.mode == EPI_GLU_FWD && (g.b_up == nullptr || k_segs || g.n_segs > 1)) return false;
+  if (g.epi.mode == EPI_CE_STATS && (g.epi.d_dtype != TPS_BF16 || g.epi.stats == nullptr || g.epi.ce_shift == nullptr ||
+                                     g.epi.ce_labels == nullptr || g.epi.ce_zy == nullptr))
+    return false;
   if (g.n_segs < 1 || g.n_segs > 3 || (g.n_segs > 1 && k_segs)) return false;
   if ((g.n_segs > 1 || k_segs) && g.epi.mode != EPI_STORE) return false;  // segments: plain stores only
   auto ok_operand = [](const void* ptr, int64_t s_outer, int64_t s_inner, int64_t inner_extent) {

@@ -328,8 +328,28 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       tc_fence_after();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * T2_BN + static_cast<uint32_t>(h * warp_cols);
-      CeTileAcc st;
-      for (int c = 0; c < warp_cols / 32; ++c) {
+      bool ce_done = false;
+      if constexpr (FAM == T2_PLAIN) {
+        if (ce) {  // the warp's 128 columns are one statistics tile
+          ce_done = true;
+          if (nh0 < p.N) {
+            const int64_t y = row < p.M ? ce_row_label(e, row) : -1;
+            float zy = 0.0f, a[32];
+            bool have = false;
+            ce_stats_tile(e, t_row, nh0, p.N, row < p.M, row, y, zy, have, [&](int64_t col0, int n, float(&v)[32]) {
+              if (!p.tma_store) {
+                if (row < p.M) epilogue_run32(e, row, col0, n, v);
+                return;
+              }
+              uint8_t* buf = stg + (chunk & 1u) * L::kBufBytes;
+              tc_store_chunk<1, true>(e, &m.d[0], &m.d[1], buf, buf, lane, row0, static_cast<int>(col0), v, a);
+              ++chunk;
+            });
+            if (have) e.ce_zy[row] = zy;
+          }
+        }
+      }
+      for (int c = 0; !ce_done && c < warp_cols / 32; ++c) {
         const int col0 = nh0 + c * 32;
         if (col0 >= p.N) break;  // warp-uniform
         uint32_t r[32];
@@ -389,12 +409,6 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         const int n = min(32, p.N - col0);
-        if (ce) {
-          if (c == 0) st.reset(e, p.N, col0);
-          st.fold(v, col0, n, e.ce_vreal);
-          if ((c == warp_cols / 32 - 1 || col0 + 32 >= p.N) && row < p.M)
-            st.flush(e, row, static_cast<int64_t>(nh0) / kStatsTileN);
-        }
         if (!p.tma_store) {
           if (row < p.M) epilogue_run32(e, row, col0, n, v);
           continue;

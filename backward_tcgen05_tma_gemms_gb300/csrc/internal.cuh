@@ -17,9 +17,12 @@ constexpr uint32_t TPS_DEVERR_LABEL = 2u;
 // EPI_STORE    D = acc                                  (dtype d_dtype)
 // EPI_ACT_FWD  D = acc (fp32, may be null), D2 = phi(acc) (dtype d2_dtype)
 // EPI_ACT_BWD  D = acc * phi'(AUX), AUX the fp32 pre-activation
-// EPI_CE_STATS D = acc (fp32 logits), and per (row, 128-column tile) the
+// EPI_CE_STATS tensor-core kernels only.  Per (row, 128-column tile): the
 //              softmax statistics of the tile's columns, split at the
-//              vocabulary-shard boundary (see CeTileAcc)
+//              vocabulary-shard boundary (see CeTileAcc), and the shift
+//              c = max over the tile's real columns (0 when it has none);
+//              D = bf16(acc - c), the logits relative to their tile's max;
+//              and, per row, the fp32 logit at the row's label column
 // Gated MLP (Hg = X Wg, U = X Wu, A = phi(Hg) * U):
 // EPI_GLU_FWD  CTA-pair kernel only: each pair tile holds 128 gate columns
 //              (from B) and the same 128 up columns (from the up operand);
@@ -69,6 +72,10 @@ struct Epilogue {
   // Columns at or beyond ce_vreal are vocabulary padding: they are stored
   // but left out of the statistics.
   int64_t ce_vreal = INT64_MAX;
+  float* ce_shift = nullptr;        // shift[row * n_tiles + tile]
+  const void* ce_labels = nullptr;  // the label of each row, int32 or int64
+  int ce_label_i64 = 0;
+  float* ce_zy = nullptr;           // zy[row]: the logit at the label (labels in [0, N))
 };
 
 // One GEMM D[M x N] = sum_k A(m, k) B(k, n), operands addressed by element
@@ -129,6 +136,11 @@ struct CeDesc {
   int32_t parts = 1;
   const float* logits = nullptr;  // T x V fp32, leading dimension ldz
   int64_t ldz = 0;
+  // launch_ce_from_tile_stats reads the logits the EPI_CE_STATS epilogue
+  // left instead: T x V bf16 relative to their tile's shift (leading
+  // dimension ldz), the shifts (T x n_tiles) and the label logits in zy.
+  const void* logits16 = nullptr;
+  const float* shift = nullptr;
   const void* labels = nullptr;   // T, int32 or int64
   int label_dtype = TPS_I64;
   float* loss = nullptr;          // T fp32
@@ -137,7 +149,7 @@ struct CeDesc {
   int dlogits_dtype = TPS_BF16;
   int32_t* owner = nullptr;       // T, nullable
   float* stats = nullptr;         // workspace T x parts x 2 (two-pass path)
-  float* zy = nullptr;            // workspace T (two-pass path)
+  float* zy = nullptr;            // workspace T: the logit at each label
   // Extended form (tps_vocab_ce_fwd_bwd_ex); when `options` is false the
   // fields below are ignored and every label must lie in [0, V).
   bool options = false;
@@ -152,7 +164,8 @@ struct CeDesc {
 // Vocabulary CE when the logits GEMM already produced per-tile statistics
 // (EPI_CE_STATS): a combine kernel forms each shard's (m_r, s_r), the global
 // log-sum-exp, the loss and the owner; a streaming kernel writes dlogits.
-// `tile_stats` is T x n_tiles x 4 floats, `ms` is T x 2 floats of scratch.
+// `tile_stats` is T x n_tiles x 4 floats, `ms` is T x 2 floats of scratch;
+// the logits come from c.logits16, c.shift and c.zy.
 int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,
                               uint32_t* dev_err, cudaStream_t stream);
 bool ce_tile_stats_supported(int64_t V, int32_t parts);

@@ -175,28 +175,30 @@ __device__ __forceinline__ void tc_store_glu_chunk(const Epilogue& e, const CUte
 
 // ---- vocabulary-CE statistics in the logits epilogue ----------------------
 // Each epilogue thread owns one output row, so the statistics of a
-// kStatsTileN-column tile need no cross-thread reduction: the thread folds
-// its chunks into (max, sum of e^{z - max}) for the part of the tile in
-// shard a (the shard of the tile's first column) and the part in shard b
-// (the next one).
+// kStatsTileN-column tile need no cross-thread reduction.  The tile is read
+// from tensor memory twice: the first pass finds the max of the part of the
+// tile in shard a (the shard of the tile's first column) and of the part in
+// shard b (the next one); the second sums e^{z - max} for each part, takes
+// the logit at the row's label, and stores the tile relative to its max
+// (the larger of the two), which bf16 then holds to 2^-9 of the distance
+// from the max: the softmax weights that matter keep fp32-level accuracy.
 
-// Fold elements [i0, i1) of v into (m, s); each element is predicated.
-__device__ __forceinline__ void ce_fold(const float (&v)[32], int i0, int i1, float& m, float& s) {
+// Max of elements [i0, i1) of v (-inf for an empty range).
+__device__ __forceinline__ float ce_chunk_max(const float (&v)[32], int i0, int i1) {
   float cm = -INFINITY;
 #pragma unroll
   for (int i = 0; i < 32; ++i)
     if (i >= i0 && i < i1) cm = fmaxf(cm, v[i]);
-  if (cm == -INFINITY) return;
-  if (cm > m) {
-    s = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - cm) * kTcLog2e);
-    m = cm;
-  }
+  return cm;
+}
+// Sum of e^{v - m} over elements [i0, i1) of v (m finite when the range is not empty).
+__device__ __forceinline__ float ce_chunk_sum(const float (&v)[32], int i0, int i1, float m) {
   const float ml = m * kTcLog2e;
   float acc = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i)
     if (i >= i0 && i < i1) acc += ex2_approx(fmaf(v[i], kTcLog2e, -ml));
-  s += acc;
+  return acc;
 }
 
 // The shard owning column c under the array_split of n into p parts.
@@ -205,7 +207,6 @@ __device__ __forceinline__ int64_t shard_of(int64_t c, int64_t n, int64_t p) {
   return c < big ? c / (q + 1) : r + (c - big) / q;
 }
 
-// Per-row running statistics of one kStatsTileN-column tile.
 struct CeTileAcc {
   int64_t split;  // first column of shard b
   float ma, sa, mb, sb;
@@ -216,19 +217,86 @@ struct CeTileAcc {
     mb = -INFINITY;
     sb = 0.0f;
   }
-  // Fold the chunk of columns [col0, col0 + n).
-  // Fold the chunk of columns [col0, col0 + n); columns at or beyond
-  // `vreal` are vocabulary padding and stay out of the statistics.
-  __device__ __forceinline__ void fold(const float (&v)[32], int64_t col0, int n, int64_t vreal) {
-    if (vreal - col0 < n) n = static_cast<int>(vreal - col0 < 0 ? 0 : vreal - col0);
-    const int na = static_cast<int>(split - col0 < 0 ? 0 : (split - col0 > n ? n : split - col0));
-    ce_fold(v, 0, na, ma, sa);
-    if (na < n) ce_fold(v, na, n, mb, sb);
+  // Of the chunk [col0, col0 + n): the real columns (those below vreal;
+  // the rest are vocabulary padding) end at chunk index nn, shard a's at na.
+  __device__ __forceinline__ void parts(int64_t col0, int n, int64_t vreal, int& na, int& nn) const {
+    nn = (vreal - col0 < n) ? static_cast<int>(vreal - col0 < 0 ? 0 : vreal - col0) : n;
+    na = static_cast<int>(split - col0 < 0 ? 0 : (split - col0 > nn ? nn : split - col0));
+  }
+  __device__ __forceinline__ void fold_max(const float (&v)[32], int64_t col0, int n, int64_t vreal) {
+    int na, nn;
+    parts(col0, n, vreal, na, nn);
+    ma = fmaxf(ma, ce_chunk_max(v, 0, na));
+    mb = fmaxf(mb, ce_chunk_max(v, na, nn));
+  }
+  __device__ __forceinline__ void fold_sum(const float (&v)[32], int64_t col0, int n, int64_t vreal) {
+    int na, nn;
+    parts(col0, n, vreal, na, nn);
+    if (na > 0) sa += ce_chunk_sum(v, 0, na, ma);
+    if (nn > na) sb += ce_chunk_sum(v, na, nn, mb);
+  }
+  __device__ __forceinline__ float shift() const {
+    const float m = fmaxf(ma, mb);
+    return m == -INFINITY ? 0.0f : m;
   }
   __device__ __forceinline__ void flush(const Epilogue& e, int64_t row, int64_t stat_tile) const {
     *reinterpret_cast<float4*>(e.stats + (row * e.n_tiles + stat_tile) * 4) = make_float4(ma, sa, mb, sb);
+    e.ce_shift[row * e.n_tiles + stat_tile] = shift();
   }
 };
+
+// The label of row `row` (int32 or int64 labels).
+__device__ __forceinline__ int64_t ce_row_label(const Epilogue& e, int64_t row) {
+  return e.ce_label_i64 ? static_cast<const int64_t*>(e.ce_labels)[row]
+                        : static_cast<int64_t>(static_cast<const int32_t*>(e.ce_labels)[row]);
+}
+
+// EPI_CE_STATS over the statistics tile that starts at column tc0 (TMEM
+// address t_col), for the row this thread owns (row_ok: row < M; label y).
+// Each 32-column chunk leaves through store(col0, n, v) with v relative to
+// the tile's shift; zy receives the label's logit when the label lies in
+// the tile (have = true).
+template <class Store>
+__device__ __forceinline__ void ce_stats_tile(const Epilogue& e, uint32_t t_col, int64_t tc0, int64_t N, bool row_ok,
+                                              int64_t row, int64_t y, float& zy, bool& have, Store&& store) {
+  constexpr int kChunks = kStatsTileN / 32;
+  const int chunks = static_cast<int>((N - tc0) / 32 < kChunks ? (N - tc0 + 31) / 32 : kChunks);
+  CeTileAcc st;
+  st.reset(e, N, tc0);
+  for (int c = 0; c < chunks; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_col + c * 32, r);
+    tmem_ld_wait();
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    const int64_t col0 = tc0 + 32 * c;
+    st.fold_max(v, col0, static_cast<int>(N - col0 < 32 ? N - col0 : 32), e.ce_vreal);
+  }
+  const float sh = st.shift();
+  for (int c = 0; c < chunks; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_col + c * 32, r);
+    tmem_ld_wait();
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    const int64_t col0 = tc0 + 32 * c;
+    const int n = static_cast<int>(N - col0 < 32 ? N - col0 : 32);
+    st.fold_sum(v, col0, n, e.ce_vreal);
+    const int64_t dy = y - col0;
+    if (dy >= 0 && dy < n) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i == dy) zy = v[i];
+      have = true;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] -= sh;
+    store(col0, n, v);
+  }
+  if (row_ok) st.flush(e, row, tc0 / kStatsTileN);
+}
 
 // ---- tile raster and L2 policy -------------------------------------------
 // Tiles are walked in groups of `group` M-tiles, M fastest (raster_n = 0),

@@ -37,13 +37,16 @@ CE = inputs.LLAMA_CE
 MLP_FLOPS = 6 * 2.0 * MLP["T"] * MLP["d"] * MLP["F"]          # 5.772e12
 CE_GEMM_FLOPS = 2 * 2.0 * CE["T"] * CE["d"] * CE["V"]          # 1.722e13
 STEP_FLOPS = MLP_FLOPS + CE_GEMM_FLOPS
-# CE core (per-shard stats, combine, dlogits): one fp32 read of the logits,
+# The logits GEMM leaves the logits as bf16 relative to the max of their
+# 128-column tile, with one fp32 shift per tile.
+CE_TILES = (CE["V"] + 127) // 128
+# CE core (combine, dlogits): one read of the bf16 logits and their shifts,
 # one bf16 write of dlogits, the label (int64) and the loss (fp32) per token.
-CE_CORE_BYTES_PER_TOKEN = CE["V"] * (4 + 2) + 8 + 4
+CE_CORE_BYTES_PER_TOKEN = CE["V"] * (2 + 2) + 4 * CE_TILES + 8 + 4
 # Algorithmic DRAM bytes of the step's eight GEMM launches, averaged per
 # launch: every operand read once and every output written once (bf16
-# operands, fp32 results; the column GEMM also writes the fp32
-# pre-activation, the dZ GEMM also reads it).
+# operands, fp32 results except the shifted bf16 logits; the column GEMM
+# also writes the fp32 pre-activation, the dZ GEMM also reads it).
 def _gemm_algo_bytes():
     T, d, F, V = MLP["T"], MLP["d"], MLP["F"], CE["V"]
     b = 0
@@ -53,7 +56,7 @@ def _gemm_algo_bytes():
     b += 2 * T * F + 2 * T * d + 4 * F * d                  # dW2: Ha, GY -> dW2
     b += 2 * T * d + 2 * T * F + 4 * d * F                  # dW1: X, dZ -> dW1
     b += 2 * T * F + 2 * d * F + 4 * T * d                  # dX: dZ, W1 -> dX
-    b += 2 * T * d + 2 * d * V + 4 * T * V                  # logits: h, W -> z (f32)
+    b += 2 * T * d + 2 * d * V + 2 * T * V + 4 * T * CE_TILES  # logits: h, W -> z (bf16, shifted), shifts
     b += 2 * T * V + 2 * d * V + 4 * T * d                  # dHidden: dlogits, W -> dh
     return b / 8
 
