@@ -180,8 +180,10 @@ __device__ __forceinline__ void tc_store_glu_chunk(const Epilogue& e, const CUte
 // tile in shard a (the shard of the tile's first column) and of the part in
 // shard b (the next one); the second sums e^{z - max} for each part, takes
 // the logit at the row's label, and stores the tile relative to its max
-// (the larger of the two), which bf16 then holds to 2^-9 of the distance
-// from the max: the softmax weights that matter keep fp32-level accuracy.
+// (the larger of the two).  bf16 rounds z - max to within 2^-8 of its
+// magnitude, so a softmax weight p = e^{z - m} / s is off by at most
+// p (max - z) 2^-8 <= 2^-8 / e in absolute terms, and the weights near the
+// max, which dominate, are nearly exact.
 
 // Max of elements [i0, i1) of v (-inf for an empty range).
 __device__ __forceinline__ float ce_chunk_max(const float (&v)[32], int i0, int i1) {

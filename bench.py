@@ -71,13 +71,18 @@ GEMM_SOURCES = ["gemm_tc.cu", "gemm_tc2.cu", "tc_common.cuh", "ptx.cuh", "epilog
 
 
 def kernel_source_hash(names):
-    """sha256 over the CUDA sources a kernel is built from, to tell whether
-    recorded ncu counters still describe the current kernel."""
+    """sha256 over the CUDA sources a kernel is built from, without comments
+    and whitespace, to tell whether recorded ncu counters still describe the
+    current kernel."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "backward_tcgen05_tma_gemms_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "backward_tcgen05_tma_gemms_gb300", "csrc", n)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()
 
 
