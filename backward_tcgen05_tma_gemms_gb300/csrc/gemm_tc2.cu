@@ -558,6 +558,16 @@ int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   // groups of pair tiles cover the same rows as twice as many single tiles
   tc_raster_choice(2 * p.m_tiles, &p.raster_n, &p.group, &p.pol_a, &p.pol_b);
   p.group = (p.group + 1) / 2;
+  // A wider group pays while its A panels (group x 256 rows x K) stay in
+  // L2 from one wave of tiles to the next: B then streams once per group,
+  // and fewer groups mean fewer passes over B (the vocabulary head of the
+  // logits GEMM: 6.6 GB read with 8 pair rows per group, 3.4 GB with 16).
+  // Longer panels are evicted within a wave anyway, and there the wave's
+  // count of distinct panels, about group + 76 / group, is smallest at 8.
+  if (getenv("TPS_GEMM_GROUP") == nullptr) {
+    const int64_t k_total = static_cast<int64_t>(g.K) + g.K2 + g.K3;
+    if (16ll * 2 * T2_BM * k_total * 2 <= (40ll << 20)) p.group = 16;
+  }
   if (p.group < 1) p.group = 1;
   if (p.group > p.m_tiles) p.group = p.m_tiles;
   p.epi = g.epi;

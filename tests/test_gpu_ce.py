@@ -105,6 +105,21 @@ def test_bf16_shard_layouts(orc, tp, V, T, gemm_kernel):
     assert expect in kinds, p.summary
 
 
+@pytest.mark.parametrize("T", [64, 300])
+def test_bf16_large_logits(orc, T, gemm_kernel):
+    """Logits up to ~240 in magnitude (weights of std 3 on d = 256).  The
+    fused path keeps the logits in bf16 relative to the max of their
+    128-column tile, which holds the softmax weights near each max to fp32
+    level (a float64 simulation of that storage: relative Frobenius error
+    of dlogits 3e-6 to 3e-5).  bf16 logits without the shift are rounded by
+    up to 2^-8 |z| (about 0.9 here) inside the exponent, and the same
+    simulation puts their dlogits 1.5-3.4 % off, beyond the tolerance."""
+    h, W, labels = inputs.ce_case(1234 + T, T, 256, 4096, torch.bfloat16, w_std=3.0)
+    with api.profile() as p:
+        check(orc, h, W, labels, 4, True, what=f"bf16 large logits T{T}")
+    assert "ce_stream" in {k.split(":")[0] for k in p.summary}, p.summary
+
+
 def test_label_out_of_range_sets_error():
     h, W, labels = inputs.ce_case(1, 4, 16, 64, torch.float32)
     labels[2] = 64
