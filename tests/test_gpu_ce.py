@@ -149,3 +149,14 @@ def test_llama_vocab_sampled(orc):
     assert torch.isfinite(loss).all()
     # mean loss near log V + var(z)/2 with var(z) = d * 0.02^2
     assert abs(loss.mean().item() - (math.log(cfg["V"]) + cfg["d"] * 0.02 ** 2 / 2)) < 0.1
+
+
+def test_bf16_int32_labels_match_int64(gemm_kernel):
+    """The logits epilogue reads each row's label to keep its fp32 logit;
+    int32 labels give bit-identical results to the same labels as int64."""
+    h, W, labels = inputs.ce_case(77, 300, 128, 4096, torch.bfloat16, w_std=0.2)
+    a, rc_a = run(h, W, labels, 4)
+    b, rc_b = run(h, W, labels.to(torch.int32), 4)
+    assert rc_a == 0 and rc_b == 0
+    for x, y, name in zip(a, b, ("loss", "dlogits", "dHidden", "owner")):
+        assert torch.equal(x, y), name

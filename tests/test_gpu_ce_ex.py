@@ -152,3 +152,13 @@ def test_bad_options():
         api.vocab_ce_fwd_bwd_ex(h, W, y, 2, vocab_size=65)
     with pytest.raises(api.TpsError):
         api.vocab_ce_fwd_bwd_ex(h, W, y, 2, reduction="mean", denominator=-1.0)
+
+
+def test_int32_labels_match_int64(gemm_kernel):
+    """ignore_index, padding and the mean with int32 labels: bit-identical
+    to the same call with int64 labels (fused statistics path)."""
+    h, W, y = case(91, 300, 128, 4096, 4000, torch.bfloat16, 40)
+    a = run(h, W, y, 4, 4000, "mean", 0.0)
+    b = run(h, W, y.to(torch.int32), 4, 4000, "mean", 0.0)
+    for x, z in zip(a, b):
+        assert torch.equal(x, z)
