@@ -272,7 +272,10 @@ int tps_attn_out_fwd_bwd(const tps_tensor* C, const tps_tensor* Wo, const tps_te
  * contiguous shards (array_split of V), forward and backward
  * ([MC] "04 / VOCABULARY SHARDS"; single supervised position per token, no
  * label smoothing, no ignore index):
- *   z = h Whead (T x V fp32, kept in the workspace);
+ *   z = h Whead (T x V, kept in the workspace: on the tensor-core path --
+ *   bf16 operands, shards of at least 128 columns -- as bf16 relative to
+ *   the max of each row's 128-column tile, with those maxima and the fp32
+ *   logit at each label beside it; otherwise fp32);
  *   per token and shard r: m_r = max_{j in V_r} z_j, s_r = sum e^{z_j - m_r};
  *   combined: m = max_r m_r, s = sum_r s_r e^{m_r - m},
  *   loss = log s + m - z_y;  dlogits_j = e^{z_j - m}/s - 1[j = y];
