@@ -160,3 +160,16 @@ def test_bf16_int32_labels_match_int64(gemm_kernel):
     assert rc_a == 0 and rc_b == 0
     for x, y, name in zip(a, b, ("loss", "dlogits", "dHidden", "owner")):
         assert torch.equal(x, y), name
+
+
+@pytest.mark.parametrize("T", [37, 300])
+def test_bf16_unaligned_vocab_rows(orc, T, gemm_kernel):
+    """V = 4100: rows of bf16 logits and dlogits are 8200 B, not a multiple
+    of 16, so the logits epilogue stores without TMA and the gradient
+    stream takes its scalar path; the head in (V, d) layout keeps the GEMM
+    operands TMA-compatible.  Shards of 2050 columns straddle tiles."""
+    h, W, labels = inputs.ce_case(4100 + T, T, 128, 4100, torch.bfloat16, w_std=0.2)
+    W = W.t().contiguous()
+    with api.profile() as p:
+        check(orc, h, W, labels, 2, True, "out_in", what=f"bf16 V4100 T{T}")
+    assert "ce_stream" in {k.split(":")[0] for k in p.summary}, p.summary
