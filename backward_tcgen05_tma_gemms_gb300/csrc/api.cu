@@ -800,17 +800,39 @@ extern "C" int tps_attn_qkv_bwd(const tps_tensor* X, const tps_tensor* Wq, const
     g.kparts = tp;
     if ((rc = run_gemm(g, dx.sr, dx.sc, s))) return rc;
   }
+  // dW(dd, j) = sum_t X[t, dd] dProj[t, j]: shard-local columns.  The three
+  // share A = X^T, so with row-contiguous gradients (in, out) they run as
+  // one launch over the concatenated columns [dWq | dWk | dWv].
+  int64_t o_in[3], o_out[3];
+  bool rows_contiguous = true;
+  for (int i = 0; i < 3; ++i) {
+    weight_strides(*dw[i], weight_layout, &o_in[i], &o_out[i]);
+    rows_contiguous = rows_contiguous && o_out[i] == 1;
+  }
+  if (rows_contiguous) {
+    GemmDesc g;
+    g.name = "attn_dWqkv";
+    g.M = a.d; g.N = a.nq + 2 * a.nkv; g.K = a.T; g.in_dtype = dt;
+    g.a = a.x.data; g.a_sm = a.x.sc; g.a_sk = a.x.sr;
+    g.n_segs = 3;
+    for (int i = 0; i < 3; ++i) {
+      g.n_cols[i] = i == 0 ? a.nq : a.nkv;
+      g.nb[i] = gr[i]->data; g.nb_sk[i] = gr[i]->sr; g.nb_sn[i] = gr[i]->sc;
+      g.nd[i] = dw[i]->data; g.nldd[i] = o_in[i];
+    }
+    g.b = g.nb[0]; g.b_sk = g.nb_sk[0]; g.b_sn = g.nb_sn[0];
+    g.epi.d_dtype = TPS_F32;
+    return run_gemm(g, 0, 1, s);
+  }
   static const char* names[3] = {"attn_dWq", "attn_dWk", "attn_dWv"};
-  for (int i = 0; i < 3; ++i) {  // dW(dd, j) = sum_t X[t, dd] dProj[t, j]: shard-local columns
-    int64_t o_in, o_out;
-    weight_strides(*dw[i], weight_layout, &o_in, &o_out);
+  for (int i = 0; i < 3; ++i) {
     GemmDesc g;
     g.name = names[i];
     g.M = a.d; g.N = i == 0 ? a.nq : a.nkv; g.K = a.T; g.in_dtype = dt;
     g.a = a.x.data; g.a_sm = a.x.sc; g.a_sk = a.x.sr;
     g.b = gr[i]->data; g.b_sk = gr[i]->sr; g.b_sn = gr[i]->sc;
     g.epi.d = dw[i]->data; g.epi.d_dtype = TPS_F32;
-    if ((rc = run_gemm(g, o_in, o_out, s))) return rc;
+    if ((rc = run_gemm(g, o_in[i], o_out[i], s))) return rc;
   }
   return TPS_OK;
 }

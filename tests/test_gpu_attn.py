@@ -46,11 +46,16 @@ def test_fp32_kv_split_and_replicated(orc, tp):
 
 @pytest.mark.parametrize("layout", ["in_out", "out_in"])
 def test_bf16_fused_qkv(orc, layout):
-    """Head boundaries on 128-column blocks: Q, K and V in one launch."""
+    """Head boundaries on 128-column blocks: Q, K and V in one launch, and
+    with (in, out) gradients dWq, dWk, dWv in one launch too."""
     c = inputs.attn_case(3, 300, 256, 8, 2, 64, torch.bfloat16, w_std=0.05, layout=layout)
     with api.profile() as p:
         check(orc, c, 8, 2, 4, layout, True, f"bf16 {layout}")
     assert p.summary["gemm_tc:attn_qkv"]["launches"] == 1, p.summary
+    if layout == "in_out":
+        assert p.summary["gemm_tc:attn_dWqkv"]["launches"] == 1, p.summary
+    else:
+        assert all(f"gemm_tc:attn_dW{x}" in p.summary for x in "qkv"), p.summary
     assert {k.split(":")[0] for k in p.summary} == {"gemm_tc"}, p.summary
 
 
@@ -61,6 +66,7 @@ def test_bf16_unaligned_heads(orc):
     with api.profile() as p:
         check(orc, c, 4, 2, 2, "in_out", True, "dh40")
     assert "gemm_tc:attn_qkv" in p.summary and p.summary["gemm_tc:attn_qkv"]["launches"] == 3, p.summary
+    assert p.summary["gemm_tc:attn_dWqkv"]["launches"] == 3, p.summary
 
 
 def test_head_rules_enforced():
