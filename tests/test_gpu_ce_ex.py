@@ -162,3 +162,38 @@ def test_int32_labels_match_int64(gemm_kernel):
     b = run(h, W, y.to(torch.int32), 4, 4000, "mean", 0.0)
     for x, z in zip(a, b):
         assert torch.equal(x, z)
+
+
+def test_llama_shape_sampled(orc):
+    """Llama-3-8B vocabulary head (T=8192, d=4096, V=128256 whose last 256
+    columns are padding, tp=8), every eighth label ignored, the mean over
+    the batch's supervised tokens and the head's gradient, at full size in
+    the benchmark's launch configuration.  Eight tokens spread over the
+    batch (two of them ignored) are recomputed by the oracle with the
+    batch's supervised count as the divisor: loss, dlogits row, dHidden row
+    and owner.  The padding columns of dlogits are zero, four columns of
+    dWhead match h^T dlogits in float64, and the reduced loss is the mean of
+    the per-token losses."""
+    cfg = inputs.LLAMA_CE
+    T, V, tp = cfg["T"], cfg["V"], cfg["tp"]
+    vr = V - 256
+    h, W, y = inputs.ce_case(0, T, cfg["d"], V, torch.bfloat16)
+    y = y % vr
+    y[::8] = IGN
+    loss, red, dlog, dh, dw, own = api.vocab_ce_fwd_bwd_ex(h.cuda(), W.cuda(), y.cuda(), tp, ignore_index=IGN,
+                                                           vocab_size=vr, reduction="mean", want_dwhead=True)
+    assert api.last_device_error() == 0
+    D = int((y != IGN).sum())
+    toks = np.array([0, 1, 1000, 2047, 4097, 5555, 8000, 8191])
+    rl, _, rdl, rdh, _, rown = orc.ce_ex(inputs.as_f64(h[toks]), inputs.as_f64(W), y[toks].numpy(), tp, IGN, vr, 2,
+                                         float(D), want_dwhead=False)
+    assert_close(loss[toks].cpu(), rl, True, "loss")
+    assert_close(dlog[toks].cpu(), rdl, True, "dlogits")
+    assert_close(dh[toks].cpu(), rdh, True, "dHidden")
+    assert np.array_equal(own[toks].cpu().numpy(), rown)
+    assert not dlog[:, vr:].any()
+    cols = [0, 12345, 64000, vr - 1]
+    ref = inputs.as_f64(h).T @ dlog[:, cols].cpu().double().numpy()
+    assert_close(dw[:, cols].cpu(), ref, True, "dWhead columns")
+    l = loss.cpu().double()
+    assert abs(red.item() - l.sum().item() / D) <= 1e-4 * abs(red.item())
