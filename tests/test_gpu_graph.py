@@ -3,7 +3,8 @@
 Every entry point launches only on the caller's stream and does its
 one-time set-up (function attributes, occupancy, driver entry points, the
 device error word) on first use, so after one eager call a step can be
-captured with torch.cuda.graph and replayed.  Replays must reproduce the
+captured with torch.cuda.graph and replayed (the extended CE's memset of
+its supervised count included).  Replays must reproduce the
 eager results bit for bit (the kernels are deterministic), also after new
 values are copied into the captured input buffers."""
 import pytest
@@ -19,7 +20,11 @@ def make(seed):
     Xg, Wg, Wu, W2g, GYg = inputs.glu_case(seed + 1, 512, 256, 768, torch.bfloat16, w_std=0.05)
     h, W, labels = inputs.ce_case(seed + 2, 256, 256, 8192, torch.bfloat16, w_std=0.05)
     a = inputs.attn_case(seed + 3, 256, 256, 8, 2, 64, torch.bfloat16, w_std=0.05)
-    d = dict(X=X, W1=W1, W2=W2, GY=GY, Xg=Xg, Wg=Wg, Wu=Wu, W2g=W2g, GYg=GYg, h=h, W=W, labels=labels)
+    A, B, G = inputs.matmul_case(seed + 4, 384, 320, 512, torch.bfloat16)
+    y = labels % 8000
+    y[::5] = -100
+    d = dict(X=X, W1=W1, W2=W2, GY=GY, Xg=Xg, Wg=Wg, Wu=Wu, W2g=W2g, GYg=GYg, h=h, W=W, labels=labels,
+             m_A=A, m_B=B, m_G=G, y_ex=y)
     d.update({"a_" + k: v for k, v in a.items()})
     return {k: v.cuda() for k, v in d.items()}
 
@@ -32,6 +37,10 @@ def step(d):
     outs += list(api.attn_qkv_bwd(d["a_X"], d["a_Wq"], d["a_Wk"], d["a_Wv"], d["a_dQ"], d["a_dK"], d["a_dV"], 8, 2,
                                   4))
     outs += list(api.attn_out_fwd_bwd(d["a_C"], d["a_Wo"], d["a_GY"], 8, 4))
+    outs += list(api.matmul_fwd_bwd(d["m_A"], d["m_B"], d["m_G"], 3, "inner"))
+    # the extended CE adds a memset of the supervised count and the finalize kernel
+    outs += list(api.vocab_ce_fwd_bwd_ex(d["h"], d["W"], d["y_ex"], 8, ignore_index=-100, vocab_size=8000,
+                                         reduction="mean", want_dwhead=True))
     return outs
 
 

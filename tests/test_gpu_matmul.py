@@ -50,7 +50,10 @@ def test_sweep_1000_cases_three_axes(orc):
                 assert_close(g, r, False, f"seed {seed} {axis} {name}")
 
 
-TC_SHAPES = [(128, 64, 256), (300, 200, 520), (1, 64, 8), (257, 1000, 136), (520, 72, 264), (1024, 512, 768)]
+# (4808, 384, 712): 19 pair rows walked in raster groups of 16 and a ragged 3,
+# with a ragged last column tile
+TC_SHAPES = [(128, 64, 256), (300, 200, 520), (1, 64, 8), (257, 1000, 136), (520, 72, 264), (1024, 512, 768),
+             (4808, 384, 712)]
 
 
 @pytest.mark.parametrize("M,K,N", TC_SHAPES)
