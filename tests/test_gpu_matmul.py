@@ -65,6 +65,18 @@ def test_bf16_tensor_core(orc, M, K, N, gemm_kernel):
     assert kinds == {"gemm_tc"}, p.summary     # all three GEMMs on the tensor cores
 
 
+@pytest.mark.parametrize("axis", ["rows", "columns"])
+@pytest.mark.parametrize("parts", [3, 8])
+def test_bf16_tensor_core_row_and_column_splits(orc, axis, parts, gemm_kernel):
+    """Row and column splits on the tensor cores: one operand's gradient is
+    the rank sum, accumulated in the contraction loop, the other is the
+    concatenation of the shards' results."""
+    A, B, G = inputs.matmul_case(parts * 11 + len(axis), 600, 320, 776, torch.bfloat16)
+    with api.profile() as p:
+        check(orc, A, B, G, parts, axis, bf16=True, what=f"600x320x776 p{parts}")
+    assert {k.split(":")[0] for k in p.summary} == {"gemm_tc"}, p.summary
+
+
 def test_bf16_unaligned_strides_use_simt(orc):
     A, B, G = inputs.matmul_case(5, 37, 13, 29, torch.bfloat16)
     with api.profile() as p:
@@ -117,3 +129,20 @@ def test_sharded_outputs_are_ranges_of_one_buffer(orc):
         g = inputs.as_f64(G)[off[r]:off[r + 1]]
         assert_close(Y[off[r]:off[r + 1]], a @ inputs.as_f64(B), False, f"rank {r} Y")
         assert_close(dA[off[r]:off[r + 1]], g @ inputs.as_f64(B).T, False, f"rank {r} dA")
+
+
+@pytest.mark.parametrize("env", [{"TPS_GEMM_L2_HINTS": "21"}, {"TPS_GEMM_L2_HINTS": "12"},
+                                 {"TPS_GEMM_L2_HINTS": "1"}, {"TPS_GEMM_GROUP": "4"}, {"TPS_GEMM_GROUP": "64"}],
+                         ids=["hints21", "hints12", "hints1", "group4", "group64"])
+def test_tuning_switches_keep_results_bit_identical(env, gemm_kernel, monkeypatch):
+    """L2 eviction hints on the operand loads and the raster group size
+    change which pair computes a tile and how its operands are cached, not
+    the arithmetic: every output is bit-identical to the default launch."""
+    A, B, G = (t.cuda() for t in inputs.matmul_case(5, 2600, 448, 1000, torch.bfloat16))
+    base = api.matmul_fwd_bwd(A, B, G, 4, "inner")
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    tuned = api.matmul_fwd_bwd(A, B, G, 4, "inner")
+    assert api.last_device_error() == 0
+    for x, y in zip(base, tuned):
+        assert torch.equal(x, y)
