@@ -80,6 +80,8 @@ def library():
                                             sz, vp]
     lib.tps_ce_workspace_bytes.argtypes = [i64, i64, i32]
     lib.tps_ce_workspace_bytes.restype = sz
+    lib.tps_ce_workspace_bytes_ex.argtypes = [i64, i64, i32, i32]
+    lib.tps_ce_workspace_bytes_ex.restype = sz
     lib.tps_last_device_error.argtypes = [vp]
     lib.tps_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.tps_strerror.argtypes = [ctypes.c_int]
@@ -231,8 +233,31 @@ def mlp_fwd_bwd_noalloc(X: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, GY:
     return tuple(out)
 
 
-def ce_workspace_bytes(T: int, V: int, tp: int) -> int:
-    return int(library().tps_ce_workspace_bytes(T, V, tp))
+def ce_workspace_bytes(T: int, V: int, tp: int, dtype: Optional[torch.dtype] = None) -> int:
+    """Workspace bytes of the CE entry points: enough for every path when
+    `dtype` is None, else for operands of `dtype` on the tensor-core path
+    (bf16 logits)."""
+    if dtype is None:
+        return int(library().tps_ce_workspace_bytes(T, V, tp))
+    return int(library().tps_ce_workspace_bytes_ex(T, V, tp, _DTYPES[dtype]))
+
+
+def _ce_call(fn, T, V, tp, dtype, workspace, device):
+    """Run fn(workspace) with the given workspace, or with one sized for
+    the tensor-core path; operands that take the fp32 path instead are
+    refused before any launch (TPS_ERR_WORKSPACE) and run again with the
+    full size."""
+    if workspace is not None:
+        _check(fn(workspace))
+        return
+    small = ce_workspace_bytes(T, V, tp, dtype)
+    ws = torch.empty(max(small, 1), dtype=torch.uint8, device=device)
+    rc = fn(ws)
+    full = ce_workspace_bytes(T, V, tp)
+    if rc == ERR_WORKSPACE and full > small:
+        del ws
+        rc = fn(torch.empty(max(full, 1), dtype=torch.uint8, device=device))
+    _check(rc)
 
 
 def glu_mlp_workspace_bytes(T: int, d: int, F: int, tp: int, dtype: torch.dtype) -> int:
@@ -347,13 +372,11 @@ def vocab_ce_fwd_bwd(h: torch.Tensor, Whead: torch.Tensor, labels: torch.Tensor,
                torch.empty(h.shape, device=h.device, dtype=torch.float32),
                torch.empty(T, device=h.device, dtype=torch.int32))
     loss, dlog, dh, owner = out
-    need = ce_workspace_bytes(T, V, tp)
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
     args = [_tt(t) for t in (h, Whead, labels, loss, dlog, dh, owner)]
-    _check(library().tps_vocab_ce_fwd_bwd(_ref(args[0]), _ref(args[1]), _ref(args[2]), tp, LAYOUTS[weight_layout],
-                                          *[_ref(a) for a in args[3:]], ctypes.c_void_p(workspace.data_ptr()),
-                                          workspace.numel() * workspace.element_size(), _stream(h.device)))
+    _ce_call(lambda ws: library().tps_vocab_ce_fwd_bwd(
+        _ref(args[0]), _ref(args[1]), _ref(args[2]), tp, LAYOUTS[weight_layout], *[_ref(a) for a in args[3:]],
+        ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(), _stream(h.device)),
+        T, V, tp, h.dtype, workspace, h.device)
     return loss, dlog, dh, owner
 
 
@@ -380,18 +403,15 @@ def vocab_ce_fwd_bwd_ex(h: torch.Tensor, Whead: torch.Tensor, labels: torch.Tens
     dh = torch.empty(h.shape, device=dev, dtype=torch.float32)
     dw = torch.empty(Whead.shape, device=dev, dtype=torch.float32) if want_dwhead else None
     owner = torch.empty(T, device=dev, dtype=torch.int32)
-    if workspace is None:
-        workspace = torch.empty(max(ce_workspace_bytes(T, V, tp), 1), dtype=torch.uint8, device=dev)
     opts = TpsCeOptions(NO_IGNORE if ignore_index is None else int(ignore_index), int(vocab_size),
                         REDUCTIONS[reduction], 0, float(denominator))
     red_t = _tt(red.reshape(1)) if red is not None else None
     head = [_tt(t) for t in (h, Whead, labels, loss)]
     tail = [_tt(t) for t in (dlog, dh, dw, owner)]
-    _check(library().tps_vocab_ce_fwd_bwd_ex(_ref(head[0]), _ref(head[1]), _ref(head[2]), tp,
-                                             LAYOUTS[weight_layout], ctypes.byref(opts), _ref(head[3]),
-                                             _ref(red_t), *[_ref(a) for a in tail],
-                                             ctypes.c_void_p(workspace.data_ptr()),
-                                             workspace.numel() * workspace.element_size(), _stream(dev)))
+    _ce_call(lambda ws: library().tps_vocab_ce_fwd_bwd_ex(
+        _ref(head[0]), _ref(head[1]), _ref(head[2]), tp, LAYOUTS[weight_layout], ctypes.byref(opts), _ref(head[3]),
+        _ref(red_t), *[_ref(a) for a in tail], ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+        _stream(dev)), T, V, tp, h.dtype, workspace, dev)
     return loss, red, dlog, dh, dw, owner
 
 

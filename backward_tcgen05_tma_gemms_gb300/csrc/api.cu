@@ -899,19 +899,20 @@ extern "C" int tps_attn_out_fwd_bwd(const tps_tensor* C, const tps_tensor* Wo, c
   return TPS_OK;
 }
 
-// CE workspace: logits (T x V fp32) | per-shard stats of the two-pass path
-// (T x tp x 2) | label logits (T) | per-tile stats (T x ceil(V/128) x 4) |
-// combined (m, 1/s) per token (T x 2) | 256 bytes of scalars (the count of
-// supervised labels, int32 at +0, and the gradient scale, f32 at +16).
+// CE workspace: logits (T x V, fp32, or bf16 on the tensor-core path) |
+// per-shard stats of the two-pass path (T x tp x 2) | label logits (T) |
+// per-tile stats (T x ceil(V/128) x 4) | combined (m, 1/s) per token (T x 2)
+// | 256 bytes of scalars (the count of supervised labels, int32 at +0, and
+// the gradient scale, f32 at +16).
 struct CeWs {
   size_t z, stats, zy, tiles, shift, ms, scal, total;
 };
-static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp) {
+static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp, size_t logit_bytes) {
   const size_t t = static_cast<size_t>(T);
   const size_t n_tiles = static_cast<size_t>((V + kStatsTileN - 1) / kStatsTileN);
   CeWs w;
   w.z = 0;
-  w.stats = w.z + align256(t * static_cast<size_t>(V) * 4);
+  w.stats = w.z + align256(t * static_cast<size_t>(V) * logit_bytes);
   w.zy = w.stats + align256(t * static_cast<size_t>(tp) * 2 * 4);
   w.tiles = w.zy + align256(t * 4);
   w.shift = w.tiles + align256(t * n_tiles * 4 * 4);
@@ -923,7 +924,13 @@ static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp) {
 
 extern "C" size_t tps_ce_workspace_bytes(int64_t T, int64_t V, int32_t tp) {
   if (T < 0 || V < 0 || tp < 1) return 0;
-  return ce_ws_layout(T, V, tp).total;
+  return ce_ws_layout(T, V, tp, 4).total;
+}
+
+extern "C" size_t tps_ce_workspace_bytes_ex(int64_t T, int64_t V, int32_t tp, int32_t dtype) {
+  if (T < 0 || V < 0 || tp < 1) return 0;
+  const bool bf16_logits = dtype == TPS_BF16 && ce_tile_stats_supported(V, tp);
+  return ce_ws_layout(T, V, tp, bf16_logits ? 2 : 4).total;
 }
 
 // Both CE entry points: `opts` NULL is the plain form (every label in
@@ -1001,37 +1008,8 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
     if (dw.dtype != TPS_F32) return fail(TPS_ERR_DTYPE, "dWhead must be f32");
     weight_strides(dw, weight_layout, &dw_in, &dw_out);
   }
-  const size_t need = tps_ce_workspace_bytes(T, V, tp);
-  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
-    return fail(TPS_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
-  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  if (T == 0) {  // no tokens: a zero sum and a zero head gradient
-    if (red != nullptr && opts != nullptr && opts->reduction != TPS_REDUCE_NONE &&
-        cudaMemsetAsync(red, 0, sizeof(float), s) != cudaSuccess)
-      return fail(TPS_ERR_CUDA, "memset failed");
-    if (want_dw) {
-      GemmDesc g;
-      g.name = "ce_dwhead";
-      g.M = d; g.N = V; g.K = 0; g.in_dtype = dt;
-      g.epi.d = dw.data; g.epi.d_dtype = TPS_F32;
-      return run_gemm(g, dw_in, dw_out, s);
-    }
-    return TPS_OK;
-  }
-
-  char* ws = static_cast<char*>(workspace);
-  const CeWs lay = ce_ws_layout(T, V, tp);
-  float* z = reinterpret_cast<float*>(ws + lay.z);
-  float* stats = reinterpret_cast<float*>(ws + lay.stats);
-  float* zy = reinterpret_cast<float*>(ws + lay.zy);
-  float* tile_stats = reinterpret_cast<float*>(ws + lay.tiles);
-  float* shift = reinterpret_cast<float*>(ws + lay.shift);
-  float* ms = reinterpret_cast<float*>(ws + lay.ms);
-  char* scal = ws + lay.scal;
-  const int64_t n_tiles = (V + kStatsTileN - 1) / kStatsTileN;
   int64_t w_in, w_out;
   weight_strides(w, weight_layout, &w_in, &w_out);  // W(dd, v)
-
   // z = h Whead: vocabulary shards are column ranges of z.  On the tensor
   // cores (shards of at least one 128-column statistics tile) the epilogue
   // also leaves each shard's partial softmax statistics per tile, and stores
@@ -1042,8 +1020,37 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
   g.M = T; g.N = V; g.K = d; g.in_dtype = dt;
   g.a = hm.data; g.a_sm = hm.sr; g.a_sk = hm.sc;
   g.b = w.data; g.b_sk = w_in; g.b_sn = w_out;
-  g.epi.d = z; g.epi.d_dtype = TPS_F32; g.epi.ldd = V;
+  g.epi.d_dtype = TPS_F32; g.epi.ldd = V;
   const bool fused = gemm_tc_supported(g) && ce_tile_stats_supported(V, tp);
+  const CeWs lay = ce_ws_layout(T, V, tp, fused ? 2 : 4);
+  if (workspace == nullptr || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return fail(TPS_ERR_WORKSPACE, "workspace needs %zu bytes (%s logits), 256-byte aligned", lay.total,
+                fused ? "bf16" : "fp32");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  if (T == 0) {  // no tokens: a zero sum and a zero head gradient
+    if (red != nullptr && opts != nullptr && opts->reduction != TPS_REDUCE_NONE &&
+        cudaMemsetAsync(red, 0, sizeof(float), s) != cudaSuccess)
+      return fail(TPS_ERR_CUDA, "memset failed");
+    if (want_dw) {
+      GemmDesc gw;
+      gw.name = "ce_dwhead";
+      gw.M = d; gw.N = V; gw.K = 0; gw.in_dtype = dt;
+      gw.epi.d = dw.data; gw.epi.d_dtype = TPS_F32;
+      return run_gemm(gw, dw_in, dw_out, s);
+    }
+    return TPS_OK;
+  }
+
+  char* ws = static_cast<char*>(workspace);
+  float* z = reinterpret_cast<float*>(ws + lay.z);
+  float* stats = reinterpret_cast<float*>(ws + lay.stats);
+  float* zy = reinterpret_cast<float*>(ws + lay.zy);
+  float* tile_stats = reinterpret_cast<float*>(ws + lay.tiles);
+  float* shift = reinterpret_cast<float*>(ws + lay.shift);
+  float* ms = reinterpret_cast<float*>(ws + lay.ms);
+  char* scal = ws + lay.scal;
+  const int64_t n_tiles = (V + kStatsTileN - 1) / kStatsTileN;
+  g.epi.d = z;
   if (fused) {
     g.epi.mode = EPI_CE_STATS;
     g.epi.d_dtype = TPS_BF16;

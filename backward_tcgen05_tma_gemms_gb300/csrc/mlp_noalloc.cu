@@ -9,17 +9,18 @@
 // device synchronization.  This entry point takes its scratch from a
 // file-scope static device array instead, so it allocates nothing.
 //
-// The array is TPS_MLP_NOALLOC_SCRATCH_BYTES long and lives on every device
-// that loads the library until the process exits.  Every call on a device
-// shares it, and it keeps the previous call's contents; the MLP overwrites
-// each scratch byte before reading it, so nothing needs clearing.  Calls
-// whose execution overlaps on the GPU (other streams, other host threads)
-// race on the array and must be serialised by the caller.
+// The array is TPS_MLP_NOALLOC_SCRATCH_BYTES long.  The driver places it on
+// a device when the library's device code is loaded there: with lazy module
+// loading (the CUDA default) that happens in the first call on the device,
+// which can synchronize; from then on the device holds the array until the
+// process exits.  Every call on a device shares it, and it keeps the
+// previous call's contents; the MLP overwrites each scratch byte before
+// reading it, so nothing needs clearing.  Calls whose execution overlaps on
+// the GPU (other streams, other host threads) race on the array and must be
+// serialised by the caller.
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
-#include <vector>
 
 #include "internal.cuh"
 #include "tps.h"
@@ -28,24 +29,15 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_mlp_noalloc_scratch[TPS_MLP_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_mu;
-std::vector<void*> g_scratch_addr;  // per device ordinal
-
 // In host code the array's name is only a host-side stand-in; the device
-// address comes from cudaGetSymbolAddress, once per device, with that
-// device current.
+// address comes from cudaGetSymbolAddress with the device current.  It is
+// looked up on every call (a table lookup once the module is loaded), so an
+// address never outlives the context it belongs to.
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TPS_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (static_cast<int>(g_scratch_addr.size()) <= dev) g_scratch_addr.resize(dev + 1, nullptr);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_mlp_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) return TPS_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_mlp_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) return TPS_ERR_CUDA;
+  *out = p;
   return TPS_OK;
 }
 

@@ -168,14 +168,17 @@ size_t tps_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int3
  * that must not call cudaMalloc (which synchronizes the device).  This entry
  * point takes the same arguments minus the workspace and allocates nothing
  * (no cudaMalloc, no cudaFree, no allocating library call): its scratch is
- * a static device array of TPS_MLP_NOALLOC_SCRATCH_BYTES (32 MiB), which
- * every device that loads the library holds until the process exits.
+ * a static device array of TPS_MLP_NOALLOC_SCRATCH_BYTES (32 MiB).
  *   - Sizes whose scratch (tps_mlp_workspace_bytes) exceeds the array are
  *     rejected with TPS_ERR_WORKSPACE before anything is launched; for bf16
  *     operands that is T x F > 4,194,304.
- *   - The first call on a device resolves the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first
- *     call before any stream capture.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress,
+ *     with the call's device current).  Under lazy module loading (the CUDA
+ *     default) the first call on a device is also when the driver loads the
+ *     library's device code there and reserves the 32 MiB, which can
+ *     synchronize the device; the device then holds the array until the
+ *     process exits.  Make that first call, or a warm-up call, before any
+ *     stream capture and before latency-critical work.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (every byte is written before it is read, so nothing needs
  *     clearing).  Calls that overlap on the GPU race on the array: the
@@ -284,7 +287,11 @@ int tps_attn_out_fwd_bwd(const tps_tensor* C, const tps_tensor* Wo, const tps_te
  * (TPS_W_OUT_IN), same dtype.  labels (T): TPS_I64 or TPS_I32 in [0, V).
  * loss (T) fp32.  dlogits (T x V): the operand dtype (bf16 for bf16 runs).
  * dHidden (..., d) fp32.  owner (T) TPS_I32 or NULL: the rank whose shard
- * holds the label.  `workspace` >= tps_ce_workspace_bytes, 256-B aligned.
+ * holds the label.  `workspace`: 256-B aligned, at least
+ * tps_ce_workspace_bytes (enough for every path), or
+ * tps_ce_workspace_bytes_ex for the operand dtype when the call takes the
+ * tensor-core path; a smaller workspace fails with TPS_ERR_WORKSPACE before
+ * anything is launched.
  * A label outside [0, V) makes that token's loss NaN and its owner -1, and
  * sets TPS_ERR_LABEL in the device error word.
  * ---------------------------------------------------------------------- */
@@ -294,8 +301,18 @@ int tps_vocab_ce_fwd_bwd(const tps_tensor* h, const tps_tensor* Whead, const tps
                          size_t workspace_bytes, void* cuda_stream);
 
 /* Workspace bytes tps_vocab_ce_fwd_bwd and tps_vocab_ce_fwd_bwd_ex need for
- * T tokens, vocabulary V and `tp` shards. */
+ * T tokens, vocabulary V and `tp` shards on any path (fp32 logits). */
 size_t tps_ce_workspace_bytes(int64_t T, int64_t V, int32_t tp);
+
+/* Workspace bytes for operands of `dtype` (TPS_F32 or TPS_BF16).  With bf16
+ * operands and shards of at least 128 columns (V / tp >= 128) the logits
+ * are kept as bf16, which halves their T x V region (4.2 GB -> 2.1 GB at
+ * T = 8192, V = 128256).  That size assumes the tensor-core path: h and
+ * Whead 16-byte aligned, unit stride along their rows and row pitches that
+ * are multiples of 16 bytes.  Operands that do not qualify run the fp32
+ * path and need tps_ce_workspace_bytes.  Returns 0 for T < 0, V < 0 or
+ * tp < 1. */
+size_t tps_ce_workspace_bytes_ex(int64_t T, int64_t V, int32_t tp, int32_t dtype);
 
 /* ------------------------------------------------------------------------
  * tps_vocab_ce_fwd_bwd_ex -- tps_vocab_ce_fwd_bwd with the extensions a

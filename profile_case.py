@@ -2,11 +2,11 @@
 profilers (ncu) and quick timing.  Prints per-launch device times from the
 library's own launch profiler.
 
-    python -m backward_tcgen05_tma_gemms_gb300.profile_case mlp --T 2048 --reps 2
-    python -m backward_tcgen05_tma_gemms_gb300.profile_case glu --T 2048 --reps 1
-    python -m backward_tcgen05_tma_gemms_gb300.profile_case ce --T 1024 --reps 2
-    python -m backward_tcgen05_tma_gemms_gb300.profile_case matmul --M 4096 --K 4096 --N 4096
-    python -m backward_tcgen05_tma_gemms_gb300.profile_case sustained --N 8192 --seconds 3
+    python profile_case.py mlp --T 2048 --reps 2
+    python profile_case.py glu --T 2048 --reps 1
+    python profile_case.py ce --T 1024 --reps 2
+    python profile_case.py matmul --M 4096 --K 4096 --N 4096
+    python profile_case.py sustained --N 8192 --seconds 3
 
 `sustained` runs the library's bf16 GEMM Y = A B (N x N x N, fp32 Y, CTA
 pairs and one-CTA tiles) and torch.matmul (cuBLAS, bf16 out) back to back,
@@ -21,12 +21,14 @@ import json
 import os
 import statistics
 import subprocess
+import sys
 import threading
 import time
 
 import torch
 
-from . import api, inputs
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from backward_tcgen05_tma_gemms_gb300 import api, inputs  # noqa: E402
 
 
 def main():

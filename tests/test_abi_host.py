@@ -30,7 +30,8 @@ def declared_symbols():
 def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ["tps_plan_shards", "tps_matmul_fwd_bwd", "tps_mlp_fwd_bwd", "tps_vocab_ce_fwd_bwd",
-              "tps_mlp_workspace_bytes", "tps_ce_workspace_bytes", "tps_last_device_error", "tps_strerror"]:
+              "tps_mlp_workspace_bytes", "tps_ce_workspace_bytes", "tps_ce_workspace_bytes_ex", "tps_last_device_error",
+              "tps_strerror"]:
         assert s in syms
 
 
@@ -111,6 +112,21 @@ def test_mlp_and_ce_validation_codes(lib):
 def test_workspace_queries(lib):
     assert lib.tps_mlp_workspace_bytes(8192, 4096, 14336, 8, 1) >= 8192 * 14336 * 8
     assert lib.tps_ce_workspace_bytes(8192, 128256, 8) >= 8192 * 128256 * 4
+
+
+def test_ce_workspace_query_by_dtype(lib):
+    """bf16 operands with shards of >= 128 columns keep the logits as bf16:
+    the query drops half of the T x V fp32 region; every other case asks
+    for the full size."""
+    T, V, tp = 8192, 128256, 8
+    full = lib.tps_ce_workspace_bytes(T, V, tp)
+    bf16 = lib.tps_ce_workspace_bytes_ex(T, V, tp, 1)
+    assert full - bf16 == T * V * 2
+    assert 0.45 < bf16 / full < 0.55
+    assert lib.tps_ce_workspace_bytes_ex(T, V, tp, 0) == full            # fp32 operands
+    assert lib.tps_ce_workspace_bytes_ex(64, 1000, 8, 1) == lib.tps_ce_workspace_bytes(64, 1000, 8)  # 125-col shards
+    assert lib.tps_ce_workspace_bytes_ex(64, 1024, 8, 1) < lib.tps_ce_workspace_bytes(64, 1024, 8)   # 128-col shards
+    assert lib.tps_ce_workspace_bytes_ex(-1, V, tp, 1) == 0 and lib.tps_ce_workspace_bytes_ex(T, V, 0, 1) == 0
 
 
 def test_python_wrapper_rejects_like_the_page():
