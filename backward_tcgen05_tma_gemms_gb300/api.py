@@ -383,13 +383,14 @@ def vocab_ce_fwd_bwd(h: torch.Tensor, Whead: torch.Tensor, labels: torch.Tensor,
 def vocab_ce_fwd_bwd_ex(h: torch.Tensor, Whead: torch.Tensor, labels: torch.Tensor, tp: int,
                         weight_layout: str = "in_out", ignore_index: Optional[int] = None, vocab_size: int = 0,
                         reduction: str = "none", denominator: float = 0.0, want_dwhead: bool = False,
-                        workspace: Optional[torch.Tensor] = None):
+                        workspace: Optional[torch.Tensor] = None, out: Optional[Sequence] = None):
     """Cross-entropy with vocabulary padding (the first `vocab_size` columns
     of the head are real, 0 = all), `ignore_index`, a "sum" or "mean"
     reduction (the mean divides by `denominator` when > 0, e.g. the
     job-wide count of supervised tokens, else by this call's count), and
     optionally the head's gradient.  Returns (loss [T], loss_reduced (0-d)
-    or None, dlogits, dHidden, dWhead or None, owner)."""
+    or None, dlogits, dHidden, dWhead or None, owner); `out` may supply
+    those six to write into (loss_reduced and dWhead may be None)."""
     _parts(tp, "tp")
     if weight_layout not in LAYOUTS or reduction not in REDUCTIONS:
         raise ValueError("argument")
@@ -397,12 +398,15 @@ def vocab_ce_fwd_bwd_ex(h: torch.Tensor, Whead: torch.Tensor, labels: torch.Tens
     T = h.numel() // d if d else 0
     V = Whead.shape[1] if weight_layout == "in_out" else Whead.shape[0]
     dev = h.device
-    loss = torch.empty(T, device=dev, dtype=torch.float32)
-    red = torch.zeros((), device=dev, dtype=torch.float32) if reduction != "none" else None
-    dlog = torch.empty(T, V, device=dev, dtype=h.dtype)
-    dh = torch.empty(h.shape, device=dev, dtype=torch.float32)
-    dw = torch.empty(Whead.shape, device=dev, dtype=torch.float32) if want_dwhead else None
-    owner = torch.empty(T, device=dev, dtype=torch.int32)
+    if out is not None:
+        loss, red, dlog, dh, dw, owner = out
+    else:
+        loss = torch.empty(T, device=dev, dtype=torch.float32)
+        red = torch.zeros((), device=dev, dtype=torch.float32) if reduction != "none" else None
+        dlog = torch.empty(T, V, device=dev, dtype=h.dtype)
+        dh = torch.empty(h.shape, device=dev, dtype=torch.float32)
+        dw = torch.empty(Whead.shape, device=dev, dtype=torch.float32) if want_dwhead else None
+        owner = torch.empty(T, device=dev, dtype=torch.int32)
     opts = TpsCeOptions(NO_IGNORE if ignore_index is None else int(ignore_index), int(vocab_size),
                         REDUCTIONS[reduction], 0, float(denominator))
     red_t = _tt(red.reshape(1)) if red is not None else None

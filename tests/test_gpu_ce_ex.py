@@ -168,29 +168,35 @@ def test_llama_shape_sampled(orc):
     """Llama-3-8B vocabulary head (T=8192, d=4096, V=128256 whose last 256
     columns are padding, tp=8), every eighth label ignored, the mean over
     the batch's supervised tokens and the head's gradient, at full size in
-    the benchmark's launch configuration.  Eight tokens spread over the
-    batch (two of them ignored) are recomputed by the oracle with the
-    batch's supervised count as the divisor: loss, dlogits row, dHidden row
-    and owner.  The padding columns of dlogits are zero, four columns of
-    dWhead match h^T dlogits in float64, and the reduced loss is the mean of
-    the per-token losses."""
+    the benchmark's launch configuration.  64 supervised tokens spread over
+    the batch get labels at both ends of every shard's real columns (each
+    rank owns eight; the first ones in tiles shared with the previous
+    shard), and with four ignored tokens they are recomputed by the oracle
+    with the batch's supervised count as the divisor: loss, dlogits row,
+    dHidden row and owner.  The padding columns of dlogits are zero, four
+    columns of dWhead match h^T dlogits in float64, and the reduced loss is
+    the mean of the per-token losses."""
+    from test_gpu_ce import boundary_labels, spread_tokens
     cfg = inputs.LLAMA_CE
     T, V, tp = cfg["T"], cfg["V"], cfg["tp"]
     vr = V - 256
     h, W, y = inputs.ce_case(0, T, cfg["d"], V, torch.bfloat16)
     y = y % vr
     y[::8] = IGN
+    sup = spread_tokens(T, 64, 6, avoid_mod=8)
+    y[torch.from_numpy(sup)] = torch.from_numpy(boundary_labels(V, tp, vr))
+    toks = np.sort(np.concatenate([sup, [0, 8, 4096, T - 8]]))
     loss, red, dlog, dh, dw, own = api.vocab_ce_fwd_bwd_ex(h.cuda(), W.cuda(), y.cuda(), tp, ignore_index=IGN,
                                                            vocab_size=vr, reduction="mean", want_dwhead=True)
     assert api.last_device_error() == 0
     D = int((y != IGN).sum())
-    toks = np.array([0, 1, 1000, 2047, 4097, 5555, 8000, 8191])
     rl, _, rdl, rdh, _, rown = orc.ce_ex(inputs.as_f64(h[toks]), inputs.as_f64(W), y[toks].numpy(), tp, IGN, vr, 2,
                                          float(D), want_dwhead=False)
     assert_close(loss[toks].cpu(), rl, True, "loss")
     assert_close(dlog[toks].cpu(), rdl, True, "dlogits")
     assert_close(dh[toks].cpu(), rdh, True, "dHidden")
     assert np.array_equal(own[toks].cpu().numpy(), rown)
+    assert np.bincount(rown[rown >= 0], minlength=tp).min() >= 4 and (rown == -1).sum() == 4
     assert not dlog[:, vr:].any()
     cols = [0, 12345, 64000, vr - 1]
     ref = inputs.as_f64(h).T @ dlog[:, cols].cpu().double().numpy()
