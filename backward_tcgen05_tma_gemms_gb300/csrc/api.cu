@@ -245,7 +245,7 @@ static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream)
     // for every supported activation, and every gated output is a product
     // with a zero factor.
     const int m = g.epi.mode;
-    const bool f32_d = (m == EPI_ACT_FWD || m == EPI_GLU_FWD || m == EPI_GLU_UP);
+    const bool f32_d = (m == EPI_GLU_FWD || m == EPI_GLU_UP);  // Hg, U; EPI_ACT_FWD's Hp is in d_dtype
     int rc = launch_fill(g.epi.d, f32_d ? TPS_F32 : g.epi.d_dtype, g.M, g.N, d_sm, d_sn, stream);
     if (rc == TPS_OK && (m == EPI_ACT_FWD || m == EPI_GLU_FWD || m == EPI_GLU_UP || m == EPI_GLU_BWD))
       rc = launch_fill(g.epi.d2, g.epi.d2_dtype, g.M, g.N, g.epi.ldd2, 1, stream);
@@ -361,13 +361,15 @@ extern "C" int tps_matmul_fwd_bwd(const tps_tensor* A, const tps_tensor* B, cons
   return TPS_OK;
 }
 
+// MLP workspace: the pre-activation, the activation and dZ, T x F each, all
+// in the operand dtype.
 extern "C" size_t tps_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int32_t dtype) {
   (void)d;
   (void)tp;
   if (T < 0 || F < 0) return 0;
   const size_t e = (dtype == TPS_F32) ? 4 : 2;
   const size_t n = static_cast<size_t>(T) * static_cast<size_t>(F);
-  return align256(n * 4) + align256(n * e) + align256(n * e);
+  return 3 * align256(n * e);
 }
 
 // A weight's logical (in, out) strides for either layout.
@@ -421,9 +423,13 @@ extern "C" int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const 
   const size_t n = static_cast<size_t>(T) * static_cast<size_t>(F);
   const size_t e = (dt == TPS_F32) ? 4 : 2;
   char* ws = static_cast<char*>(workspace);
-  float* Hp = reinterpret_cast<float*>(ws);                 // T x F fp32 pre-activation
-  void* Ha = ws + align256(n * 4);                          // T x F activation (operand dtype)
-  void* dZ = ws + align256(n * 4) + align256(n * e);        // T x F dZ (operand dtype)
+  // T x F pre-activation, activation and dZ, each in the operand dtype.  A
+  // bf16 pre-activation moves phi'(Hp) by at most phi''(x) x 2^-9 |x|,
+  // which raises the relative error of dZ (one bf16 rounding already) by
+  // about 5 % for GELU and SiLU, under 30 % for tanh.
+  void* Hp = ws;
+  void* Ha = ws + align256(n * e);
+  void* dZ = ws + 2 * align256(n * e);
 
   int64_t w1_in, w1_out, w2_in, w2_out, dw1_in, dw1_out, dw2_in, dw2_out;
   weight_strides(w1, weight_layout, &w1_in, &w1_out);      // W1(dd, f)
@@ -438,7 +444,7 @@ extern "C" int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const 
     g.a = x.data; g.a_sm = x.sr; g.a_sk = x.sc;
     g.b = w1.data; g.b_sk = w1_in; g.b_sn = w1_out;
     g.epi.mode = EPI_ACT_FWD; g.epi.act = act;
-    g.epi.d = Hp; g.epi.d_dtype = TPS_F32;
+    g.epi.d = Hp; g.epi.d_dtype = dt;
     g.epi.d2 = Ha; g.epi.ldd2 = F; g.epi.d2_dtype = dt;
     if ((rc = run_gemm(g, F, 1, s))) return rc;
   }
@@ -460,7 +466,11 @@ extern "C" int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const 
     g.b = w2.data; g.b_sk = w2_out; g.b_sn = w2_in;
     g.epi.mode = EPI_ACT_BWD; g.epi.act = act;
     g.epi.d = dZ; g.epi.d_dtype = dt;
-    g.epi.aux = Hp; g.epi.ld_aux = F;
+    g.epi.ld_aux = F;
+    if (dt == TPS_F32)
+      g.epi.aux = static_cast<const float*>(Hp);
+    else
+      g.epi.aux_bf16 = static_cast<const uint16_t*>(Hp);
     if ((rc = run_gemm(g, F, 1, s))) return rc;
   }
   {  // dW2(f, dd) = sum_t Ha[t, f] GY[t, dd]
@@ -901,12 +911,17 @@ extern "C" int tps_attn_out_fwd_bwd(const tps_tensor* C, const tps_tensor* Wo, c
 
 // CE workspace: logits (T x V, fp32, or bf16 on the tensor-core path) |
 // per-shard stats of the two-pass path (T x tp x 2) | label logits (T) |
-// per-tile stats (T x ceil(V/128) x 4) | combined (m, 1/s) per token (T x 2)
+// per-tile stats (T x ceil(V/128) x 4) | per-tile shifts (T rows of
+// ceil(V/128) floats, padded to a multiple of 4) | combined (m, 1/s) per
+// token (T x 2)
 // | 256 bytes of scalars (the count of supervised labels, int32 at +0, and
 // the gradient scale, f32 at +16).
 struct CeWs {
   size_t z, stats, zy, tiles, shift, ms, scal, total;
 };
+// Row stride of the per-tile shifts: 16-byte rows, so that a run of shifts
+// starting at a multiple of 4 tiles can be copied in bulk.
+static int64_t ce_shift_ld(int64_t V) { return ((V + kStatsTileN - 1) / kStatsTileN + 3) & ~int64_t(3); }
 static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp, size_t logit_bytes) {
   const size_t t = static_cast<size_t>(T);
   const size_t n_tiles = static_cast<size_t>((V + kStatsTileN - 1) / kStatsTileN);
@@ -916,7 +931,7 @@ static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp, size_t logit_bytes) {
   w.zy = w.stats + align256(t * static_cast<size_t>(tp) * 2 * 4);
   w.tiles = w.zy + align256(t * 4);
   w.shift = w.tiles + align256(t * n_tiles * 4 * 4);
-  w.ms = w.shift + align256(t * n_tiles * 4);
+  w.ms = w.shift + align256(t * ce_shift_ld(V) * 4);
   w.scal = w.ms + align256(t * 2 * 4);
   w.total = w.scal + 256;
   return w;
@@ -1059,6 +1074,7 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
     g.epi.ce_parts = tp;
     g.epi.ce_vreal = vreal;
     g.epi.ce_shift = shift;
+    g.epi.ce_shift_ld = ce_shift_ld(V);
     g.epi.ce_labels = labels->data;
     g.epi.ce_label_i64 = labels->dtype == TPS_I64 ? 1 : 0;
     g.epi.ce_zy = zy;
@@ -1071,6 +1087,7 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
     if (fused) {
       c.logits16 = z;
       c.shift = shift;
+      c.shift_ld = ce_shift_ld(V);
     }
     c.labels = labels->data; c.label_dtype = labels->dtype;
     c.loss = static_cast<float*>(loss->data);

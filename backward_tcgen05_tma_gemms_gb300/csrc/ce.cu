@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.cuh"
@@ -49,6 +50,7 @@ struct CeParams {
   // (T x n_tiles) and, in zy, the fp32 logit at each label
   const __nv_bfloat16* z16;
   const float* zshift;
+  int64_t shift_ld;  // row stride of zshift
   int64_t n_tiles;
   const void* labels;
   int label_is_i64;
@@ -876,7 +878,7 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
     const int64_t c0 = (it - t * per_row) * CEF_ITEM;
     const __nv_bfloat16* zrow = p.z16 + t * p.ldz;
     const unsigned short* zbits = reinterpret_cast<const unsigned short*>(zrow);
-    const float* crow = p.zshift + t * p.n_tiles;
+    const float* crow = p.zshift + t * p.shift_ld;
 #pragma unroll
     for (int k = 0; k < CEF_VEC; ++k) {
       const int64_t e = c0 + 8 * (threadIdx.x + k * CEF_THREADS);
@@ -950,6 +952,249 @@ __global__ void __launch_bounds__(CEF_THREADS) ce_grad_stream_kernel(const CePar
   }
 }
 
+// ------------------------------------------------------------ fused combine + stream
+// One persistent kernel for the whole CE core when the shifted bf16 logits
+// rows are 16-byte aligned.  Work items are (token, 8192-column chunk) in
+// row-major order, and block b takes the contiguous range
+// [b I / G, (b + 1) I / G) of the I items (G blocks), so it meets a short run
+// of consecutive rows.  Three roles:
+//   producer (one thread)   bulk-copies each item's 16 KB of logits and its
+//                           64 tile shifts into a ring of CFS_STAGES stages
+//   combiner (one warp)     for each row of the range, in order: the pages'
+//                           per-shard (m_r, s_r) from the tile statistics of
+//                           the logits GEMM, their combine into m and s, and,
+//                           in the block that holds the row's first item,
+//                           the loss and the owner; (m, scale / s) and the
+//                           one-hot column go to a ring of CFS_ROWS rows
+//   consumers (8 warps)     dlogits = e^{z - m} scale / s - scale 1[j = y]
+//                           from the staged logits, 16-byte streaming stores
+// The combiner runs up to CFS_ROWS rows ahead, so the statistics of the
+// next rows are read while the current ones stream, and the separate
+// combine launch (and its pass over the statistics) disappears.
+constexpr int CFS_CONSUMERS = 8;
+constexpr int CFS_THREADS = 32 * (CFS_CONSUMERS + 2);
+constexpr int64_t CFS_CHUNK = 8192;                                  // columns per item
+constexpr int CFS_SHIFTS = static_cast<int>(CFS_CHUNK / kStatsTileN);  // 64
+constexpr int CFS_STAGES = 4;
+constexpr int CFS_ROWS = 4;
+static_assert(CFS_CHUNK == 8 * 4 * 32 * CFS_CONSUMERS, "each consumer thread takes four 8-column vectors per item");
+
+struct CfsShared {
+  uint16_t z[CFS_STAGES][CFS_CHUNK];   // shifted bf16 logits of one item per stage
+  float c[CFS_STAGES][CFS_SHIFTS];     // the item's tile shifts
+  float2 row_ms[CFS_ROWS];             // (m log2 e, scale / s); ignored rows (+inf, 0)
+  long long row_y[CFS_ROWS];           // one-hot column (-1: none)
+  uint64_t full[CFS_STAGES], empty[CFS_STAGES], row_full[CFS_ROWS], row_empty[CFS_ROWS];
+  uint32_t abort;
+};
+
+template <typename TOut>
+__global__ void __launch_bounds__(CFS_THREADS) ce_fused_stream_kernel(const CeParams p, const float* ts) {
+  extern __shared__ __align__(128) uint8_t cfs_raw[];
+  CfsShared& sh = *reinterpret_cast<CfsShared*>(cfs_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t per_row = (p.V + CFS_CHUNK - 1) / CFS_CHUNK;
+  const int64_t items = p.T * per_row;
+  const int64_t it0 = items * blockIdx.x / gridDim.x, it1 = items * (blockIdx.x + 1) / gridDim.x;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < CFS_STAGES; ++i) {
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], CFS_CONSUMERS);
+    }
+    for (int i = 0; i < CFS_ROWS; ++i) {
+      mbar_init(&sh.row_full[i], 1);
+      mbar_init(&sh.row_empty[i], CFS_CONSUMERS);
+    }
+    sh.abort = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (it0 >= it1) return;
+  const float sc = grad_scale(p);
+
+  if (warp == CFS_CONSUMERS) {
+    // ---------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int64_t issued = 0;
+      for (int64_t it = it0; it < it1; ++it) {
+        if (!mbar_wait(&sh.empty[stage], phase ^ 1u, &sh.abort, p.err)) break;
+        const int64_t t = it / per_row, c0 = (it - t * per_row) * CFS_CHUNK;
+        const int64_t n = imin64(CFS_CHUNK, p.V - c0);          // a multiple of 8
+        const int64_t nt = ((n + kStatsTileN - 1) / kStatsTileN + 3) & ~int64_t(3);
+        const uint32_t zb = static_cast<uint32_t>(n * 2), cb = static_cast<uint32_t>(nt * 4);
+        mbar_expect_tx(&sh.full[stage], zb + cb);
+        bulk_load(sh.z[stage], p.z16 + t * p.ldz + c0, zb, &sh.full[stage]);
+        bulk_load(sh.c[stage], p.zshift + t * p.shift_ld + c0 / kStatsTileN, cb, &sh.full[stage]);
+        ++issued;
+        if (++stage == CFS_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // the copies still in flight land before the block may exit
+      const int64_t first = issued > CFS_STAGES ? issued - CFS_STAGES : 0;
+      for (int64_t i = first; i < issued; ++i)
+        mbar_wait_drain(&sh.full[i % CFS_STAGES], static_cast<uint32_t>((i / CFS_STAGES) & 1), p.err);
+    }
+  } else if (warp == CFS_CONSUMERS + 1) {
+    // ---------------------------------------------------- combiner
+    const int64_t t_first = it0 / per_row, t_last = (it1 - 1) / per_row;
+    uint32_t slot = 0, phase = 0;
+    for (int64_t t = t_first; t <= t_last; ++t) {
+      if (!mbar_wait(&sh.row_empty[slot], phase ^ 1u, &sh.abort, p.err)) break;
+      const float4* row = reinterpret_cast<const float4*>(ts) + t * p.n_tiles;
+      float m = -INFINITY, s = 0.0f;
+      for (int32_t r = 0; r < p.parts; ++r) {
+        const int64_t beg = shard_offset(p.V, p.parts, r), end = shard_offset(p.V, p.parts, r + 1);
+        const int64_t t0 = beg / kStatsTileN, t1 = (end - 1) / kStatsTileN;
+        const bool split0 = beg % kStatsTileN != 0;  // shard r starts inside tile t0: its second part
+        float mr = -INFINITY, sr = 0.0f;
+        for (int64_t tt = t0 + lane; tt <= t1; tt += 4 * 32) {
+          float4 e[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int64_t u = tt + 32 * k;
+            e[k] = u <= t1 ? __ldg(row + u) : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const bool second = (tt + 32 * k == t0) && split0;
+            ms_combine_acc(mr, sr, second ? e[k].z : e[k].x, second ? e[k].w : e[k].y);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+          ms_combine_acc(mr, sr, __shfl_xor_sync(0xffffffffu, mr, o), __shfl_xor_sync(0xffffffffu, sr, o));
+        ms_combine_acc(m, s, mr, sr);  // the pages' combine across shards
+      }
+      if (lane == 0) {
+        const int64_t y = load_label(p, t);
+        const int kind = label_kind(p, y);
+        sh.row_ms[slot] = kind == 1 ? make_float2(INFINITY, 0.0f) : make_float2(m * kLog2e, sc / s);
+        sh.row_y[slot] = kind == 1 ? -1 : y;
+        if (t * per_row >= it0) {  // this block holds the row's first item
+          if (kind == 1) {
+            p.loss[t] = 0.0f;
+            if (p.owner) p.owner[t] = -1;
+          } else if (kind == 0) {
+            p.loss[t] = logf(s) + m - p.zy[t];
+            if (p.owner) {
+              int32_t r = 0;
+              while (r + 1 < p.parts && shard_offset(p.V, p.parts, r + 1) <= y) ++r;
+              p.owner[t] = r;
+            }
+          } else {
+            p.loss[t] = __int_as_float(0x7fc00000);  // NaN
+            if (p.owner) p.owner[t] = -1;
+            atomicOr(p.err, TPS_DEVERR_LABEL);
+          }
+        }
+        mbar_arrive(&sh.row_full[slot]);
+      }
+      __syncwarp();
+      if (++slot == CFS_ROWS) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+  } else {
+    // ---------------------------------------------------- consumers
+    const bool vec = ((p.ldg & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.dlog) & 15u) == 0);
+    uint32_t stage = 0, phase = 0, slot = 0, rphase = 0;
+    int64_t cur = -1, y = -1;
+    float ml = 0.0f, inv = 0.0f;
+    for (int64_t it = it0; it < it1; ++it) {
+      const int64_t t = it / per_row, c0 = (it - t * per_row) * CFS_CHUNK;
+      if (t != cur) {
+        if (cur >= 0) {  // done with the previous row: free its slot
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.row_empty[slot]);
+          if (++slot == CFS_ROWS) {
+            slot = 0;
+            rphase ^= 1u;
+          }
+        }
+        if (!mbar_wait(&sh.row_full[slot], rphase, &sh.abort, p.err)) break;
+        const float2 r = sh.row_ms[slot];
+        ml = r.x;
+        inv = r.y;
+        y = sh.row_y[slot];
+        cur = t;
+      }
+      if (!mbar_wait(&sh.full[stage], phase, &sh.abort, p.err)) break;
+      const int64_t n = imin64(CFS_CHUNK, p.V - c0);
+      TOut* grow = static_cast<TOut*>(p.dlog) + t * p.ldg + c0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = 8 * (static_cast<int>(threadIdx.x) + k * 32 * CFS_CONSUMERS);
+        if (e >= n) continue;
+        const uint4 q = *reinterpret_cast<const uint4*>(&sh.z[stage][e]);
+        const float adj = fmaf(sh.c[stage][e / kStatsTileN], kLog2e, -ml);  // (c - m) log2(e)
+        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+        float g[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          g[2 * j] = ex2_approx(fmaf(bf16_lo(wd[j]), kLog2e, adj)) * inv;
+          g[2 * j + 1] = ex2_approx(fmaf(bf16_hi(wd[j]), kLog2e, adj)) * inv;
+        }
+        const int64_t col = c0 + e;
+        if (y >= col && y < col + 8) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) g[j] -= (y == col + j) ? sc : 0.0f;
+        }
+        if (col + 7 >= p.vreal) {  // vocabulary padding
+#pragma unroll
+          for (int j = 0; j < 8; ++j) g[j] = (col + j < p.vreal) ? g[j] : 0.0f;
+        }
+        if (vec) {
+          if constexpr (sizeof(TOut) == 2) {
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              __nv_bfloat162 b = __floats2bfloat162_rn(g[2 * j], g[2 * j + 1]);
+              o[j] = *reinterpret_cast<uint32_t*>(&b);
+            }
+            __stcs(reinterpret_cast<uint4*>(grow + e), make_uint4(o[0], o[1], o[2], o[3]));
+          } else {
+            __stcs(reinterpret_cast<float4*>(grow + e), make_float4(g[0], g[1], g[2], g[3]));
+            __stcs(reinterpret_cast<float4*>(grow + e + 4), make_float4(g[4], g[5], g[6], g[7]));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) store_grad(grow + e + j, g[j]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[stage]);
+      if (++stage == CFS_STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+}
+
+// Extended form, before the fused kernel: the number of supervised labels
+// and the gradient scale 1 / D (one block; D as in ce_finalize_kernel).
+__global__ void __launch_bounds__(1024) ce_count_scale_kernel(const CeParams p, int reduction, double denominator) {
+  __shared__ int red[32];
+  int n = 0;
+  for (int64_t t = threadIdx.x; t < p.T; t += blockDim.x) n += label_kind(p, load_label(p, t)) == 0 ? 1 : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = n;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int total = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += red[w];
+    *p.count = total;
+    double D = 1.0;
+    if (reduction == TPS_REDUCE_MEAN) D = denominator > 0.0 ? denominator : (total > 0 ? double(total) : 1.0);
+    if (p.scale != nullptr) *const_cast<float*>(p.scale) = static_cast<float>(1.0 / D);
+  }
+}
+
 bool ce_tile_stats_supported(int64_t V, int32_t parts) { return parts >= 1 && V / parts >= kStatsTileN; }
 
 static CeParams make_params(const CeDesc& c, uint32_t* dev_err) {
@@ -961,6 +1206,7 @@ static CeParams make_params(const CeDesc& c, uint32_t* dev_err) {
   p.ldz = c.ldz;
   p.z16 = static_cast<const __nv_bfloat16*>(c.logits16);
   p.zshift = c.shift;
+  p.shift_ld = c.shift_ld;
   p.n_tiles = 0;
   p.labels = c.labels;
   p.label_is_i64 = (c.label_dtype == TPS_I64);
@@ -1001,6 +1247,47 @@ int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t 
   const double bytes = double(c.T) * double(c.V) * (2.0 + gsize) + double(c.T) * double(n_tiles) * 4.0 +
                        double(c.T) * (8.0 + 4.0);
   ProfScope prof("ce_stream", "ce_core", 0.0, bytes, stream);
+  int dev = 0, sms = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // One fused kernel when every item's logits and shifts can be bulk-copied:
+  // 16-byte aligned logits rows and shift rows.
+  const bool one_kernel = (c.V % 8 == 0) && (c.ldz % 8 == 0) && (reinterpret_cast<uintptr_t>(c.logits16) & 15u) == 0 &&
+                          (c.shift_ld % 4 == 0) && (reinterpret_cast<uintptr_t>(c.shift) & 15u) == 0 &&
+                          getenv("TPS_CE_TWO_KERNELS") == nullptr;
+  if (one_kernel) {
+    if (c.options) {  // the divisor of a mean needs every label: count them first
+      ce_count_scale_kernel<<<1, 1024, 0, stream>>>(p, c.reduction, c.denominator);
+      note_launch();
+      if (cudaPeekAtLastError() != cudaSuccess) return TPS_ERR_CUDA;
+    }
+    static int occ_f = 0, occ_b = 0;
+    static cudaError_t attr_err = cudaSuccess;
+    static std::once_flag once;
+    std::call_once(once, [] {
+      const int smem = static_cast<int>(sizeof(CfsShared));
+      attr_err = cudaFuncSetAttribute(ce_fused_stream_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(ce_fused_stream_kernel<__nv_bfloat16>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_f, ce_fused_stream_kernel<float>, CFS_THREADS, smem);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_b, ce_fused_stream_kernel<__nv_bfloat16>, CFS_THREADS, smem);
+    });
+    if (attr_err != cudaSuccess) return TPS_ERR_CUDA;
+    const int occ = c.dlogits_dtype == TPS_F32 ? occ_f : occ_b;
+    const int64_t items = c.T * ((c.V + CFS_CHUNK - 1) / CFS_CHUNK);
+    const int64_t want = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
+    const unsigned grid = static_cast<unsigned>(items < want ? items : want);
+    CeParams q = p;
+    q.count = nullptr;  // counted above
+    if (c.dlogits_dtype == TPS_F32)
+      ce_fused_stream_kernel<float><<<grid, CFS_THREADS, sizeof(CfsShared), stream>>>(q, tile_stats);
+    else
+      ce_fused_stream_kernel<__nv_bfloat16><<<grid, CFS_THREADS, sizeof(CfsShared), stream>>>(q, tile_stats);
+    note_launch();
+    if (cudaPeekAtLastError() != cudaSuccess) return TPS_ERR_CUDA;
+    return c.options ? launch_finalize(c, false, true, stream) : TPS_OK;  // the reduced loss
+  }
   const int64_t nb = (c.T + CEF_TOK_PER_BLOCK - 1) / CEF_TOK_PER_BLOCK;
   if (nb > 0x7FFFFFFF) return TPS_ERR_SHAPE;
   if (c.options && cudaMemsetAsync(c.count, 0, sizeof(int32_t), stream) != cudaSuccess) return TPS_ERR_CUDA;
@@ -1011,9 +1298,6 @@ int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t 
     const int rc = launch_finalize(c, true, true, stream);
     if (rc != TPS_OK) return rc;
   }
-  int dev = 0, sms = 1;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // exactly the blocks that fit at once: a larger grid would run as a
   // second, partial wave
   static int occ_f = 0, occ_b = 0;

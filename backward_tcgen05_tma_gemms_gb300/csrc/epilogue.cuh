@@ -70,6 +70,33 @@ __device__ __forceinline__ void load_run32(const float* p, int n, float (&a)[32]
   }
 }
 
+// `n` (<= 32) bf16 values from p (zero beyond n) as floats.
+__device__ __forceinline__ void load_run32_bf16(const uint16_t* p, int n, float (&a)[32]) {
+  if (n == 32 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + i);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        a[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+        a[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a[i] = (i < n) ? __uint_as_float(static_cast<uint32_t>(__ldg(p + i)) << 16) : 0.0f;
+  }
+}
+
+// The EPI_ACT_BWD pre-activation of row `row`, columns [col0, col0 + n).
+__device__ __forceinline__ void load_pre32(const Epilogue& e, int64_t row, int64_t col0, int n, float (&a)[32]) {
+  if (e.aux_bf16 != nullptr)
+    load_run32_bf16(e.aux_bf16 + row * e.ld_aux + col0, n, a);
+  else
+    load_run32(e.aux + row * e.ld_aux + col0, n, a);
+}
+
 // Apply the epilogue to 32 consecutive accumulator values of row `row`,
 // columns [col0, col0 + n).
 __device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, int64_t col0, int n,
@@ -77,7 +104,7 @@ __device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, i
   if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
     store_run32(e.d, e.d_dtype, row * e.ldd + col0, n, v);
   } else if (e.mode == EPI_ACT_FWD) {
-    if (e.d != nullptr) store_run32(e.d, TPS_F32, row * e.ldd + col0, n, v);
+    if (e.d != nullptr) store_run32(e.d, e.d_dtype, row * e.ldd + col0, n, v);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = act_fwd(e.act, v[i]);
     store_run32(e.d2, e.d2_dtype, row * e.ldd2 + col0, n, v);
@@ -90,7 +117,7 @@ __device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, i
     store_run32(e.d2, e.d2_dtype, row * e.ldd2 + col0, n, v);
   } else {
     float a[32];
-    load_run32(e.aux + row * e.ld_aux + col0, n, a);
+    load_pre32(e, row, col0, n, a);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] *= act_grad(e.act, a[i]);
     store_run32(e.d, e.d_dtype, row * e.ldd + col0, n, v);
@@ -132,7 +159,7 @@ __device__ __forceinline__ void epilogue_elem(const Epilogue& e, int64_t row, in
   if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
     store_elem(e.d, e.d_dtype, row * e.ldd + col, v);
   } else if (e.mode == EPI_ACT_FWD) {
-    if (e.d != nullptr) store_elem(e.d, TPS_F32, row * e.ldd + col, v);
+    if (e.d != nullptr) store_elem(e.d, e.d_dtype, row * e.ldd + col, v);
     store_elem(e.d2, e.d2_dtype, row * e.ldd2 + col, act_fwd(e.act, v));
   } else if (e.mode == EPI_GLU_UP) {
     if (e.d != nullptr) store_elem(e.d, TPS_F32, row * e.ldd + col, v);
@@ -143,7 +170,9 @@ __device__ __forceinline__ void epilogue_elem(const Epilogue& e, int64_t row, in
     store_elem(e.d, e.d_dtype, row * e.ldd + col, v * e.aux2[row * e.ld_aux2 + col] * g);
     store_elem(e.d2, e.d2_dtype, row * e.ldd2 + col, v * f);
   } else {
-    store_elem(e.d, e.d_dtype, row * e.ldd + col, v * act_grad(e.act, e.aux[row * e.ld_aux + col]));
+    const int64_t i = row * e.ld_aux + col;
+    const float pre = e.aux_bf16 != nullptr ? __uint_as_float(static_cast<uint32_t>(e.aux_bf16[i]) << 16) : e.aux[i];
+    store_elem(e.d, e.d_dtype, row * e.ldd + col, v * act_grad(e.act, pre));
   }
 }
 

@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       float a_next[32];
       if (bwd) {
         if (row < p.M) {
-          load_run32(e.aux + row * e.ld_aux + n0, min(32, p.N - n0), a_next);
+          load_pre32(e, row, n0, min(32, p.N - n0), a_next);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) a_next[i] = 0.0f;
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = a_next[i];
           if (row < p.M && col0 + 32 < p.N && c + 1 < TC_BN / 32)
-            load_run32(e.aux + row * e.ld_aux + col0 + 32, min(32, p.N - col0 - 32), a_next);
+            load_pre32(e, row, col0 + 32, min(32, p.N - col0 - 32), a_next);
         }
         tmem_ld_wait();
         float v[32];
@@ -452,7 +452,8 @@ bool tc_make_output_maps(const GemmDesc& g, CUtensorMap* td, CUtensorMap* td2, C
   }
   if (g.epi.mode == EPI_ACT_FWD || g.epi.mode == EPI_GLU_UP) {
     bool ok = true;
-    if (g.epi.d != nullptr) ok = tc_make_out_map(td, g.epi.d, g.M, g.N, g.epi.ldd, TPS_F32);
+    const int pre_dtype = g.epi.mode == EPI_ACT_FWD ? g.epi.d_dtype : TPS_F32;  // U of EPI_GLU_UP is fp32
+    if (g.epi.d != nullptr) ok = tc_make_out_map(td, g.epi.d, g.M, g.N, g.epi.ldd, pre_dtype);
     return ok && g.epi.d2_dtype == TPS_BF16 && tc_make_out_map(td2, g.epi.d2, g.M, g.N, g.epi.ldd2, TPS_BF16);
   }
   return tc_make_out_map(td, g.epi.d, g.M, g.N, g.epi.ldd, g.epi.d_dtype);

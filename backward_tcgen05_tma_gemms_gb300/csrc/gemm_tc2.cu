@@ -96,11 +96,12 @@ struct T2Params {
 // Epilogue families, compiled as separate kernels so that one form's extra
 // live registers and staging do not cost another its registers or stages.
 //   T2_PLAIN    EPI_STORE, EPI_CE_STATS (one output box per chunk)
-//   T2_ACT      EPI_ACT_FWD, EPI_ACT_BWD, EPI_GLU_UP
+//   T2_ACT16    EPI_ACT_FWD, EPI_ACT_BWD with a bf16 pre-activation
+//   T2_ACT      EPI_ACT_FWD, EPI_ACT_BWD with an fp32 pre-activation, EPI_GLU_UP
 //   T2_GLU_FWD  EPI_GLU_FWD
 //   T2_GLU_BWD  EPI_GLU_BWD
 //   T2_SEG      EPI_STORE with contraction or column segments
-enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2, T2_SEG = 3, T2_ACT = 4 };
+enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2, T2_SEG = 3, T2_ACT = 4, T2_ACT16 = 5 };
 
 // Shared-memory layout per family: five operand stages of 32 KB and the
 // epilogue's staging.  With four stages the mainloop measured latency-bound
@@ -108,7 +109,8 @@ enum T2Family : int { T2_PLAIN = 0, T2_GLU_FWD = 1, T2_GLU_BWD = 2, T2_SEG = 3, 
 // the Llama shapes); a sixth stage, where it fits, measured slower again.
 //   plain, segmented  one 4 KB box per warp (fp32 and bf16 share it),
 //                     double-buffered                       -> 5 stages
-//   act               fp32 + bf16 boxes (6 KB), single       -> 5 stages
+//   act, bf16 pre     two bf16 boxes (4 KB), double-buffered -> 5 stages
+//   act, fp32 pre     fp32 + bf16 boxes (6 KB), single       -> 5 stages
 //   gated backward    two bf16 boxes (4 KB), double-buffered -> 5 stages
 //   gated forward     Hg then U through one fp32 box, A bf16
 //                     (6 KB), single-buffered                -> 5 stages
@@ -116,9 +118,11 @@ template <int FAM>
 struct T2Layout {
   static constexpr bool kStoreOnly = FAM == T2_PLAIN || FAM == T2_SEG;
   static constexpr int kStages = 5;
-  static constexpr int kBufBytes =
-      kStoreOnly ? TC_STG_F32_BYTES : (FAM == T2_GLU_BWD ? 2 * TC_STG_BF16_BYTES : T2_STG_BUF);
-  static constexpr int kBufs = (FAM == T2_GLU_BWD || kStoreOnly) ? 2 : 1;
+  static constexpr bool kTwoBf16 = FAM == T2_GLU_BWD || FAM == T2_ACT16;  // two bf16 boxes per buffer
+  static constexpr int kBufBytes = kStoreOnly ? TC_STG_F32_BYTES : (kTwoBf16 ? 2 * TC_STG_BF16_BYTES : T2_STG_BUF);
+  static constexpr int kBufs = (kTwoBf16 || kStoreOnly) ? 2 : 1;
+  // offset of the second (activation) box of an activation-family buffer
+  static constexpr int kSecondBox = kTwoBf16 ? TC_STG_BF16_BYTES : TC_STG_F32_BYTES;
   static constexpr int kWarpStaging = kBufs * kBufBytes;
   static constexpr size_t kSmem =
       1024 + kStages * T2_STAGE_BYTES + T2_EPI_WARPS * kWarpStaging + sizeof(T2Barriers);
@@ -294,7 +298,8 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     uint8_t* stg = staging + ew * L::kWarpStaging;
     const Epilogue& e = p.epi;
     const bool ce = FAM == T2_PLAIN && e.mode == EPI_CE_STATS;
-    const bool bwd = FAM == T2_ACT && p.tma_store && (e.mode == EPI_ACT_BWD || e.mode == EPI_GLU_UP);  // AUX prefetch
+    const bool bwd = (FAM == T2_ACT || FAM == T2_ACT16) && p.tma_store &&
+                     (e.mode == EPI_ACT_BWD || e.mode == EPI_GLU_UP);  // AUX prefetch
     constexpr bool glu = FAM == T2_GLU_FWD;
     constexpr bool gbwd = FAM == T2_GLU_BWD;
     // accumulator columns this warp drains: 128 (gated: 64 gate + 64 up)
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       float a_next[32];
       if (bwd) {
         if (row < p.M && nh0 < p.N) {
-          load_run32(e.aux + row * e.ld_aux + nh0, min(32, p.N - nh0), a_next);
+          load_pre32(e, row, nh0, min(32, p.N - nh0), a_next);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) a_next[i] = 0.0f;
@@ -402,7 +407,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = a_next[i];
           if (row < p.M && col0 + 32 < p.N && c + 1 < warp_cols / 32)
-            load_run32(e.aux + row * e.ld_aux + col0 + 32, min(32, p.N - col0 - 32), a_next);
+            load_pre32(e, row, col0 + 32, min(32, p.N - col0 - 32), a_next);
         }
         tmem_ld_wait();
         float v[32];
@@ -416,8 +421,8 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         // the fp32 and bf16 slots (store-only: one shared box), single- or double-buffered
         uint8_t* buf = stg + (L::kBufs == 2 ? (chunk & 1u) * L::kBufBytes : 0u);
         tc_store_chunk<L::kBufs - 1, L::kStoreOnly>(e, &m.d[oseg], &m.d[1], buf,
-                                                    L::kStoreOnly ? buf : buf + TC_STG_F32_BYTES, lane, row0,
-                                         col0 - ocol0, v, a);
+                                                    L::kStoreOnly ? buf : buf + L::kSecondBox, lane, row0,
+                                                    col0 - ocol0, v, a);
         ++chunk;
       }
       tc_fence_before();
@@ -486,6 +491,9 @@ static int launch_pair_family(const GemmDesc& g, const T2Maps& m, const T2Params
     if (g.epi.mode != EPI_STORE) return TPS_ERR_ARG;
     return launch_pair_majors<T2_SEG>(g, m, p, pairs, a_mn, b_mn, stream);
   }
+  const bool pre16 = (g.epi.mode == EPI_ACT_FWD && (g.epi.d == nullptr || g.epi.d_dtype == TPS_BF16)) ||
+                     (g.epi.mode == EPI_ACT_BWD && g.epi.aux_bf16 != nullptr && g.epi.d_dtype == TPS_BF16);
+  if (pre16) return launch_pair_majors<T2_ACT16>(g, m, p, pairs, a_mn, b_mn, stream);
   if (g.epi.mode == EPI_ACT_FWD || g.epi.mode == EPI_ACT_BWD || g.epi.mode == EPI_GLU_UP)
     return launch_pair_majors<T2_ACT>(g, m, p, pairs, a_mn, b_mn, stream);
   return launch_pair_majors<T2_PLAIN>(g, m, p, pairs, a_mn, b_mn, stream);

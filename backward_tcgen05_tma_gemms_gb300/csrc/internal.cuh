@@ -54,8 +54,12 @@ struct Epilogue {
   void* d2 = nullptr;         // EPI_ACT_FWD activated output, row-major
   int64_t ldd2 = 0;
   int d2_dtype = TPS_BF16;
-  const float* aux = nullptr; // EPI_ACT_BWD pre-activation, row-major fp32
+  const float* aux = nullptr; // EPI_ACT_BWD pre-activation (EPI_GLU_UP: Hg), row-major fp32
   int64_t ld_aux = 0;
+  // EPI_ACT_BWD: when set, the pre-activation is read as bf16 from here
+  // (row-major, leading dimension ld_aux) instead of from `aux`.  EPI_ACT_FWD
+  // stores its pre-activation `d` in d_dtype (fp32 or bf16).
+  const uint16_t* aux_bf16 = nullptr;
   void* d3 = nullptr;         // EPI_GLU_FWD: U, row-major fp32
   int64_t ldd3 = 0;
   const float* aux2 = nullptr;  // EPI_GLU_BWD: U, row-major fp32
@@ -72,7 +76,8 @@ struct Epilogue {
   // Columns at or beyond ce_vreal are vocabulary padding: they are stored
   // but left out of the statistics.
   int64_t ce_vreal = INT64_MAX;
-  float* ce_shift = nullptr;        // shift[row * n_tiles + tile]
+  float* ce_shift = nullptr;        // shift[row * ce_shift_ld + tile]
+  int64_t ce_shift_ld = 0;          // >= n_tiles
   const void* ce_labels = nullptr;  // the label of each row, int32 or int64
   int ce_label_i64 = 0;
   float* ce_zy = nullptr;           // zy[row]: the logit at the label (labels in [0, N))
@@ -141,6 +146,7 @@ struct CeDesc {
   // dimension ldz), the shifts (T x n_tiles) and the label logits in zy.
   const void* logits16 = nullptr;
   const float* shift = nullptr;
+  int64_t shift_ld = 0;           // row stride of `shift`, a multiple of 4 floats
   const void* labels = nullptr;   // T, int32 or int64
   int label_dtype = TPS_I64;
   float* loss = nullptr;          // T fp32
@@ -162,8 +168,10 @@ struct CeDesc {
   float* scale = nullptr;                // workspace: 1 / divisor
 };
 // Vocabulary CE when the logits GEMM already produced per-tile statistics
-// (EPI_CE_STATS): a combine kernel forms each shard's (m_r, s_r), the global
-// log-sum-exp, the loss and the owner; a streaming kernel writes dlogits.
+// (EPI_CE_STATS): each shard's (m_r, s_r), the global log-sum-exp, the loss
+// and the owner are formed from them, and dlogits is streamed from the
+// shifted bf16 logits -- in one kernel when the logits rows are 16-byte
+// aligned, else by a combine kernel and a streaming kernel.
 // `tile_stats` is T x n_tiles x 4 floats, `ms` is T x 2 floats of scratch;
 // the logits come from c.logits16, c.shift and c.zy.
 int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,

@@ -50,7 +50,9 @@ __device__ __forceinline__ void stage_bf16_sw64(uint8_t* buf, int r, const float
 
 // Fused epilogue of one 32 x 32 chunk (lane = row) through TMA stores.
 // `v` holds the accumulators, `a` the pre-activation for EPI_ACT_BWD (Hg
-// for EPI_GLU_UP).  PENDING is the number of this warp's earlier
+// for EPI_GLU_UP).  EPI_ACT_FWD stages its pre-activation in `stg_f32` (a
+// 32 x 32 bf16 box there when d_dtype is bf16) and the activation in
+// `stg_bf16`.  PENDING is the number of this warp's earlier
 // bulk-store groups that may still be reading staging when the buffers are
 // overwritten (0 for one staging buffer, 1 when the caller alternates two).
 // STORE_ONLY: the caller guarantees EPI_STORE.
@@ -71,7 +73,12 @@ __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensor
     else
       stage_bf16_sw64(stg_bf16, lane, v);
   } else if (e.mode == EPI_ACT_FWD) {
-    if (e.d != nullptr) stage_f32_sw128(stg_f32, lane, v);
+    if (e.d != nullptr) {  // the pre-activation, fp32 or bf16, from the first slot
+      if (e.d_dtype == TPS_F32)
+        stage_f32_sw128(stg_f32, lane, v);
+      else
+        stage_bf16_sw64(stg_f32, lane, v);
+    }
     act_dispatch(e.act, [&](auto A) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = act_fwd_c<decltype(A)::value>(v[i]);
@@ -243,7 +250,7 @@ struct CeTileAcc {
   }
   __device__ __forceinline__ void flush(const Epilogue& e, int64_t row, int64_t stat_tile) const {
     *reinterpret_cast<float4*>(e.stats + (row * e.n_tiles + stat_tile) * 4) = make_float4(ma, sa, mb, sb);
-    e.ce_shift[row * e.n_tiles + stat_tile] = shift();
+    e.ce_shift[row * e.ce_shift_ld + stat_tile] = shift();
   }
 };
 

@@ -46,13 +46,13 @@ CE_CORE_BYTES_PER_TOKEN = CE["V"] * (2 + 2) + 4 * CE_TILES + 8 + 4
 # Algorithmic DRAM bytes of the step's eight GEMM launches, averaged per
 # launch: every operand read once and every output written once (bf16
 # operands, fp32 results except the shifted bf16 logits; the column GEMM
-# also writes the fp32 pre-activation, the dZ GEMM also reads it).
+# also writes the bf16 pre-activation, the dZ GEMM also reads it).
 def _gemm_algo_bytes():
     T, d, F, V = MLP["T"], MLP["d"], MLP["F"], CE["V"]
     b = 0
-    b += 2 * T * d + 2 * d * F + 4 * T * F + 2 * T * F      # fc1: X, W1 -> Hp (f32), Ha (bf16)
+    b += 2 * T * d + 2 * d * F + 2 * T * F + 2 * T * F      # fc1: X, W1 -> Hp (bf16), Ha (bf16)
     b += 2 * T * F + 2 * F * d + 4 * T * d                  # fc2: Ha, W2 -> Y
-    b += 2 * T * d + 2 * F * d + 4 * T * F + 2 * T * F      # dh: GY, W2, Hp -> dZ (bf16)
+    b += 2 * T * d + 2 * F * d + 2 * T * F + 2 * T * F      # dh: GY, W2, Hp (bf16) -> dZ (bf16)
     b += 2 * T * F + 2 * T * d + 4 * F * d                  # dW2: Ha, GY -> dW2
     b += 2 * T * d + 2 * T * F + 4 * d * F                  # dW1: X, dZ -> dW1
     b += 2 * T * F + 2 * d * F + 4 * T * d                  # dX: dZ, W1 -> dX

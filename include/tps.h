@@ -147,7 +147,8 @@ int tps_matmul_fwd_bwd(const tps_tensor* A, const tps_tensor* B, const tps_tenso
  * W1, W2: layout `weight_layout` (TPS_W_IN_OUT or TPS_W_OUT_IN), same dtype.
  * Y, dX (..., d) fp32; dW1, dW2 fp32 with the shapes of W1, W2.
  * `workspace` (device, 256-byte aligned, >= tps_mlp_workspace_bytes) holds
- * the pre-activation (fp32), the activation and dZ (operand dtype).
+ * the pre-activation X W1, the activation and dZ, all in the operand dtype
+ * (bf16 runs keep phi'(X W1) from the bf16 pre-activation).
  * Errors as tps_matmul_fwd_bwd, plus TPS_ERR_WORKSPACE, TPS_ERR_ARG (act).
  * ---------------------------------------------------------------------- */
 int tps_mlp_fwd_bwd(const tps_tensor* X, const tps_tensor* W1, const tps_tensor* W2, const tps_tensor* GY,
@@ -171,7 +172,7 @@ size_t tps_mlp_workspace_bytes(int64_t T, int64_t d, int64_t F, int32_t tp, int3
  * a static device array of TPS_MLP_NOALLOC_SCRATCH_BYTES (32 MiB).
  *   - Sizes whose scratch (tps_mlp_workspace_bytes) exceeds the array are
  *     rejected with TPS_ERR_WORKSPACE before anything is launched; for bf16
- *     operands that is T x F > 4,194,304.
+ *     operands that is T x F > 5,592,320.
  *   - Every call looks up the array's device address (cudaGetSymbolAddress,
  *     with the call's device current).  Under lazy module loading (the CUDA
  *     default) the first call on a device is also when the driver loads the

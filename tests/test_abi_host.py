@@ -110,7 +110,9 @@ def test_mlp_and_ce_validation_codes(lib):
 
 
 def test_workspace_queries(lib):
-    assert lib.tps_mlp_workspace_bytes(8192, 4096, 14336, 8, 1) >= 8192 * 14336 * 8
+    # pre-activation, activation and dZ, T x F each in the operand dtype
+    assert lib.tps_mlp_workspace_bytes(8192, 4096, 14336, 8, 1) == 3 * 8192 * 14336 * 2
+    assert lib.tps_mlp_workspace_bytes(64, 32, 100, 8, 0) == 3 * ((64 * 100 * 4 + 255) // 256 * 256)
     assert lib.tps_ce_workspace_bytes(8192, 128256, 8) >= 8192 * 128256 * 4
 
 

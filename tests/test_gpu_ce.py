@@ -130,25 +130,58 @@ def test_label_out_of_range_sets_error():
     assert api.last_device_error() == 0     # the word was cleared
 
 
+def boundary_labels(V, tp, vreal=None):
+    """Eight labels per rank: four at the first columns of its shard and
+    four at its last (real) columns.  At V = 128256, tp = 8 the shards start
+    at multiples of 16032 = 125 x 128 + 32, so each shard's first 96
+    columns share a 128-column statistics tile with the previous shard: the
+    labels there read their logit from a tile whose statistics are split
+    between two shards."""
+    off = api.plan_shards(V, tp)
+    vr = V if vreal is None else vreal
+    labs = []
+    for r in range(tp):
+        lo, hi = off[r], min(off[r + 1], vr)
+        labs += [lo, lo + 1, lo + 31, lo + 95, hi - 96, hi - 33, hi - 2, hi - 1]
+    return np.array(labs, dtype=np.int64)
+
+
+def spread_tokens(T, n, seed, avoid_mod=None):
+    """n distinct tokens spread over [0, T) including the first and last
+    (optionally none that are multiples of avoid_mod)."""
+    rng = np.random.default_rng(seed)
+    pool = np.arange(1, T - 1)
+    if avoid_mod:
+        pool = pool[pool % avoid_mod != 0]
+    toks = np.concatenate([[0 if not avoid_mod else 1, T - 1], rng.choice(pool, n - 2, replace=False)])
+    return np.sort(toks)
+
+
 def test_llama_vocab_sampled(orc):
     """h 8192 x 4096, head 4096 x 128256, tp=8 (16032 per shard), bf16, at
-    full size in the benchmark's launch configuration; 8 tokens spread over
-    the batch are recomputed by the oracle (loss, full dlogits row, dHidden
-    row) and every owner rank is checked against a host scan."""
+    full size in the benchmark's launch configuration.  64 tokens spread
+    over the batch get labels at both ends of every shard (each rank owns
+    eight), and the oracle recomputes their loss, full dlogits row and
+    dHidden row; every owner rank of the batch is checked against a host
+    scan."""
     cfg = inputs.LLAMA_CE
-    h, W, labels = inputs.ce_case(0, cfg["T"], cfg["d"], cfg["V"], torch.bfloat16)
-    (loss, dlog, dh, own), rc = run(h, W, labels, cfg["tp"])
+    T, V, tp = cfg["T"], cfg["V"], cfg["tp"]
+    h, W, labels = inputs.ce_case(0, T, cfg["d"], V, torch.bfloat16)
+    toks = spread_tokens(T, 64, 5)
+    labels[torch.from_numpy(toks)] = torch.from_numpy(boundary_labels(V, tp))
+    (loss, dlog, dh, own), rc = run(h, W, labels, tp)
     assert rc == 0
-    toks = np.array([0, 1, 1000, 2047, 4096, 5555, 8000, 8191])
-    rl, rdl, rdh, rown = orc.ce_tokens(inputs.as_f64(h), inputs.as_f64(W), labels.numpy(), cfg["tp"], toks)
+    rl, rdl, rdh, rown = orc.ce_tokens(inputs.as_f64(h), inputs.as_f64(W), labels.numpy(), tp, toks)
     assert_close(loss[toks], rl, True, "loss")
     assert_close(dlog[toks], rdl, True, "dlogits")
     assert_close(dh[toks], rdh, True, "dHidden")
-    off = np.array(api.plan_shards(cfg["V"], cfg["tp"]))
+    assert np.array_equal(own[toks].numpy(), rown)
+    assert np.bincount(rown, minlength=tp).min() >= 4
+    off = np.array(api.plan_shards(V, tp))
     assert np.array_equal(own.numpy(), np.searchsorted(off, labels.numpy(), side="right") - 1)
     assert torch.isfinite(loss).all()
     # mean loss near log V + var(z)/2 with var(z) = d * 0.02^2
-    assert abs(loss.mean().item() - (math.log(cfg["V"]) + cfg["d"] * 0.02 ** 2 / 2)) < 0.1
+    assert abs(loss.mean().item() - (math.log(V) + cfg["d"] * 0.02 ** 2 / 2)) < 0.1
 
 
 def test_bf16_int32_labels_match_int64(gemm_kernel):
@@ -173,3 +206,23 @@ def test_bf16_unaligned_vocab_rows(orc, T, gemm_kernel):
     with api.profile() as p:
         check(orc, h, W, labels, 2, True, "out_in", what=f"bf16 V4100 T{T}")
     assert "ce_stream" in {k.split(":")[0] for k in p.summary}, p.summary
+
+
+@pytest.mark.parametrize("T,V,tp", [(300, 4096, 7), (513, 16032, 8)])
+def test_fused_core_matches_two_kernels(T, V, tp, monkeypatch):
+    """The fused CE core (per-shard combine and gradient stream in one
+    kernel, logits bulk-copied into shared memory) and the two-kernel form
+    (combine kernel, then streaming kernel) evaluate the same formulas in
+    the same order: identical bits, shard boundaries inside tiles included
+    (16032 / 8 = 2004 = 15 x 128 + 84)."""
+    h, W, labels = inputs.ce_case(T + V, T, 64, V, torch.bfloat16, w_std=0.2)
+    n0 = api.launch_count()
+    a, rc_a = run(h, W, labels, tp)
+    fused_launches = api.launch_count() - n0
+    monkeypatch.setenv("TPS_CE_TWO_KERNELS", "1")
+    n0 = api.launch_count()
+    b, rc_b = run(h, W, labels, tp)
+    assert api.launch_count() - n0 == fused_launches + 1   # logits GEMM, CE core, dHidden GEMM
+    assert rc_a == 0 and rc_b == 0
+    for x, y, name in zip(a, b, ("loss", "dlogits", "dHidden", "owner")):
+        assert torch.equal(x, y), name
