@@ -910,8 +910,9 @@ extern "C" int tps_attn_out_fwd_bwd(const tps_tensor* C, const tps_tensor* Wo, c
 }
 
 // CE workspace: logits (T x V, fp32, or bf16 on the tensor-core path) |
-// per-shard stats of the two-pass path (T x tp x 2) | label logits (T) |
-// per-tile stats (T x ceil(V/128) x 4) | per-tile shifts (T rows of
+// per-shard stats (T x tp x 2: the two-pass path's, or on the tensor-core
+// path the statistics of tiles that straddle a shard start) | label logits
+// (T) | per-tile stats (T x ceil(V/128) x 2) | per-tile shifts (T rows of
 // ceil(V/128) floats, padded to a multiple of 4) | combined (m, 1/s) per
 // token (T x 2)
 // | 256 bytes of scalars (the count of supervised labels, int32 at +0, and
@@ -930,7 +931,7 @@ static CeWs ce_ws_layout(int64_t T, int64_t V, int32_t tp, size_t logit_bytes) {
   w.stats = w.z + align256(t * static_cast<size_t>(V) * logit_bytes);
   w.zy = w.stats + align256(t * static_cast<size_t>(tp) * 2 * 4);
   w.tiles = w.zy + align256(t * 4);
-  w.shift = w.tiles + align256(t * n_tiles * 4 * 4);
+  w.shift = w.tiles + align256(t * n_tiles * 2 * 4);
   w.ms = w.shift + align256(t * ce_shift_ld(V) * 4);
   w.scal = w.ms + align256(t * 2 * 4);
   w.total = w.scal + 256;
@@ -1070,6 +1071,7 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
     g.epi.mode = EPI_CE_STATS;
     g.epi.d_dtype = TPS_BF16;
     g.epi.stats = tile_stats;
+    g.epi.stats_b = stats;
     g.epi.n_tiles = n_tiles;
     g.epi.ce_parts = tp;
     g.epi.ce_vreal = vreal;

@@ -794,9 +794,11 @@ __global__ void __launch_bounds__(1024) ce_finalize_kernel(const float* loss, in
 
 // ------------------------------------------------------------ from tile statistics
 // The logits GEMM's epilogue left, per (token, 128-column tile), the
-// statistics of the tile's columns split at the shard boundary.  Shard r's
-// (m_r, s_r) combines the tiles whose first column lies in r (their first
-// part) and, when r starts inside a tile, that tile's second part.
+// statistics of the tile's columns in the shard of its first column, and
+// per (token, shard) the statistics of the part of the tile in which the
+// shard starts, when that is not a tile boundary.  Shard r's (m_r, s_r)
+// combines the tiles whose first column lies in r and, when r starts inside
+// a tile, that tile's part in r.
 
 constexpr int CEF_TOK_PER_BLOCK = 8;  // one warp per token
 
@@ -805,16 +807,16 @@ __global__ void __launch_bounds__(32 * CEF_TOK_PER_BLOCK) ce_combine_kernel(cons
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * CEF_TOK_PER_BLOCK + w;
   if (t >= p.T) return;
-  const float4* row = reinterpret_cast<const float4*>(ts) + t * n_tiles;
+  const float2* row = reinterpret_cast<const float2*>(ts) + t * n_tiles;
+  const float2* row_b = reinterpret_cast<const float2*>(p.stats) + t * p.parts;
   float m = -INFINITY, s = 0.0f;  // running global combine (identical in all lanes)
   for (int32_t r = 0; r < p.parts; ++r) {
     const int64_t beg = shard_offset(p.V, p.parts, r), end = shard_offset(p.V, p.parts, r + 1);
     const int64_t t0 = beg / kStatsTileN, t1 = (end - 1) / kStatsTileN;
     float mr = -INFINITY, sr = 0.0f;
     for (int64_t tt = t0 + lane; tt <= t1; tt += 32) {
-      const float4 e = row[tt];
-      const bool second = (tt == t0) && (beg % kStatsTileN != 0);
-      ms_combine_acc(mr, sr, second ? e.z : e.x, second ? e.w : e.y);
+      const float2 e = (tt == t0 && beg % kStatsTileN != 0) ? row_b[r] : row[tt];
+      ms_combine_acc(mr, sr, e.x, e.y);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
@@ -1043,25 +1045,23 @@ __global__ void __launch_bounds__(CFS_THREADS) ce_fused_stream_kernel(const CePa
     uint32_t slot = 0, phase = 0;
     for (int64_t t = t_first; t <= t_last; ++t) {
       if (!mbar_wait(&sh.row_empty[slot], phase ^ 1u, &sh.abort, p.err)) break;
-      const float4* row = reinterpret_cast<const float4*>(ts) + t * p.n_tiles;
+      const float2* row = reinterpret_cast<const float2*>(ts) + t * p.n_tiles;
+      const float2* row_b = reinterpret_cast<const float2*>(p.stats) + t * p.parts;
       float m = -INFINITY, s = 0.0f;
       for (int32_t r = 0; r < p.parts; ++r) {
         const int64_t beg = shard_offset(p.V, p.parts, r), end = shard_offset(p.V, p.parts, r + 1);
         const int64_t t0 = beg / kStatsTileN, t1 = (end - 1) / kStatsTileN;
-        const bool split0 = beg % kStatsTileN != 0;  // shard r starts inside tile t0: its second part
+        const bool split0 = beg % kStatsTileN != 0;  // shard r starts inside tile t0: its part in r
         float mr = -INFINITY, sr = 0.0f;
         for (int64_t tt = t0 + lane; tt <= t1; tt += 4 * 32) {
-          float4 e[4];
+          float2 e[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int64_t u = tt + 32 * k;
-            e[k] = u <= t1 ? __ldg(row + u) : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+            e[k] = u > t1 ? make_float2(-INFINITY, 0.0f) : ((u == t0 && split0) ? row_b[r] : __ldg(row + u));
           }
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const bool second = (tt + 32 * k == t0) && split0;
-            ms_combine_acc(mr, sr, second ? e[k].z : e[k].x, second ? e[k].w : e[k].y);
-          }
+          for (int k = 0; k < 4; ++k) ms_combine_acc(mr, sr, e[k].x, e[k].y);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
@@ -1241,7 +1241,7 @@ int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t 
   if (c.T == 0) return TPS_OK;
   if (c.logits16 == nullptr || c.shift == nullptr || c.zy == nullptr) return TPS_ERR_ARG;
   CeParams p = make_params(c, dev_err);
-  p.stats = nullptr;
+  p.stats = c.stats;  // statistics of the tiles in which a shard starts
   p.n_tiles = n_tiles;
   const int64_t gsize = c.dlogits_dtype == TPS_F32 ? 4 : 2;
   const double bytes = double(c.T) * double(c.V) * (2.0 + gsize) + double(c.T) * double(n_tiles) * 4.0 +

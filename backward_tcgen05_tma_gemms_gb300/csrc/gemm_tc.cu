@@ -378,7 +378,8 @@ bool gemm_tc_supported(const GemmDesc& g) {
   if (g.M >= (1ll << 31) || g.N >= (1ll << 31) || g.K + g.K2 + g.K3 >= (1ll << 31)) return false;
   const bool k_segs = g.K2 > 0 || g.K3 > 0;
   if (g.epi.mode == EPI_GLU_FWD && (g.b_up == nullptr || k_segs || g.n_segs > 1)) return false;
-  if (g.epi.mode == EPI_CE_STATS && (g.epi.d_dtype != TPS_BF16 || g.epi.stats == nullptr || g.epi.ce_shift == nullptr ||
+  if (g.epi.mode == EPI_CE_STATS && (g.epi.d_dtype != TPS_BF16 || g.epi.stats == nullptr || g.epi.stats_b == nullptr ||
+                                     g.epi.ce_shift == nullptr ||
                                      g.epi.ce_labels == nullptr || g.epi.ce_zy == nullptr))
     return false;
   if (g.n_segs < 1 || g.n_segs > 3 || (g.n_segs > 1 && k_segs)) return false;

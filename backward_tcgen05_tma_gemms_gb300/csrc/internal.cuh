@@ -64,13 +64,16 @@ struct Epilogue {
   int64_t ldd3 = 0;
   const float* aux2 = nullptr;  // EPI_GLU_BWD: U, row-major fp32
   int64_t ld_aux2 = 0;
-  // EPI_CE_STATS: stats[(row * n_tiles + tile) * 4 + {0,1,2,3}] =
-  // (m_a, s_a, m_b, s_b): max and sum of e^{z - max} over the tile's columns
-  // in the shard that owns the tile's first column (a) and in the next shard
-  // (b, empty = (-inf, 0) unless a shard boundary falls inside the tile).
-  // Shards are the array_split of N into ce_parts; every shard must be at
-  // least kStatsTileN wide so that a tile meets at most two.
+  // EPI_CE_STATS: stats[(row * n_tiles + tile) * 2 + {0, 1}] = (m_a, s_a),
+  // the max and sum of e^{z - max} over the tile's columns in the shard that
+  // owns the tile's first column.  When shard b starts inside the tile, the
+  // same pair over the tile's columns in shard b goes to
+  // stats_b[(row * ce_parts + b) * 2 + {0, 1}] (entries of shards that
+  // start on a tile boundary are never written).  Shards are the
+  // array_split of N into ce_parts; every shard must be at least
+  // kStatsTileN wide so that a tile meets at most two.
   float* stats = nullptr;
+  float* stats_b = nullptr;
   int64_t n_tiles = 0;
   int32_t ce_parts = 1;
   // Columns at or beyond ce_vreal are vocabulary padding: they are stored
@@ -172,8 +175,10 @@ struct CeDesc {
 // and the owner are formed from them, and dlogits is streamed from the
 // shifted bf16 logits -- in one kernel when the logits rows are 16-byte
 // aligned, else by a combine kernel and a streaming kernel.
-// `tile_stats` is T x n_tiles x 4 floats, `ms` is T x 2 floats of scratch;
-// the logits come from c.logits16, c.shift and c.zy.
+// `tile_stats` is T x n_tiles x 2 floats and c.stats (T x parts x 2) holds
+// the statistics of the tiles in which a shard starts (Epilogue::stats_b);
+// `ms` is T x 2 floats of scratch; the logits come from c.logits16,
+// c.shift and c.zy.
 int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,
                               uint32_t* dev_err, cudaStream_t stream);
 bool ce_tile_stats_supported(int64_t V, int32_t parts);

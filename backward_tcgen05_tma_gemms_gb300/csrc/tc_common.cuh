@@ -218,9 +218,13 @@ __device__ __forceinline__ int64_t shard_of(int64_t c, int64_t n, int64_t p) {
 
 struct CeTileAcc {
   int64_t split;  // first column of shard b
+  int64_t b;      // shard b: the one after the shard of the tile's first column
+  bool has_b;     // shard b starts inside the tile
   float ma, sa, mb, sb;
   __device__ __forceinline__ void reset(const Epilogue& e, int64_t N, int64_t tile_col0) {
-    split = shard_offset(N, e.ce_parts, shard_of(tile_col0, N, e.ce_parts) + 1);
+    b = shard_of(tile_col0, N, e.ce_parts) + 1;
+    split = shard_offset(N, e.ce_parts, b);
+    has_b = b < e.ce_parts && split > tile_col0 && split < tile_col0 + kStatsTileN;
     ma = -INFINITY;
     sa = 0.0f;
     mb = -INFINITY;
@@ -249,7 +253,8 @@ struct CeTileAcc {
     return m == -INFINITY ? 0.0f : m;
   }
   __device__ __forceinline__ void flush(const Epilogue& e, int64_t row, int64_t stat_tile) const {
-    *reinterpret_cast<float4*>(e.stats + (row * e.n_tiles + stat_tile) * 4) = make_float4(ma, sa, mb, sb);
+    reinterpret_cast<float2*>(e.stats)[row * e.n_tiles + stat_tile] = make_float2(ma, sa);
+    if (has_b) reinterpret_cast<float2*>(e.stats_b)[row * e.ce_parts + b] = make_float2(mb, sb);
     e.ce_shift[row * e.ce_shift_ld + stat_tile] = shift();
   }
 };

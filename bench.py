@@ -291,17 +291,20 @@ def run_gpu(args, rank, world, local_rank):
     del graph
 
     # ---- end-to-end: pinned host inputs in, every result out, every step.
-    # Copy streams pipeline consecutive steps: host->device copies of step
-    # i+1's inputs and device->host copies of step i-1's results overlap the
-    # kernels of step i.  Each direction has --copy-streams streams (the
-    # host link moves about 290 GB/s both ways at once with two or more per
-    # direction, 170 GB/s with one), and every tensor above COPY_CHUNK bytes
-    # is split over them.  Inputs and results have --e2e-buffers buffers on
-    # both sides, so a step's kernels wait only for copies two steps back;
-    # events order every reuse.
-    nbuf = args.e2e_buffers
+    # Software pipeline over two buffer sets, each step one CUDA-graph
+    # replay whose three branches run concurrently: the host->device copies
+    # of step i+1's inputs, the library calls of step i, and the
+    # device->host copies of step i-1's results.  The graphs replay back to
+    # back on one stream, so step i+1 starts when all three branches of step
+    # i are done, and the host only launches graphs (an eager loop of copy
+    # and library calls stalled the GPU for tens of ms whenever the host
+    # fell behind).  The first step's input copies and the last step's
+    # result copies run outside the graphs, inside the timed region.
+    # Every tensor above COPY_CHUNK bytes is split over --copy-streams
+    # streams per direction: the host link moves about 270 GB/s both ways
+    # at once with two streams per direction, 170 GB/s with one.
     pinned = {k: v.pin_memory() for k, v in host.items()}
-    in_bufs = [d] + [{k: torch.empty_like(v) for k, v in d.items()} for _ in range(nbuf - 1)]
+    in_bufs = [d, {k: torch.empty_like(v) for k, v in d.items()}]
     mlp_names = ("Y", "dX", "dW1", "dW2")
     ce_names = ("loss", "dlogits", "dHidden", "owner")
 
@@ -310,98 +313,105 @@ def run_gpu(args, rank, world, local_rank):
                     dW2=torch.empty(F, dm, **f32), loss=torch.empty(T, **f32),
                     dlogits=torch.empty(T, V, device=dev, dtype=torch.bfloat16), dHidden=torch.empty(T, dm, **f32),
                     owner=torch.empty(T, device=dev, dtype=torch.int32))
-    out_bufs = [new_outs() for _ in range(nbuf)]
+    out_bufs = [new_outs(), new_outs()]
     host_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out_bufs[0].items()}
-                for _ in range(nbuf)]
+                for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = sum(v.numel() * v.element_size() for v in out_bufs[0].values())
     ns = args.copy_streams
     s_h2d = [torch.cuda.Stream(dev) for _ in range(ns)]
     s_d2h = [torch.cuda.Stream(dev) for _ in range(ns)]
-    ev = lambda: torch.cuda.Event()
-    ev_in_free = [[ev() for _ in range(ns)] for _ in range(nbuf)]   # per buffer, per h2d stream
-    ev_out_free = [[ev() for _ in range(ns)] for _ in range(nbuf)]  # per buffer, per d2h stream
-    for row in ev_in_free + ev_out_free:
-        for e_ in row:
-            e_.record(stream)
 
-    def pieces(names, tensors):
-        """(dst key, flat slice) pieces of the named tensors, the large ones
-        split into COPY_CHUNK-sized parts."""
+    def pieces(tensors):
+        """(key, first, end) flat slices of the tensors, the large ones split
+        into COPY_CHUNK-sized parts."""
         out = []
-        for k in names:
-            t = tensors[k].view(-1)
+        for k, t in tensors.items():
             n = t.numel()
             step = max(1, COPY_CHUNK // t.element_size())
             for j in range(0, n, step):
                 out.append((k, j, min(n, j + step)))
         return out
 
-    def copies(streams, waits, items, dst, src):
-        """Enqueue the copies round-robin over `streams`, each stream first
-        waiting for `waits`; returns one completion event per stream."""
+    def branch(streams, dst, src):
+        """Copies src -> dst round-robin over `streams`, forked from and
+        joined back into the current stream."""
+        cur = torch.cuda.current_stream(dev)
+        fork = torch.cuda.Event()
+        fork.record(cur)
         for s_ in streams:
-            for w in waits:
-                s_.wait_event(w)
-        for n_, (k, j0, j1) in enumerate(items):
-            s_ = streams[n_ % len(streams)]
-            with torch.cuda.stream(s_):
+            s_.wait_event(fork)
+        for n_, (k, j0, j1) in enumerate(pieces(src)):
+            with torch.cuda.stream(streams[n_ % len(streams)]):
                 dst[k].view(-1)[j0:j1].copy_(src[k].view(-1)[j0:j1], non_blocking=True)
-        done = []
+        joins = []
         for s_ in streams:
-            e_ = ev()
+            e_ = torch.cuda.Event()
             e_.record(s_)
-            done.append(e_)
-        return done
+            joins.append(e_)
+        return joins
 
-    mlp_in, ce_in = ("X", "W1", "W2", "GY"), ("h", "W", "labels")
-
-    def e2e_step(i):
-        b = i % nbuf
-        src, out, hout = in_bufs[b], out_bufs[b], host_out[b]
-        mlp_ready = copies(s_h2d, ev_in_free[b], pieces(mlp_in, pinned), src, pinned)
-        ce_ready = copies(s_h2d, [], pieces(ce_in, pinned), src, pinned)
-        for e_ in mlp_ready + ev_out_free[b]:
-            stream.wait_event(e_)
+    def compute(b):
+        src, out = in_bufs[b], out_bufs[b]
         api.mlp_fwd_bwd(src["X"], src["W1"], src["W2"], src["GY"], MLP["tp"], "gelu_tanh", "in_out",
                         workspace=mlp_ws, out=tuple(out[k] for k in mlp_names))
-        ev_mlp_done = ev()
-        ev_mlp_done.record(stream)
-        for e_ in ce_ready:
-            stream.wait_event(e_)
         api.vocab_ce_fwd_bwd(src["h"], src["W"], src["labels"], CE["tp"], "in_out", workspace=ce_ws,
                              out=tuple(out[k] for k in ce_names))
-        ev_ce_done = ev()
-        ev_ce_done.record(stream)
-        for e_ in ev_in_free[b]:
-            e_.record(stream)
-        copies(s_d2h, [ev_mlp_done], pieces(mlp_names, out), hout, out)
-        ev_out_free[b] = copies(s_d2h, [ev_ce_done], pieces(ce_names, out), hout, out)
 
-    for i in range(nbuf):
-        e2e_step(i)
+    def pipeline_step(b, load_next=True, store_prev=True):
+        """Step on buffer set b: inputs of the next step into set 1-b,
+        kernels on set b, results of the previous step out of set 1-b."""
+        cur = torch.cuda.current_stream(dev)
+        joins = branch(s_h2d, in_bufs[1 - b], pinned) if load_next else []
+        joins += branch(s_d2h, host_out[1 - b], out_bufs[1 - b]) if store_prev else []
+        compute(b)
+        for e_ in joins:
+            cur.wait_event(e_)
+
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graphs = []
+    with torch.cuda.stream(cap):
+        pipeline_step(0)
+        pipeline_step(1)          # warm both buffer sets before capture
+        cap.synchronize()
+        for b in range(2):
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_, stream=cap):
+                pipeline_step(b)
+            graphs.append(g_)
+    stream.wait_stream(cap)
+
+    def e2e_run(n):
+        """n pipelined steps: the first step's inputs in, n steps, the last
+        step's results out."""
+        joins = branch(s_h2d, in_bufs[0], pinned)
+        for e_ in joins:
+            stream.wait_event(e_)
+        for i in range(n):
+            b = i % 2
+            if i == 0 or i == n - 1:   # the pipeline's ends: nothing before or after them
+                pipeline_step(b, load_next=i < n - 1, store_prev=i > 0)
+            else:
+                graphs[b].replay()
+        for e_ in branch(s_d2h, host_out[(n - 1) % 2], out_bufs[(n - 1) % 2]):
+            stream.wait_event(e_)
+
+    e2e_run(3)
     torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with clk.window():
         e0.record(stream)
-        go = ev()
-        go.record(stream)
-        for s_ in s_h2d + s_d2h:
-            s_.wait_event(go)
-        for i in range(args.steps):
-            e2e_step(i)
-        for row in ev_out_free:
-            for e_ in row:
-                stream.wait_event(e_)
+        e2e_run(args.steps)
         e1.record(stream)
         torch.cuda.synchronize(dev)
     time.sleep(0.2)
     clk.__exit__(None, None, None)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    last = host_out[(args.steps - 1) % nbuf]
+    last = host_out[(args.steps - 1) % 2]
     assert torch.isfinite(last["loss"]).all(), "non-finite loss"
     # each dlogits row is softmax - onehot: it sums to ~0
     assert abs(float(last["dlogits"][0].float().sum())) < 0.05, "dlogits row does not sum to 0"
@@ -409,6 +419,7 @@ def run_gpu(args, rank, world, local_rank):
     rc = api.last_device_error()
     if rc != 0:
         raise RuntimeError(f"device error {rc} in the end-to-end region")
+    del graphs
 
     # max over ranks
     if world > 1:
@@ -538,7 +549,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-widened", action="store_true", help="skip timing the rows beyond the step")
     ap.add_argument("--copy-streams", type=int, default=2, help="end-to-end copy streams per direction")
-    ap.add_argument("--e2e-buffers", type=int, default=3, help="end-to-end input and result buffers")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -626,7 +636,11 @@ def main():
                   "what": "the same step captured once in a CUDA graph and replayed (inputs resident)"},
         "clocks": r["clocks"],
         "e2e": {"value": STEP_FLOPS * world / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+                "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "what": "every step copies all inputs from pinned host memory and all results (dlogits and owner "
+                        "included) back, pipelined over two buffer sets: each step one CUDA-graph replay of the "
+                        "next step's input copies, this step's library calls and the previous step's result "
+                        "copies; the first inputs and last results inside the timed region too"},
     }
     if r["widened"] is not None:
         line["widened_rows"] = r["widened"]
