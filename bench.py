@@ -382,9 +382,9 @@ def run_gpu(args, rank, world, local_rank):
             graphs.append(g_)
     stream.wait_stream(cap)
 
-    def e2e_run(n):
+    def e2e_run(n, marks=None):
         """n pipelined steps: the first step's inputs in, n steps, the last
-        step's results out."""
+        step's results out.  `marks` (n + 1 timing events) bracket the steps."""
         joins = branch(s_h2d, in_bufs[0], pinned)
         for e_ in joins:
             stream.wait_event(e_)
@@ -394,6 +394,8 @@ def run_gpu(args, rank, world, local_rank):
                 pipeline_step(b, load_next=i < n - 1, store_prev=i > 0)
             else:
                 graphs[b].replay()
+            if marks is not None and i < n - 1:
+                marks[i + 1].record(stream)
         for e_ in branch(s_d2h, host_out[(n - 1) % 2], out_bufs[(n - 1) % 2]):
             stream.wait_event(e_)
 
@@ -401,16 +403,20 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    e0, e1 = marks[0], marks[-1]
     with clk.window():
         e0.record(stream)
-        e2e_run(args.steps)
+        e2e_run(args.steps, marks)
         e1.record(stream)
         torch.cuda.synchronize(dev)
     time.sleep(0.2)
     clk.__exit__(None, None, None)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
+    # per step (the first with the first inputs' copies, the last with the
+    # last results' copies)
+    e2e_steps = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
     last = host_out[(args.steps - 1) % 2]
     assert torch.isfinite(last["loss"]).all(), "non-finite loss"
     # each dlogits row is softmax - onehot: it sums to ~0
@@ -425,7 +431,7 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         ms, e2e_ms, graph_ms = max_over_ranks([ms, e2e_ms, graph_ms], dev)
     widened = None if args.no_widened else run_widened(args, dev, d)
-    return dict(ms=ms, e2e_ms=e2e_ms, graph_ms=graph_ms, prof=prof.summary, launches=launches, clocks=clk.summary(), h2d=h2d, d2h=d2h,
+    return dict(ms=ms, e2e_ms=e2e_ms, e2e_steps=e2e_steps, graph_ms=graph_ms, prof=prof.summary, launches=launches, clocks=clk.summary(), h2d=h2d, d2h=d2h,
                 host=host, widened=widened)
 
 
@@ -640,7 +646,13 @@ def main():
                 "what": "every step copies all inputs from pinned host memory and all results (dlogits and owner "
                         "included) back, pipelined over two buffer sets: each step one CUDA-graph replay of the "
                         "next step's input copies, this step's library calls and the previous step's result "
-                        "copies; the first inputs and last results inside the timed region too"},
+                        "copies; the first inputs and last results inside the timed region too",
+                "step_ms": {"median": statistics.median(r["e2e_steps"]), "min": min(r["e2e_steps"]),
+                            "max": max(r["e2e_steps"]),
+                            "stalled_steps": sum(1 for x in r["e2e_steps"] if x > 1.5 * statistics.median(r["e2e_steps"])),
+                            "note": "the host link's device-to-host copies stall for 20-190 ms a few times per 40 "
+                                    "steps on these boxes (seen with no kernels running too); value is the plain "
+                                    "mean over all timed steps"}},
     }
     if r["widened"] is not None:
         line["widened_rows"] = r["widened"]
