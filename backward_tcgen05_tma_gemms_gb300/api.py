@@ -15,10 +15,14 @@ from typing import Optional, Sequence
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libtps.so")
+# TPS_LIBRARY selects another build of the library (the debug build,
+# libtps_debug.so, whose kernels bounds-check every store).
+LIB_PATH = os.environ.get("TPS_LIBRARY") or os.path.join(_PKG, "libtps.so")
 
 F32, BF16, I32, I64 = 0, 1, 2, 3
-OK, ERR_SHAPE, ERR_PARTITION, ERR_DTYPE, ERR_LAYOUT, ERR_LABEL, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_ARG = range(10)
+(OK, ERR_SHAPE, ERR_PARTITION, ERR_DTYPE, ERR_LAYOUT, ERR_LABEL, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_ARG,
+ ERR_BOUNDS) = range(11)
+BUILD_DEBUG = 1  # bit of tps_build_flags()
 AXES = {"rows": 0, "columns": 1, "inner": 2}
 ACTS = {"gelu": 0, "gelu_erf": 0, "gelu_tanh": 1, "tanh": 2, "silu": 3}
 LAYOUTS = {"in_out": 0, "out_in": 1}

@@ -5,7 +5,12 @@ then linked into a shared library with the CUDA runtime linked statically,
 so loading the library needs no GPU and no libcuda at load time (the driver
 entry points are resolved through the runtime on first use).
 
-    python -m backward_tcgen05_tma_gemms_gb300.build [--force]
+`debug=True` builds libtps_debug.so instead (TPS_DEBUG=1: every epilogue
+and cross-entropy store is checked against the bounds of its output, and a
+store outside is skipped and reported as TPS_ERR_BOUNDS).  Set
+TPS_LIBRARY to its path to make the Python binding load it.
+
+    python -m backward_tcgen05_tma_gemms_gb300.build [--force] [--debug]
 """
 from __future__ import annotations
 
@@ -21,6 +26,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtps.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libtps_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -42,8 +49,8 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, extra, build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -53,27 +60,32 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile and link libtps.so if any source is newer than it; return its path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
+    """Compile and link libtps.so (libtps_debug.so with debug=True) if any
+    source is newer than it; return its path."""
+    lib, build_dir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if debug:
+        extra += ["-DTPS_DEBUG=1"]
     srcs = sources()
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--ptxas-v", action="store_true", help="print register / shared memory usage")
+    ap.add_argument("--debug", action="store_true", help="build libtps_debug.so (bounds-checked stores)")
     a = ap.parse_args()
-    print(build(force=a.force, verbose_ptxas=a.ptxas_v))
+    print(build(force=a.force, verbose_ptxas=a.ptxas_v, debug=a.debug))

@@ -236,6 +236,9 @@ static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream)
       }
       return TPS_OK;
     }
+    g.epi.dbg_rows = g.M;
+    g.epi.dbg_cols = g.N;
+    g.epi.dbg_err = err;
     const int rc = launch_gemm_tc(g, err, stream);
     if (rc == TPS_ERR_CUDA) return fail(rc, "%s: launch failed: %s", g.name, cudaGetErrorString(cudaGetLastError()));
     return rc;
@@ -280,6 +283,9 @@ static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream)
   } else {
     g.epi.ldd = d_sm;
   }
+  g.epi.dbg_rows = g.M;  // the output as the kernels write it (row-major M x N)
+  g.epi.dbg_cols = g.N;
+  g.epi.dbg_err = err;
   const int rc = gemm_tc_supported(g) ? launch_gemm_tc(g, err, stream) : launch_gemm_simt(g, err, stream);
   if (rc == TPS_ERR_CUDA) return fail(rc, "%s: launch failed: %s", g.name, cudaGetErrorString(cudaGetLastError()));
   return rc;
@@ -1161,9 +1167,12 @@ extern "C" int tps_last_device_error(void* cuda_stream) {
   const uint32_t zero = 0;
   if (cudaMemcpyToSymbol(g_dev_err_word, &zero, sizeof(zero)) != cudaSuccess) return TPS_ERR_CUDA;
   if (v & TPS_DEVERR_TIMEOUT) return TPS_ERR_TIMEOUT;
+  if (v & TPS_DEVERR_BOUNDS) return TPS_ERR_BOUNDS;
   if (v & TPS_DEVERR_LABEL) return TPS_ERR_LABEL;
   return TPS_OK;
 }
+
+extern "C" int tps_build_flags(void) { return TPS_DEBUG ? TPS_BUILD_DEBUG : 0; }
 
 extern "C" const char* tps_strerror(int code) {
   switch (code) {
@@ -1177,6 +1186,7 @@ extern "C" const char* tps_strerror(int code) {
     case TPS_ERR_CUDA: return "cuda";
     case TPS_ERR_TIMEOUT: return "device wait timed out";
     case TPS_ERR_ARG: return "argument";
+    case TPS_ERR_BOUNDS: return "store outside its output (debug build)";
     default: return "unknown";
   }
 }

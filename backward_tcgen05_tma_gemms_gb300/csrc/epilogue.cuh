@@ -97,10 +97,29 @@ __device__ __forceinline__ void load_pre32(const Epilogue& e, int64_t row, int64
     load_run32(e.aux + row * e.ld_aux + col0, n, a);
 }
 
+// Debug builds: does the run of n values of row `row` from column col0 lie
+// inside the output?  If not, records TPS_DEVERR_BOUNDS and returns false
+// (the caller skips the store).  Release builds compile this to `true`.
+__device__ __forceinline__ bool dbg_store_ok(const Epilogue& e, int64_t row, int64_t col0, int64_t n) {
+#if TPS_DEBUG
+  if (row < 0 || row >= e.dbg_rows || col0 < 0 || col0 + n > e.dbg_cols) {
+    if (e.dbg_err != nullptr) atomicOr(e.dbg_err, TPS_DEVERR_BOUNDS);
+    return false;
+  }
+#else
+  (void)e;
+  (void)row;
+  (void)col0;
+  (void)n;
+#endif
+  return true;
+}
+
 // Apply the epilogue to 32 consecutive accumulator values of row `row`,
 // columns [col0, col0 + n).
 __device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, int64_t col0, int n,
                                                float (&v)[32]) {
+  if (!dbg_store_ok(e, row, col0, n)) return;
   if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
     store_run32(e.d, e.d_dtype, row * e.ldd + col0, n, v);
   } else if (e.mode == EPI_ACT_FWD) {
@@ -128,6 +147,7 @@ __device__ __forceinline__ void epilogue_run32(const Epilogue& e, int64_t row, i
 // the kernels which never run it do not carry its registers).
 __device__ __forceinline__ void epilogue_glu_bwd_run32(const Epilogue& e, int64_t row, int64_t col0, int n,
                                                        float (&v)[32]) {
+  if (!dbg_store_ok(e, row, col0, n)) return;
   float hg[32], u[32];
   load_run32(e.aux + row * e.ld_aux + col0, n, hg);
   load_run32(e.aux2 + row * e.ld_aux2 + col0, n, u);
@@ -147,6 +167,7 @@ __device__ __forceinline__ void epilogue_glu_bwd_run32(const Epilogue& e, int64_
 // accumulators of the same 32 columns.
 __device__ __forceinline__ void epilogue_glu_run32(const Epilogue& e, int64_t row, int64_t col0, int n,
                                                    float (&hg)[32], float (&u)[32]) {
+  if (!dbg_store_ok(e, row, col0, n)) return;
   store_run32(e.d, TPS_F32, row * e.ldd + col0, n, hg);
   store_run32(e.d3, TPS_F32, row * e.ldd3 + col0, n, u);
 #pragma unroll
@@ -156,6 +177,7 @@ __device__ __forceinline__ void epilogue_glu_run32(const Epilogue& e, int64_t ro
 
 // Scalar form used by the SIMT kernel.
 __device__ __forceinline__ void epilogue_elem(const Epilogue& e, int64_t row, int64_t col, float v) {
+  if (!dbg_store_ok(e, row, col, 1)) return;
   if (e.mode == EPI_STORE || e.mode == EPI_CE_STATS) {
     store_elem(e.d, e.d_dtype, row * e.ldd + col, v);
   } else if (e.mode == EPI_ACT_FWD) {

@@ -12,6 +12,14 @@ namespace tps {
 // Device error word bits (read back by tps_last_device_error).
 constexpr uint32_t TPS_DEVERR_TIMEOUT = 1u;
 constexpr uint32_t TPS_DEVERR_LABEL = 2u;
+constexpr uint32_t TPS_DEVERR_BOUNDS = 4u;  // debug builds: a store outside its output
+
+// The debug build (TPS_DEBUG=1) checks every epilogue and cross-entropy
+// store against the bounds of its output; a store outside is skipped and
+// TPS_DEVERR_BOUNDS recorded.  Release builds compile the checks out.
+#ifndef TPS_DEBUG
+#define TPS_DEBUG 0
+#endif
 
 // ------------------------------------------------------------ epilogues
 // EPI_STORE    D = acc                                  (dtype d_dtype)
@@ -84,6 +92,10 @@ struct Epilogue {
   const void* ce_labels = nullptr;  // the label of each row, int32 or int64
   int ce_label_i64 = 0;
   float* ce_zy = nullptr;           // zy[row]: the logit at the label (labels in [0, N))
+  // Debug builds: the output's extent (rows, columns) and the error word the
+  // bounds checks report to.
+  int64_t dbg_rows = 0, dbg_cols = 0;
+  uint32_t* dbg_err = nullptr;
 };
 
 // One GEMM D[M x N] = sum_k A(m, k) B(k, n), operands addressed by element

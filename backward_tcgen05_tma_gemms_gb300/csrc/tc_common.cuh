@@ -48,7 +48,10 @@ __device__ __forceinline__ void stage_bf16_sw64(uint8_t* buf, int r, const float
   }
 }
 
-// Fused epilogue of one 32 x 32 chunk (lane = row) through TMA stores.
+// Fused epilogue of one 32 x 32 chunk (lane = row) through TMA stores.  The
+// TMA unit clips every box to its tensor map, whose extent is the output's
+// (M, N): a box of a ragged tile that starts past the output writes
+// nothing, so these stores need no bounds check in debug builds.
 // `v` holds the accumulators, `a` the pre-activation for EPI_ACT_BWD (Hg
 // for EPI_GLU_UP).  EPI_ACT_FWD stages its pre-activation in `stg_f32` (a
 // 32 x 32 bf16 box there when d_dtype is bf16) and the activation in
@@ -253,6 +256,7 @@ struct CeTileAcc {
     return m == -INFINITY ? 0.0f : m;
   }
   __device__ __forceinline__ void flush(const Epilogue& e, int64_t row, int64_t stat_tile) const {
+    if (!dbg_store_ok(e, row, stat_tile * kStatsTileN, 1)) return;
     reinterpret_cast<float2*>(e.stats)[row * e.n_tiles + stat_tile] = make_float2(ma, sa);
     if (has_b) reinterpret_cast<float2*>(e.stats_b)[row * e.ce_parts + b] = make_float2(mb, sb);
     e.ce_shift[row * e.ce_shift_ld + stat_tile] = shift();

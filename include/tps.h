@@ -83,7 +83,8 @@ enum {
   TPS_ERR_WORKSPACE = 6, /* workspace missing, too small or misaligned */
   TPS_ERR_CUDA = 7,      /* a CUDA runtime call failed */
   TPS_ERR_TIMEOUT = 8,   /* a device-side wait exceeded its limit */
-  TPS_ERR_ARG = 9        /* NULL where a tensor is required, bad enum */
+  TPS_ERR_ARG = 9,       /* NULL where a tensor is required, bad enum */
+  TPS_ERR_BOUNDS = 10    /* a kernel store fell outside its output (debug builds only) */
 };
 
 /* Split axes of tps_matmul_fwd_bwd ([SG] "解题路线" steps 2-4). */
@@ -363,9 +364,23 @@ int tps_vocab_ce_fwd_bwd_ex(const tps_tensor* h, const tps_tensor* Whead, const 
  * tps_last_device_error -- synchronizes `cuda_stream`, then reads and clears
  * the current device's error word.  Returns TPS_OK, TPS_ERR_TIMEOUT (a
  * kernel gave up waiting and exited early; its outputs are invalid),
- * TPS_ERR_LABEL, or TPS_ERR_CUDA if the synchronization itself failed.
+ * TPS_ERR_LABEL, TPS_ERR_BOUNDS (debug builds: a store outside its output
+ * was skipped), or TPS_ERR_CUDA if the synchronization itself failed.
  * ---------------------------------------------------------------------- */
 int tps_last_device_error(void* cuda_stream);
+
+/* ------------------------------------------------------------------------
+ * tps_build_flags -- how this library was built: TPS_BUILD_DEBUG is set in
+ * the debug build (compiled with TPS_DEBUG=1), whose kernels check every
+ * direct epilogue store, every CE statistics store and every store of the
+ * CE core against the bounds of its output -- the stand-in for a memory
+ * sanitizer (TMA stores need no check: the hardware clips each box to its
+ * tensor map, built with the output's extent).  A store outside its output is skipped
+ * and recorded as TPS_ERR_BOUNDS in the device error word; nothing traps.
+ * No counterpart on the source pages.
+ * ---------------------------------------------------------------------- */
+#define TPS_BUILD_DEBUG 1
+int tps_build_flags(void);
 
 /* ------------------------------------------------------------------------
  * tps_selftest_wait_timeout -- failure-detection self test.  Launches one

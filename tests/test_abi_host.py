@@ -241,3 +241,15 @@ def test_header_is_plain_c(tmp_path):
     if shutil.which("g++"):
         subprocess.run(["g++", "-std=c++11", "-Wall", "-Werror", "-I", inc, "-x", "c++", "-c", str(src), "-o",
                         str(tmp_path / "cpp.o")], check=True)
+
+
+def test_debug_build_reports_its_flag(lib):
+    """The debug build (TPS_DEBUG=1, bounds-checked stores) compiles, loads
+    without a GPU and says what it is; the release build says it is not."""
+    from backward_tcgen05_tma_gemms_gb300 import api, build
+    path = build.build(debug=True)
+    dbg = ctypes.CDLL(path)
+    assert dbg.tps_build_flags() & api.BUILD_DEBUG
+    assert not lib.tps_build_flags() & api.BUILD_DEBUG
+    dbg.tps_strerror.restype = ctypes.c_char_p
+    assert b"debug" in dbg.tps_strerror(api.ERR_BOUNDS)
