@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -955,6 +956,35 @@ extern "C" size_t tps_ce_workspace_bytes_ex(int64_t T, int64_t V, int32_t tp, in
   return ce_ws_layout(T, V, tp, bf16_logits ? 2 : 4).total;
 }
 
+// Runs of a K split for a long-K GEMM on CTA pairs: the count (1..4, every
+// run at least 256 K tiles) whose (tile, run) units fill the waves of
+// resident pairs best, kept only when it fills them at least 5 % better
+// than one run (the partial sums cost an extra read and write of the
+// output per run).  Measured on the dHidden GEMM (V = 128256, d = 4096):
+// T = 2048 (128 tiles, 1.7 waves of 76 pairs) 1.14-1.16 ms with four runs
+// against 1.20-1.21 ms; T = 4096 (3.4 waves) 2.37 ms with two runs against
+// 2.61 ms; T = 8192 (6.7 waves, 0.96 filled) 4.81-4.95 ms with one, two or
+// four runs alike, so it keeps one.
+static int choose_ksplit(int64_t tiles, int64_t k_tiles) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  const int64_t pairs = sms / 2;
+  if (pairs < 1 || tiles < 1) return 1;
+  int best = 1;
+  double best_fill = 0.0, one_run = 0.0;
+  for (int runs = 1; runs <= 4 && k_tiles / runs >= 256; ++runs) {
+    const int64_t units = tiles * runs, rounds = (units + pairs - 1) / pairs;
+    const double fill = double(units) / double(rounds * pairs);
+    if (runs == 1) one_run = fill;
+    if (fill > best_fill + 1e-9) {
+      best = runs;
+      best_fill = fill;
+    }
+  }
+  return best_fill >= 1.05 * one_run ? best : 1;
+}
+
 // Both CE entry points: `opts` NULL is the plain form (every label in
 // [0, V), no reduction); `loss_reduced` and `dWhead` are nullable.
 static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tensor* labels, int32_t tp,
@@ -1124,6 +1154,20 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
     g.b = w.data; g.b_sk = w_out; g.b_sn = w_in;
     g.epi.d = dh.data; g.epi.d_dtype = TPS_F32;
     g.kparts = tp;
+    // The vocabulary is K here and very long, and the output has few pair
+    // tiles (T/256 x d/256): when they make a ragged number of waves, split
+    // K into runs whose partial tiles are added into dHidden in order (the
+    // pages' per-shard partial dHidden, summed) so that the (tile, run)
+    // units fill the waves better.  The per-tile counters live in the
+    // (m, 1/s) region, which the CE core no longer needs.
+    const char* ks = getenv("TPS_CE_KSPLIT");
+    const int ksplit = ks ? atoi(ks) : choose_ksplit(pair_tile_count(T, d), (V + 63) / 64);
+    const size_t flag_bytes = static_cast<size_t>(pair_tile_count(T, d)) * sizeof(uint32_t);
+    if (ksplit > 1 && flag_bytes <= static_cast<size_t>(T) * 2 * sizeof(float)) {
+      if (cudaMemsetAsync(ms, 0, flag_bytes, s) != cudaSuccess) return fail(TPS_ERR_CUDA, "memset failed");
+      g.ksplit = ksplit;
+      g.kflags = reinterpret_cast<uint32_t*>(ms);
+    }
     if ((rc = run_gemm(g, dh.sr, dh.sc, s))) return rc;
   }
   if (want_dw) {  // dWhead = h^T dlogits; shard r's columns are its head slice

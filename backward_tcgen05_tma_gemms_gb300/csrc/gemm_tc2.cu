@@ -83,6 +83,10 @@ struct T2Maps {
 struct T2Params {
   int M, N, K;
   int m_tiles, n_tiles, k_tiles, num_tiles;  // m_tiles counts 256-row pair tiles
+  // K split (GemmDesc::ksplit): work unit u is tile u % num_tiles and run
+  // u / num_tiles of kt_run K tiles; num_units = num_tiles * ksplit
+  int ksplit, kt_run, num_units;
+  uint32_t* kflags;
   int k_end[3];                              // cumulative K tiles of the contraction segments
   int n_segs, n_end[3];                      // column segments: cumulative column ends
   int glu;                                   // EPI_GLU_FWD: b[1] is the up weight
@@ -195,7 +199,9 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       int64_t issued = 0;
       bool ok = true;
       const uint64_t pa = tc_policy(p.pol_a), pb = tc_policy(p.pol_b);
-      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+      for (int u = pair; ok && u < p.num_units; u += npairs) {
+        const int tile = u % p.num_tiles, run = u / p.num_tiles;
+        const int kt_begin = run * p.kt_run, kt_end = min(p.k_tiles, kt_begin + p.kt_run);
         int mt, nt;
         tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
         const int m0 = mt * 2 * T2_BM + static_cast<int>(rank) * T2_BM;
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
           if (nseg > 0) nb0 -= p.n_end[nseg - 1];
         }
         const CUtensorMap* mb0 = (p.glu && rank == 1) ? &m.b[1] : &m.b[nseg];
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = kt_begin; kt < kt_end; ++kt) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
@@ -256,11 +262,13 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(2 * T2_BM, T2_BN, A_MN, B_MN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+      for (int u = pair; ok && u < p.num_units; u += npairs) {
+        const int run = u / p.num_tiles;
+        const int kt_begin = run * p.kt_run, kt_end = min(p.k_tiles, kt_begin + p.kt_run);
         if (!mbar_wait(&bars->tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * T2_BN;
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = kt_begin; kt < kt_end; ++kt) {
           if (!mbar_wait(&bars->full[stage], phase, abort_flag, p.err)) {
             ok = false;
             break;
@@ -274,7 +282,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                                      : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, TC_MN_BOX_BYTES, 1024)
                                      : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kt | kk) != 0 ? 1u : 0u);
+            tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kt != kt_begin || kk != 0) ? 1u : 0u);
           }
           tc_commit_pair_mc(&bars->empty[stage], 0x3);  // frees the stage in both CTAs
           if (++stage == T2_STAGES) {
@@ -305,7 +313,8 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     // accumulator columns this warp drains: 128 (gated: 64 gate + 64 up)
     const int warp_cols = glu ? T2_BN_CTA / 2 : T2_BN / 2;
     uint32_t acc = 0, acc_phase = 0, chunk = 0;
-    for (int tile = pair; tile < p.num_tiles; tile += npairs) {
+    for (int u = pair; u < p.num_units; u += npairs) {
+      const int tile = u % p.num_tiles, run = u / p.num_tiles;
       int mt, nt;
       tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
       const int m0 = mt * 2 * T2_BM + static_cast<int>(rank) * T2_BM;
@@ -328,6 +337,28 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) a_next[i] = 0.0f;
         }
+      }
+      if (p.ksplit > 1 && run > 0) {
+        // K split: the previous run of this tile (all 2 x 8 epilogue warps
+        // of its pair) must be in memory before this run adds to it.
+        uint32_t ready = 1u;
+        if (lane == 0) {
+          const uint32_t need = static_cast<uint32_t>(2 * T2_EPI_WARPS * run);
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(p.kflags + tile) < need) {
+            if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+              if (!*abort_flag) {
+                *abort_flag = 1u;
+                atomicOr(p.err, TPS_DEVERR_TIMEOUT);
+              }
+              ready = 0u;
+              break;
+            }
+            __nanosleep(256);
+          }
+          fence_async_global();
+        }
+        if (!__shfl_sync(0xffffffffu, ready, 0)) break;
       }
       if (!mbar_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
@@ -420,6 +451,13 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         }
         // the fp32 and bf16 slots (store-only: one shared box), single- or double-buffered
         uint8_t* buf = stg + (L::kBufs == 2 ? (chunk & 1u) * L::kBufBytes : 0u);
+        if constexpr (FAM == T2_PLAIN) {
+          if (run > 0) {  // K split: add this run's partial tile to the output
+            tc_store_chunk<1, true, true>(e, &m.d[0], &m.d[1], buf, buf, lane, row0, col0, v, a);
+            ++chunk;
+            continue;
+          }
+        }
         tc_store_chunk<L::kBufs - 1, L::kStoreOnly>(e, &m.d[oseg], &m.d[1], buf,
                                                     L::kStoreOnly ? buf : buf + L::kSecondBox, lane, row0,
                                                     col0 - ocol0, v, a);
@@ -430,6 +468,14 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       if (lane == 0) mbar_arrive_cluster(tmem_empty0_leader + acc * static_cast<uint32_t>(sizeof(uint64_t)));
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
+      if (p.ksplit > 1) {  // K split: this warp's part of the run is in memory
+        if (lane == 0) {
+          bulk_wait0();
+          fence_async_global();
+          red_release_gpu_add(p.kflags + tile, 1u);
+        }
+        __syncwarp();
+      }
     }
     if (p.tma_store && lane == 0) bulk_wait0();
   }
@@ -466,6 +512,19 @@ static int launch_pair_typed(const GemmDesc& g, const T2Maps& m, const T2Params&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.ksplit > 1) {
+    // Under a K split an epilogue waits for a run that another pair holds:
+    // launch only as many pairs as can be resident at once, so that every
+    // run it waits for belongs to a running pair.
+    static std::once_flag cl_once;
+    static int max_clusters = 0;
+    std::call_once(cl_once, [&cfg] {
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_tc2_kernel<A_MN, B_MN, FAM>, &cfg) != cudaSuccess)
+        max_clusters = 0;
+    });
+    if (max_clusters < 1) return TPS_ERR_CUDA;
+    if (pairs > max_clusters) cfg.gridDim = dim3(static_cast<unsigned>(2 * max_clusters), 1, 1);
+  }
   const double flops = 2.0 * double(g.M) * double(g.N) * double(g.K + g.K2 + g.K3) * (p.glu ? 2.0 : 1.0);
   ProfScope prof("gemm_tc", g.name, flops, 0.0, stream);
   const cudaError_t e =
@@ -563,6 +622,8 @@ int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   }
   if (n_segs && nc != g.N) return TPS_ERR_ARG;
   p.num_tiles = p.m_tiles * p.n_tiles;
+  p.ksplit = 1;
+  p.kflags = nullptr;
   // groups of pair tiles cover the same rows as twice as many single tiles
   tc_raster_choice(2 * p.m_tiles, &p.raster_n, &p.group, &p.pol_a, &p.pol_b);
   p.group = (p.group + 1) / 2;
@@ -582,8 +643,16 @@ int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   p.err = dev_err;
   p.tma_store = tc_make_output_maps(g, &m.d[0], &m.d[1], &m.d[2]) ? 1 : 0;
   if (n_segs && !p.tma_store) return TPS_ERR_LAYOUT;  // column segments leave through TMA stores only
+  // K split: plain fp32 stores through TMA, at least one K tile per run
+  if (g.ksplit > 1 && g.kflags != nullptr && g.epi.mode == EPI_STORE && g.epi.d_dtype == TPS_F32 && p.tma_store &&
+      !glu && !k_segs && !n_segs && p.k_tiles >= g.ksplit)
+    p.ksplit = g.ksplit;
+  p.kt_run = (p.k_tiles + p.ksplit - 1) / p.ksplit;
+  p.ksplit = (p.k_tiles + p.kt_run - 1) / p.kt_run;  // every run holds at least one K tile
+  p.num_units = p.num_tiles * p.ksplit;
+  if (p.ksplit > 1) p.kflags = g.kflags;
   const int max_pairs = tc_num_sms() / 2;
-  const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
+  const int pairs = p.num_units < max_pairs ? p.num_units : max_pairs;
 
   return launch_pair_family(g, m, p, pairs, a_mn, b_mn, stream);
 }

@@ -141,8 +141,19 @@ struct GemmDesc {
   int64_t nb_sk[3] = {0, 0, 0}, nb_sn[3] = {0, 0, 0};
   void* nd[3] = {nullptr, nullptr, nullptr};
   int64_t nldd[3] = {0, 0, 0};
+  // K split into ksplit equal runs of K tiles (CTA-pair kernel, EPI_STORE
+  // to an fp32 output through TMA stores): the work units are (tile, run)
+  // pairs, run-major; run 0 stores its partial tile and run s > 0 adds its
+  // partial into the output with a TMA reduction once run s - 1 of the same
+  // tile is in memory, which `kflags` (one zeroed counter per pair tile,
+  // m_tiles x n_tiles) tracks.  The sum is taken in run order, so results
+  // are deterministic.  Ignored (one run) when the conditions do not hold.
+  int ksplit = 1;
+  uint32_t* kflags = nullptr;
   const char* name = "gemm";  // label used by the launch profiler
 };
+// Pair tiles of a GEMM on the CTA-pair kernel (the size of GemmDesc::kflags).
+inline int64_t pair_tile_count(int64_t M, int64_t N) { return ((M + 255) / 256) * ((N + 255) / 256); }
 
 // Launchers (return a TPS_* status; asynchronous on `stream`).
 int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);   // picks one of:

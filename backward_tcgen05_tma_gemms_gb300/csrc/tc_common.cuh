@@ -58,8 +58,9 @@ __device__ __forceinline__ void stage_bf16_sw64(uint8_t* buf, int r, const float
 // `stg_bf16`.  PENDING is the number of this warp's earlier
 // bulk-store groups that may still be reading staging when the buffers are
 // overwritten (0 for one staging buffer, 1 when the caller alternates two).
-// STORE_ONLY: the caller guarantees EPI_STORE.
-template <int PENDING, bool STORE_ONLY = false>
+// STORE_ONLY: the caller guarantees EPI_STORE.  REDUCE (EPI_STORE, fp32):
+// add the box into the output with a TMA reduction instead of storing it.
+template <int PENDING, bool STORE_ONLY = false, bool REDUCE = false>
 __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensorMap* tmD, const CUtensorMap* tmD2,
                                                uint8_t* stg_f32, uint8_t* stg_bf16, int lane, int row0, int col0,
                                                float (&v)[32], const float (&a)[32]) {
@@ -110,6 +111,8 @@ __device__ __forceinline__ void tc_store_chunk(const Epilogue& e, const CUtensor
     if (!STORE_ONLY && (e.mode == EPI_ACT_FWD || e.mode == EPI_GLU_UP)) {
       if (e.d != nullptr) tma_store_2d(tmD, stg_f32, col0, row0);
       tma_store_2d(tmD2, stg_bf16, col0, row0);
+    } else if (REDUCE) {
+      tma_reduce_add_2d(tmD, stg_f32, col0, row0);
     } else {
       tma_store_2d(tmD, e.d_dtype == TPS_F32 ? stg_f32 : stg_bf16, col0, row0);
     }

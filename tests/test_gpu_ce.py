@@ -226,3 +226,21 @@ def test_fused_core_matches_two_kernels(T, V, tp, monkeypatch):
     assert rc_a == 0 and rc_b == 0
     for x, y, name in zip(a, b, ("loss", "dlogits", "dHidden", "owner")):
         assert torch.equal(x, y), name
+
+
+@pytest.mark.parametrize("ksplit", ["1", "3", "4"])
+def test_dhidden_k_split(orc, ksplit, monkeypatch):
+    """dHidden = dlogits Whead^T with its K (the vocabulary) cut into runs
+    of K tiles, each run's partial tile added into dHidden in run order by
+    TMA reductions once the previous run of the same tile is in memory
+    (the default is two runs).  V = 5000 gives 79 K tiles, so three and
+    four runs are unequal, and 600 tokens leave a ragged last pair tile.
+    Every run count matches the oracle, and two calls give identical bits:
+    the order of the partial sums is fixed."""
+    monkeypatch.setenv("TPS_CE_KSPLIT", ksplit)
+    h, W, labels = inputs.ce_case(11, 600, 256, 5000, torch.bfloat16, w_std=0.2)
+    check(orc, h, W, labels, 4, True, what=f"{ksplit} runs")
+    a, rc_a = run(h, W, labels, 4)
+    b, rc_b = run(h, W, labels, 4)
+    assert rc_a == 0 and rc_b == 0
+    assert torch.equal(a[2], b[2])
