@@ -377,8 +377,9 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                 if (row < p.M) epilogue_run32(e, row, col0, n, v);
                 return;
               }
-              uint8_t* buf = stg + (chunk & 1u) * L::kBufBytes;
-              tc_store_chunk<1, true>(e, &m.d[0], &m.d[1], buf, buf, lane, row0, static_cast<int>(col0), v, a);
+              uint8_t* buf = stg + (L::kBufs == 2 ? (chunk & 1u) * L::kBufBytes : 0u);
+              tc_store_chunk<L::kBufs - 1, true>(e, &m.d[0], &m.d[1], buf, buf, lane, row0, static_cast<int>(col0),
+                                                 v, a);
               ++chunk;
             });
             if (have) e.ce_zy[row] = zy;
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         uint8_t* buf = stg + (L::kBufs == 2 ? (chunk & 1u) * L::kBufBytes : 0u);
         if constexpr (FAM == T2_PLAIN) {
           if (run > 0) {  // K split: add this run's partial tile to the output
-            tc_store_chunk<1, true, true>(e, &m.d[0], &m.d[1], buf, buf, lane, row0, col0, v, a);
+            tc_store_chunk<L::kBufs - 1, true, true>(e, &m.d[0], &m.d[1], buf, buf, lane, row0, col0, v, a);
             ++chunk;
             continue;
           }

@@ -233,20 +233,38 @@ __host__ __device__ inline int64_t shard_offset(int64_t dim, int64_t parts, int6
 }
 
 // ------------------------------------------------------------ activations
+// 2^x with the hardware approximation (flushes subnormal results to 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // GELU (erf form) x * Phi(x), with CUDA's erff; tanh with CUDA's tanhf.
 // GELU tanh approximation 0.5 x (1 + tanh(z)), z = sqrt(2/pi) (x + 0.044715
 // x^3), evaluated through the identity 0.5 (1 + tanh(z)) = 1 / (1 + e^{-2z})
-// (one exponential and one division instead of a tanh); the exponent is
-// clamped at 80, where the sigmoid is already 0 in fp32.  Derivatives are
-// those of the definitions: for the tanh form, with s = 1/(1 + e^{-2z}),
-// d/dx = s + 2 x s (1 - s) sqrt(2/pi) (1 + 3 * 0.044715 x^2).
-__device__ __forceinline__ float gelu_tanh_sigmoid(float x) {
-  const float z = 0.79788456080286536f * (x + 0.044715f * x * x * x);
-  return __fdividef(1.0f, 1.0f + __expf(fminf(-2.0f * z, 80.0f)));
+// = 1 / (1 + 2^{x (k1 + k3 x^2)}), k1 = -2 sqrt(2/pi) log2(e), k3 = 0.044715
+// k1 (one ex2 and one reciprocal, the constants folded so that the
+// epilogues spend few instructions per element); the exponent is clamped at
+// 80 log2(e), where the sigmoid is already 0 in fp32.  Derivatives are those
+// of the definitions: for the tanh form, with s = 1/(1 + e^{-2z}),
+// d/dx = s + 2 x s (1 - s) sqrt(2/pi) (1 + 3 * 0.044715 x^2)
+//      = s + x (c1 + c3 x^2) (s - s^2), c1 = 2 sqrt(2/pi), c3 = 3 * 0.044715 c1.
+constexpr float kGeluK1 = -2.0f * 0.79788456080286536f * 1.4426950408889634f;
+constexpr float kGeluK3 = 0.044715f * kGeluK1;
+constexpr float kGeluC1 = 2.0f * 0.79788456080286536f;
+constexpr float kGeluC3 = 3.0f * 0.044715f * kGeluC1;
+constexpr float kExpClampLog2 = 80.0f * 1.4426950408889634f;
+__device__ __forceinline__ float gelu_tanh_sigmoid_x2(float x, float x2) {
+  return __fdividef(1.0f, 1.0f + ex2_approx(fminf(x * fmaf(kGeluK3, x2, kGeluK1), kExpClampLog2)));
 }
-// Logistic sigma(x) = 1 / (1 + e^{-x}); the exponent is clamped at 80
-// (sigma is already 0 in fp32 there) so the division never sees infinity.
-__device__ __forceinline__ float logistic(float x) { return __fdividef(1.0f, 1.0f + __expf(fminf(-x, 80.0f))); }
+__device__ __forceinline__ float gelu_tanh_sigmoid(float x) { return gelu_tanh_sigmoid_x2(x, x * x); }
+// Logistic sigma(x) = 1 / (1 + e^{-x}) = 1 / (1 + 2^{-x log2(e)}); the
+// exponent is clamped at 80 log2(e) (sigma is already 0 in fp32 there) so the
+// division never sees infinity.
+__device__ __forceinline__ float logistic(float x) {
+  return __fdividef(1.0f, 1.0f + ex2_approx(fminf(x * -1.4426950408889634f, kExpClampLog2)));
+}
 __device__ __forceinline__ float act_fwd(int act, float x) {
   if (act == TPS_ACT_GELU_ERF) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
   if (act == TPS_ACT_GELU_TANH) return x * gelu_tanh_sigmoid(x);
@@ -260,12 +278,13 @@ __device__ __forceinline__ float act_grad(int act, float x) {
     return cdf + x * pdf;
   }
   if (act == TPS_ACT_GELU_TANH) {
-    const float s = gelu_tanh_sigmoid(x);
-    return s + 2.0f * x * s * (1.0f - s) * 0.79788456080286536f * (1.0f + 3.0f * 0.044715f * x * x);
+    const float x2 = x * x;
+    const float s = gelu_tanh_sigmoid_x2(x, x2);
+    return fmaf(x * fmaf(kGeluC3, x2, kGeluC1), fmaf(-s, s, s), s);
   }
   if (act == TPS_ACT_SILU) {  // d/dx x s(x) = s + x s (1 - s)
     const float s = logistic(x);
-    return s + x * s * (1.0f - s);
+    return fmaf(x, fmaf(-s, s, s), s);
   }
   const float h = tanhf(x);
   return 1.0f - h * h;
@@ -290,7 +309,7 @@ __device__ __forceinline__ void act_fwd_grad(int act, float x, float& f, float& 
   if (act == TPS_ACT_SILU) {
     const float s = logistic(x);
     f = x * s;
-    g = s + x * s * (1.0f - s);
+    g = fmaf(x, fmaf(-s, s, s), s);
   } else {
     f = act_fwd(act, x);
     g = act_grad(act, x);
