@@ -216,6 +216,28 @@ __device__ __forceinline__ float ce_chunk_sum(const float (&v)[32], int i0, int 
   return acc;
 }
 
+// Max of all 32 elements, and sum of e^{v - m} over all 32, for the chunks
+// that lie entirely in one shard's real columns (all but a few per row): no
+// per-element range tests, and a tree / four partial sums instead of one
+// serial chain.
+__device__ __forceinline__ float ce_max32(const float (&v)[32]) {
+  float m[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m[i] = fmaxf(v[i], v[i + 16]);
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
+}
+__device__ __forceinline__ float ce_sum32(const float (&v)[32], float m) {
+  const float ml = m * kTcLog2e;
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i & 3] += ex2_approx(fmaf(v[i], kTcLog2e, -ml));
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 // The shard owning column c under the array_split of n into p parts.
 __device__ __forceinline__ int64_t shard_of(int64_t c, int64_t n, int64_t p) {
   const int64_t q = n / p, r = n % p, big = r * (q + 1);
@@ -245,12 +267,20 @@ struct CeTileAcc {
   __device__ __forceinline__ void fold_max(const float (&v)[32], int64_t col0, int n, int64_t vreal) {
     int na, nn;
     parts(col0, n, vreal, na, nn);
+    if (na == 32) {  // the whole chunk is real and in shard a
+      ma = fmaxf(ma, ce_max32(v));
+      return;
+    }
     ma = fmaxf(ma, ce_chunk_max(v, 0, na));
     mb = fmaxf(mb, ce_chunk_max(v, na, nn));
   }
   __device__ __forceinline__ void fold_sum(const float (&v)[32], int64_t col0, int n, int64_t vreal) {
     int na, nn;
     parts(col0, n, vreal, na, nn);
+    if (na == 32) {
+      sa += ce_sum32(v, ma);
+      return;
+    }
     if (na > 0) sa += ce_chunk_sum(v, 0, na, ma);
     if (nn > na) sb += ce_chunk_sum(v, na, nn, mb);
   }
