@@ -280,6 +280,8 @@ static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream)
     t.b3_sk = g.a3_sk;
     t.b3_sn = g.a3_sm;
     t.epi.ldd = d_sn;
+    t.wide = false;
+    if (g.ce_grad.ms != nullptr) return fail(TPS_ERR_LAYOUT, "%s: the CE-gradient operand needs a row-major output", g.name);
     g = t;
   } else {
     g.epi.ldd = d_sm;
@@ -287,7 +289,13 @@ static int run_gemm(GemmDesc g, int64_t d_sm, int64_t d_sn, cudaStream_t stream)
   g.epi.dbg_rows = g.M;  // the output as the kernels write it (row-major M x N)
   g.epi.dbg_cols = g.N;
   g.epi.dbg_err = err;
-  const int rc = gemm_tc_supported(g) ? launch_gemm_tc(g, err, stream) : launch_gemm_simt(g, err, stream);
+  int rc;
+  if (g.wide && gemm_wide_supported(g))
+    rc = launch_gemm_wide(g, err, stream);
+  else if (g.ce_grad.ms != nullptr)
+    return fail(TPS_ERR_ARG, "%s: the CE-gradient operand needs the wide-tile kernel", g.name);
+  else
+    rc = gemm_tc_supported(g) ? launch_gemm_tc(g, err, stream) : launch_gemm_simt(g, err, stream);
   if (rc == TPS_ERR_CUDA) return fail(rc, "%s: launch failed: %s", g.name, cudaGetErrorString(cudaGetLastError()));
   return rc;
 }
@@ -960,11 +968,13 @@ extern "C" size_t tps_ce_workspace_bytes_ex(int64_t T, int64_t V, int32_t tp, in
 // run at least 256 K tiles) whose (tile, run) units fill the waves of
 // resident pairs best, kept only when it fills them at least 5 % better
 // than one run (the partial sums cost an extra read and write of the
-// output per run).  Measured on the dHidden GEMM (V = 128256, d = 4096):
-// T = 2048 (128 tiles, 1.7 waves of 76 pairs) 1.14-1.16 ms with four runs
-// against 1.20-1.21 ms; T = 4096 (3.4 waves) 2.37 ms with two runs against
-// 2.61 ms; T = 8192 (6.7 waves, 0.96 filled) 4.81-4.95 ms with one, two or
-// four runs alike, so it keeps one.
+// output per run).  Measured on the dHidden GEMM (V = 128256, d = 4096)
+// with 256 x 256 tiles: T = 2048 (128 tiles, 1.7 waves of 76 pairs)
+// 1.14-1.16 ms with four runs against 1.20-1.21 ms; T = 4096 (3.4 waves)
+// 2.37 ms with two runs against 2.61 ms; T = 8192 (6.7 waves, 0.96 filled)
+// 4.81-4.95 ms with one, two or four runs alike, so it keeps one.  With
+// 256 x 512 tiles T = 8192 makes 256 tiles (3.4 waves): two runs, 4.34-4.40
+// ms against 5.09-5.15 with one.
 static int choose_ksplit(int64_t tiles, int64_t k_tiles) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -1118,6 +1128,39 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
     g.epi.ce_zy = zy;
   }
   if ((rc = run_gemm(g, V, 1, s))) return rc;
+  // dHidden = sum_r dlogits_r Whead_r^T: rank sum in the K loop
+  GemmDesc gh;
+  gh.name = "ce_dhidden";
+  gh.M = T; gh.N = d; gh.K = V; gh.in_dtype = dt;
+  gh.a = dl.data; gh.a_sm = dl.sr; gh.a_sk = 1;
+  gh.b = w.data; gh.b_sk = w_out; gh.b_sn = w_in;
+  gh.epi.d = dh.data; gh.epi.d_dtype = TPS_F32; gh.epi.ldd = dh.sr;
+  gh.kparts = tp;
+  // Wide (256 x 512) pair tiles for this long-K GEMM: 2-4 % faster than
+  // 256 x 256 at T = 2048-8192 (TPS_CE_WIDE=0 keeps the 256-wide tiles).
+  // TPS_CE_GRAD_IN_GEMM=1 (plain bf16 form) forms dlogits from the shifted
+  // logits inside it, after the combine alone; measured 2.2 times slower
+  // than the CE core and this GEMM together, so it is off by default.
+  const char* wv = getenv("TPS_CE_WIDE");
+  const char* gv = getenv("TPS_CE_GRAD_IN_GEMM");
+  gh.wide = fused && dh.sc == 1 && (wv ? atoi(wv) != 0 : true);
+  bool grad_in_gemm = gh.wide && !ext && dt == TPS_BF16 && (gv ? atoi(gv) != 0 : false);
+  if (gh.wide && !gemm_wide_supported(gh)) gh.wide = grad_in_gemm = false;
+  if (grad_in_gemm) {
+    GemmDesc gx = gh;
+    gx.a = z; gx.a_sm = V;  // the shifted bf16 logits
+    gx.ce_grad.ms = ms;
+    gx.ce_grad.shift = shift;
+    gx.ce_grad.shift_ld = ce_shift_ld(V);
+    gx.ce_grad.labels = labels->data;
+    gx.ce_grad.label_i64 = labels->dtype == TPS_I64 ? 1 : 0;
+    gx.ce_grad.dlogits = dl.data;
+    gx.ce_grad.ldg = dl.sr;
+    if (gemm_wide_supported(gx))
+      gh = gx;
+    else
+      grad_in_gemm = false;
+  }
   {
     CeDesc c;
     c.T = T; c.V = V; c.parts = tp;
@@ -1143,32 +1186,32 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
     }
     uint32_t* err = dev_err_ptr();
     if (err == nullptr) return fail(TPS_ERR_CUDA, "cannot resolve the device error word");
-    rc = fused ? launch_ce_from_tile_stats(c, tile_stats, n_tiles, ms, err, s) : launch_ce(c, err, s, nullptr);
+    if (grad_in_gemm)
+      rc = launch_ce_combine(c, tile_stats, n_tiles, ms, err, s);
+    else
+      rc = fused ? launch_ce_from_tile_stats(c, tile_stats, n_tiles, ms, err, s) : launch_ce(c, err, s, nullptr);
     if (rc) return fail(rc, "ce launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   }
-  {  // dHidden = sum_r dlogits_r Whead_r^T: rank sum in the K loop
-    GemmDesc g;
-    g.name = "ce_dhidden";
-    g.M = T; g.N = d; g.K = V; g.in_dtype = dt;
-    g.a = dl.data; g.a_sm = dl.sr; g.a_sk = 1;
-    g.b = w.data; g.b_sk = w_out; g.b_sn = w_in;
-    g.epi.d = dh.data; g.epi.d_dtype = TPS_F32;
-    g.kparts = tp;
+  {
     // The vocabulary is K here and very long, and the output has few pair
-    // tiles (T/256 x d/256): when they make a ragged number of waves, split
-    // K into runs whose partial tiles are added into dHidden in order (the
-    // pages' per-shard partial dHidden, summed) so that the (tile, run)
-    // units fill the waves better.  The per-tile counters live in the
-    // (m, 1/s) region, which the CE core no longer needs.
+    // tiles: when they make a ragged number of waves, split K into runs
+    // whose partial tiles are added into dHidden in order (the pages'
+    // per-shard partial dHidden, summed) so that the (tile, run) units fill
+    // the waves better.  The per-tile counters live in a region the CE
+    // core has finished with: the (m, 1/s) rows, or, when the GEMM forms
+    // dlogits and still reads them, the tile statistics.
+    const int64_t tiles = gh.wide ? wide_tile_count(T, d) : pair_tile_count(T, d);
     const char* ks = getenv("TPS_CE_KSPLIT");
-    const int ksplit = ks ? atoi(ks) : choose_ksplit(pair_tile_count(T, d), (V + 63) / 64);
-    const size_t flag_bytes = static_cast<size_t>(pair_tile_count(T, d)) * sizeof(uint32_t);
-    if (ksplit > 1 && flag_bytes <= static_cast<size_t>(T) * 2 * sizeof(float)) {
-      if (cudaMemsetAsync(ms, 0, flag_bytes, s) != cudaSuccess) return fail(TPS_ERR_CUDA, "memset failed");
-      g.ksplit = ksplit;
-      g.kflags = reinterpret_cast<uint32_t*>(ms);
+    const int ksplit = ks ? atoi(ks) : choose_ksplit(tiles, (V + 63) / 64);
+    const size_t flag_bytes = static_cast<size_t>(tiles) * sizeof(uint32_t);
+    uint32_t* flags = reinterpret_cast<uint32_t*>(gh.wide ? tile_stats : ms);
+    const size_t room = gh.wide ? static_cast<size_t>(T) * static_cast<size_t>(n_tiles) * 8 : static_cast<size_t>(T) * 8;
+    if (ksplit > 1 && flag_bytes <= room) {
+      if (cudaMemsetAsync(flags, 0, flag_bytes, s) != cudaSuccess) return fail(TPS_ERR_CUDA, "memset failed");
+      gh.ksplit = ksplit;
+      gh.kflags = flags;
     }
-    if ((rc = run_gemm(g, dh.sr, dh.sc, s))) return rc;
+    if ((rc = run_gemm(gh, dh.sr, dh.sc, s))) return rc;
   }
   if (want_dw) {  // dWhead = h^T dlogits; shard r's columns are its head slice
     GemmDesc g;

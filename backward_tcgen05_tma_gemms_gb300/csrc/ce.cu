@@ -1340,6 +1340,25 @@ int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t 
   return cudaPeekAtLastError() == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
 }
 
+// The combine alone, for the path whose dlogits are formed inside the
+// dHidden GEMM (CeGradOperand): the loss, the owner and each row's
+// (m, 1/s).  Plain form only (no options).
+int launch_ce_combine(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms, uint32_t* dev_err,
+                      cudaStream_t stream) {
+  if (c.T == 0) return TPS_OK;
+  if (c.options || c.zy == nullptr) return TPS_ERR_ARG;
+  CeParams p = make_params(c, dev_err);
+  p.stats = c.stats;  // statistics of the tiles in which a shard starts
+  p.n_tiles = n_tiles;
+  const int64_t nb = (c.T + CEF_TOK_PER_BLOCK - 1) / CEF_TOK_PER_BLOCK;
+  if (nb > 0x7FFFFFFF) return TPS_ERR_SHAPE;
+  const double bytes = double(c.T) * double(n_tiles) * 8.0 + double(c.T) * 20.0;
+  ProfScope prof("ce_combine", "ce_core", 0.0, bytes, stream);
+  ce_combine_kernel<<<static_cast<unsigned>(nb), 32 * CEF_TOK_PER_BLOCK, 0, stream>>>(p, tile_stats, n_tiles, ms);
+  note_launch();
+  return cudaPeekAtLastError() == cudaSuccess ? TPS_OK : TPS_ERR_CUDA;
+}
+
 // ------------------------------------------------------------ host
 bool ce_cluster_supported(int64_t V, int32_t parts, int /*dlogits_dtype*/) {
   if (parts < 1 || parts > CE_MAX_CLUSTER) return false;

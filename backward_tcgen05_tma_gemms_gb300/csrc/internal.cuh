@@ -98,6 +98,24 @@ struct Epilogue {
   uint32_t* dbg_err = nullptr;
 };
 
+// The vocabulary CE's gradient as the A operand of the dHidden GEMM, formed
+// from the logits GEMM's shifted bf16 logits as their tiles arrive in
+// shared memory: A(t, j) = e^{z_tj - m_t} / s_t - 1[j = y_t], with z_tj
+// stored as bf16(z_tj - c), c the shift of the 128-column statistics tile
+// holding column j.  The GEMM's A pointer is then the shifted logits (K =
+// the vocabulary), and the tile pass over the output's first column block
+// also writes A once to `dlogits` (bf16, leading dimension ldg).  Rows
+// whose label lies outside [0, K) get no one-hot term.
+struct CeGradOperand {
+  const float* ms = nullptr;     // T x 2: (m, 1/s) of each row
+  const float* shift = nullptr;  // shift[t * shift_ld + j / kStatsTileN]
+  int64_t shift_ld = 0;
+  const void* labels = nullptr;  // T labels, int32 or int64
+  int label_i64 = 0;
+  void* dlogits = nullptr;
+  int64_t ldg = 0;
+};
+
 // One GEMM D[M x N] = sum_k A(m, k) B(k, n), operands addressed by element
 // strides: A(m, k) = a[m * a_sm + k * a_sk], B(k, n) = b[k * b_sk + n * b_sn].
 // One stride of each operand is 1 (its contiguous dimension).
@@ -150,16 +168,26 @@ struct GemmDesc {
   // are deterministic.  Ignored (one run) when the conditions do not hold.
   int ksplit = 1;
   uint32_t* kflags = nullptr;
+  // Wide tiles (gemm_wide.cu): 256 x 512 pair tiles with one accumulator,
+  // for long contractions whose epilogue is a small part of each tile
+  // (EPI_STORE to fp32 through TMA, A K-major); kflags then has one
+  // counter per wide tile (wide_tile_count).  ce_grad.ms set: A is formed
+  // as the CE gradient (CeGradOperand), which needs the wide tiles.
+  bool wide = false;
+  CeGradOperand ce_grad;
   const char* name = "gemm";  // label used by the launch profiler
 };
 // Pair tiles of a GEMM on the CTA-pair kernel (the size of GemmDesc::kflags).
 inline int64_t pair_tile_count(int64_t M, int64_t N) { return ((M + 255) / 256) * ((N + 255) / 256); }
+inline int64_t wide_tile_count(int64_t M, int64_t N) { return ((M + 255) / 256) * ((N + 511) / 512); }
 
 // Launchers (return a TPS_* status; asynchronous on `stream`).
 int launch_gemm_tc(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);   // picks one of:
 int launch_gemm_tc1(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);  // one CTA per tile
 int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);  // CTA pairs
 int launch_gemm_simt(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);
+int launch_gemm_wide(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream);  // wide CTA-pair tiles
+bool gemm_wide_supported(const GemmDesc& g);
 bool gemm_tc_supported(const GemmDesc& g);
 
 struct CeDesc {
@@ -205,6 +233,10 @@ struct CeDesc {
 int launch_ce_from_tile_stats(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms,
                               uint32_t* dev_err, cudaStream_t stream);
 bool ce_tile_stats_supported(int64_t V, int32_t parts);
+// Only the combine of launch_ce_from_tile_stats (loss, owner, (m, 1/s) in
+// `ms`), for dlogits formed inside the dHidden GEMM; plain form only.
+int launch_ce_combine(const CeDesc& c, const float* tile_stats, int64_t n_tiles, float* ms, uint32_t* dev_err,
+                      cudaStream_t stream);
 
 // Picks the one-read cluster kernel when the shard plan allows it, else the
 // two-pass kernels.  `used_cluster` reports the choice.

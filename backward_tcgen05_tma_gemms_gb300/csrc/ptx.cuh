@@ -67,6 +67,21 @@ __device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint64_t* bar, uint32_t 
 }
 constexpr uint32_t kWaitSuspendNs = 100000;
 
+// The same suspending try_wait with cluster-scope acquire: for a barrier
+// whose arrivals come from threads of the other CTA of a pair, so that their
+// writes before the (release, cluster) arrive are visible to this thread.
+__device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok;
+}
+
 // Bounded wait for the phase with the given parity.  `abort_flag` (shared
 // memory) lets one role tell the others to stop waiting after a timeout.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
@@ -86,6 +101,20 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, vo
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                           uint32_t* err) {
   return mbar_wait_for(bar, parity, abort_flag, err, kWaitLimitNs);
+}
+// Bounded wait with cluster-scope acquire (see mbar_try_wait_cluster).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                  uint32_t* err) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity, kWaitSuspendNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1u;
+      atomicOr(err, TPS_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // Wait without honouring the abort flag (used to drain in-flight copies or

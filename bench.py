@@ -77,7 +77,7 @@ def bench_config(world):
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
-GEMM_SOURCES = ["gemm_tc.cu", "gemm_tc2.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh", "internal.cuh"]
+GEMM_SOURCES = ["gemm_tc.cu", "gemm_tc2.cu", "gemm_wide.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh", "internal.cuh"]
 
 
 def kernel_source_hash(names):

@@ -198,3 +198,25 @@ def test_ce_ex_guard(T, d, V, tp, layout):
     ws = workspace("ce_ex workspace", api.ce_workspace_bytes(T, V, tp))
     api.vocab_ce_fwd_bwd_ex(h, W, y, tp, layout, workspace=ws.t, out=[g.t for g in gs], **kw)
     check_all(gs + [ws], list(refs) + [None])
+
+
+@pytest.mark.parametrize("form", ["pair", "wide", "grad"])
+@pytest.mark.parametrize("T,d,V,tp,layout", [(300, 128, 4096, 7, "in_out"), (600, 640, 5000, 4, "out_in")])
+def test_ce_wide_guard(T, d, V, tp, layout, form, monkeypatch):
+    """The dHidden GEMM with a K split in three runs: on 256 x 256 tiles
+    ("pair"), on 256 x 512 tiles ("wide", the default), and on 256 x 512
+    tiles forming dlogits and storing them ("grad"); ragged rows, a
+    128-column second output tile, a last K tile of 8 columns."""
+    monkeypatch.setenv("TPS_CE_WIDE", "0" if form == "pair" else "1")
+    monkeypatch.setenv("TPS_CE_GRAD_IN_GEMM", "1" if form == "grad" else "0")
+    monkeypatch.setenv("TPS_CE_KSPLIT", "3")
+    h, W, labels = inputs.ce_case(T + V + d, T, d, V, torch.bfloat16, w_std=0.2)
+    if layout == "out_in":
+        W = W.t().contiguous()
+    h, W, labels = h.cuda(), W.cuda(), labels.cuda()
+    gs = guard(("loss", (T,), torch.float32), ("dlogits", (T, V), torch.bfloat16), ("dHidden", (T, d), torch.float32),
+               ("owner", (T,), torch.int32))
+    refs = api.vocab_ce_fwd_bwd(h, W, labels, tp, layout, out=plain(gs))
+    ws = workspace("ce workspace", api.ce_workspace_bytes(T, V, tp, torch.bfloat16))
+    api.vocab_ce_fwd_bwd(h, W, labels, tp, layout, workspace=ws.t, out=[g.t for g in gs])
+    check_all(gs + [ws], list(refs) + [None])
