@@ -300,7 +300,7 @@ def run_gpu(args, rank, world, local_rank):
     # and library calls stalled the GPU for tens of ms whenever the host
     # fell behind).  The first step's input copies and the last step's
     # result copies run outside the graphs, inside the timed region.
-    # Every tensor above COPY_CHUNK bytes is split over --copy-streams
+    # Every tensor above --copy-chunk-mb is split over --copy-streams
     # streams per direction: the host link moves about 270 GB/s both ways
     # at once with two streams per direction, 170 GB/s with one.
     pinned = {k: v.pin_memory() for k, v in host.items()}
@@ -324,11 +324,11 @@ def run_gpu(args, rank, world, local_rank):
 
     def pieces(tensors):
         """(key, first, end) flat slices of the tensors, the large ones split
-        into COPY_CHUNK-sized parts."""
+        into --copy-chunk-mb parts."""
         out = []
         for k, t in tensors.items():
             n = t.numel()
-            step = max(1, COPY_CHUNK // t.element_size())
+            step = max(1, (args.copy_chunk_mb << 20) // t.element_size())
             for j in range(0, n, step):
                 out.append((k, j, min(n, j + step)))
         return out
@@ -555,6 +555,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-widened", action="store_true", help="skip timing the rows beyond the step")
     ap.add_argument("--copy-streams", type=int, default=2, help="end-to-end copy streams per direction")
+    ap.add_argument("--copy-chunk-mb", type=int, default=COPY_CHUNK >> 20,
+                    help="end-to-end copies of larger tensors are split into chunks of this many MiB")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
