@@ -1198,18 +1198,31 @@ static int ce_impl(const tps_tensor* h, const tps_tensor* Whead, const tps_tenso
     // whose partial tiles are added into dHidden in order (the pages'
     // per-shard partial dHidden, summed) so that the (tile, run) units fill
     // the waves better.  The per-tile counters live in a region the CE
-    // core has finished with: the (m, 1/s) rows, or, when the GEMM forms
-    // dlogits and still reads them, the tile statistics.
+    // core has finished with: the tile statistics on the tensor-core path
+    // (the GEMM that forms dlogits itself still reads the (m, 1/s) rows),
+    // else the (m, 1/s) rows.
     const int64_t tiles = gh.wide ? wide_tile_count(T, d) : pair_tile_count(T, d);
     const char* ks = getenv("TPS_CE_KSPLIT");
     const int ksplit = ks ? atoi(ks) : choose_ksplit(tiles, (V + 63) / 64);
-    const size_t flag_bytes = static_cast<size_t>(tiles) * sizeof(uint32_t);
-    uint32_t* flags = reinterpret_cast<uint32_t*>(gh.wide ? tile_stats : ms);
-    const size_t room = gh.wide ? static_cast<size_t>(T) * static_cast<size_t>(n_tiles) * 8 : static_cast<size_t>(T) * 8;
-    if (ksplit > 1 && flag_bytes <= room) {
+    // One more counter after the per-tile ones hands out the work units in
+    // order: at T = 8192 the wide-tile GEMM took 4.35-4.40 ms against
+    // 4.55-4.57 with the static round-robin, whose pairs drift apart over
+    // their 2004-step tiles (TPS_CE_DYNAMIC=0 keeps the round-robin).  The
+    // counter needs a zeroed word, which the fp32-logits paths' (m, 1/s)
+    // region cannot spare beside the per-tile counters, so it runs on the
+    // tensor-core path only.
+    const char* dv = getenv("TPS_CE_DYNAMIC");
+    const bool dynamic = fused && (dv ? atoi(dv) != 0 : true);
+    const size_t flag_bytes = static_cast<size_t>(tiles + (dynamic ? 1 : 0)) * sizeof(uint32_t);
+    uint32_t* flags = reinterpret_cast<uint32_t*>(fused ? tile_stats : ms);
+    const size_t room = fused ? static_cast<size_t>(T) * static_cast<size_t>(n_tiles) * 8 : static_cast<size_t>(T) * 8;
+    if ((ksplit > 1 || dynamic) && flag_bytes <= room) {
       if (cudaMemsetAsync(flags, 0, flag_bytes, s) != cudaSuccess) return fail(TPS_ERR_CUDA, "memset failed");
-      gh.ksplit = ksplit;
-      gh.kflags = flags;
+      if (ksplit > 1) {
+        gh.ksplit = ksplit;
+        gh.kflags = flags;
+      }
+      if (dynamic) gh.unit_counter = flags + tiles;
     }
     if ((rc = run_gemm(gh, dh.sr, dh.sc, s))) return rc;
   }

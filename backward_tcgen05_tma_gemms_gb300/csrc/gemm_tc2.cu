@@ -67,9 +67,15 @@ struct T2Barriers {
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
+  uint64_t sched_full[kUnitRing];  // PairUnits ring (dynamic schedule)
+  uint64_t sched_empty[kUnitRing];
+  int32_t sched_unit[kUnitRing];
   uint32_t tmem_slot;
   uint32_t abort;
 };
+// Readers of each unit the dynamic schedule publishes: the even CTA's MMA
+// thread, both CTAs' epilogue warps and the odd CTA's producer.
+constexpr int T2_SCHED_READERS = 2 + 2 * T2_EPI_WARPS;
 
 
 // Tensor maps of one launch: a[s], b[s] are the operands of contraction
@@ -87,6 +93,7 @@ struct T2Params {
   // u / num_tiles of kt_run K tiles; num_units = num_tiles * ksplit
   int ksplit, kt_run, num_units;
   uint32_t* kflags;
+  uint32_t* unit_counter;  // dynamic schedule (GemmDesc::unit_counter), else nullptr
   int k_end[3];                              // cumulative K tiles of the contraction segments
   int n_segs, n_end[3];                      // column segments: cumulative column ends
   int glu;                                   // EPI_GLU_FWD: b[1] is the up weight
@@ -171,6 +178,10 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       mbar_init(&bars->tmem_empty[b], 2 * T2_EPI_WARPS);
     }
     mbar_init(&bars->drain, 1);
+    for (int s = 0; s < kUnitRing; ++s) {
+      mbar_init(&bars->sched_full[s], 1);
+      mbar_init(&bars->sched_empty[s], T2_SCHED_READERS);
+    }
     bars->abort = 0u;
     fence_mbar_init();
   }
@@ -191,6 +202,9 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
   const uint32_t tmem_base = bars->tmem_slot;
   const uint32_t full0_leader = cluster_map(smem_u32(&bars->full[0]), 0);
   const uint32_t tmem_empty0_leader = cluster_map(smem_u32(&bars->tmem_empty[0]), 0);
+  PairUnits units;
+  units.init(bars->sched_full, bars->sched_empty, bars->sched_unit, abort_flag, p.err, p.unit_counter, pair, npairs,
+             p.num_units, warp == 0 && rank == 0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -199,7 +213,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       int64_t issued = 0;
       bool ok = true;
       const uint64_t pa = tc_policy(p.pol_a), pb = tc_policy(p.pol_b);
-      for (int u = pair; ok && u < p.num_units; u += npairs) {
+      for (int u = units.take(); ok && u >= 0; u = units.take()) {
         const int tile = u % p.num_tiles, run = u / p.num_tiles;
         const int kt_begin = run * p.kt_run, kt_end = min(p.k_tiles, kt_begin + p.kt_run);
         int mt, nt;
@@ -262,7 +276,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(2 * T2_BM, T2_BN, A_MN, B_MN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = pair; ok && u < p.num_units; u += npairs) {
+      for (int u = units.take(); ok && u >= 0; u = units.take()) {
         const int run = u / p.num_tiles;
         const int kt_begin = run * p.kt_run, kt_end = min(p.k_tiles, kt_begin + p.kt_run);
         if (!mbar_wait(&bars->tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     // accumulator columns this warp drains: 128 (gated: 64 gate + 64 up)
     const int warp_cols = glu ? T2_BN_CTA / 2 : T2_BN / 2;
     uint32_t acc = 0, acc_phase = 0, chunk = 0;
-    for (int u = pair; u < p.num_units; u += npairs) {
+    for (int u = units.take_warp(lane); u >= 0; u = units.take_warp(lane)) {
       const int tile = u % p.num_tiles, run = u / p.num_tiles;
       int mt, nt;
       tc_raster(p.raster_n, p.group, p.m_tiles, p.n_tiles, tile, mt, nt);
@@ -625,6 +639,7 @@ int launch_gemm_tc2(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) {
   p.num_tiles = p.m_tiles * p.n_tiles;
   p.ksplit = 1;
   p.kflags = nullptr;
+  p.unit_counter = g.unit_counter;
   // groups of pair tiles cover the same rows as twice as many single tiles
   tc_raster_choice(2 * p.m_tiles, &p.raster_n, &p.group, &p.pol_a, &p.pol_b);
   p.group = (p.group + 1) / 2;

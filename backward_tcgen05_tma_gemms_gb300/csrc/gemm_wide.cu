@@ -61,6 +61,9 @@ constexpr int W_THREADS = 320;
 constexpr int W_EPI_WARPS = 8;
 constexpr uint32_t W_TMEM_COLS = 512;                 // one fp32 accumulator, 256 columns per MMA
 constexpr int W_STG = TC_STG_F32_BYTES;               // one 4 KB box per epilogue warp
+// Readers of each unit the dynamic schedule publishes (PairUnits): the even
+// CTA's MMA thread, both CTAs' epilogue warps and the odd CTA's producer.
+constexpr int W_SCHED_READERS = 2 + 2 * W_EPI_WARPS;
 
 struct WBarriers {
   uint64_t full[W_STAGES];
@@ -69,6 +72,9 @@ struct WBarriers {
   uint64_t tmem_full;
   uint64_t tmem_empty;
   uint64_t drain;
+  uint64_t sched_full[kUnitRing];   // PairUnits ring
+  uint64_t sched_empty[kUnitRing];
+  int32_t sched_unit[kUnitRing];
   uint32_t tmem_slot;
   uint32_t abort;
 };
@@ -85,6 +91,7 @@ struct WParams {
   // K split as in gemm_tc2.cu: unit u is tile u % num_tiles, run u / num_tiles
   int ksplit, kt_run, num_units;
   uint32_t* kflags;
+  uint32_t* unit_counter;  // dynamic schedule (GemmDesc::unit_counter), else nullptr
   int group;
   Epilogue epi;
   CeGradOperand xf;
@@ -136,6 +143,10 @@ __global__ void __launch_bounds__(W_THREADS, 1) gemm_wide_kernel(const __grid_co
     mbar_init(&bars->tmem_full, 1);
     mbar_init(&bars->tmem_empty, 2 * W_EPI_WARPS);
     mbar_init(&bars->drain, 1);
+    for (int s = 0; s < kUnitRing; ++s) {
+      mbar_init(&bars->sched_full[s], 1);
+      mbar_init(&bars->sched_empty[s], W_SCHED_READERS);
+    }
     bars->abort = 0u;
     fence_mbar_init();
   }
@@ -153,6 +164,9 @@ __global__ void __launch_bounds__(W_THREADS, 1) gemm_wide_kernel(const __grid_co
   const uint32_t tmem_base = bars->tmem_slot;
   const uint32_t full0_leader = cluster_map(smem_u32(&bars->full[0]), 0);
   const uint32_t tmem_empty_leader = cluster_map(smem_u32(&bars->tmem_empty), 0);
+  PairUnits units;
+  units.init(bars->sched_full, bars->sched_empty, bars->sched_unit, abort_flag, p.err, p.unit_counter, pair, npairs,
+             p.num_units, warp == 0 && rank == 0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -160,7 +174,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) gemm_wide_kernel(const __grid_co
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int u = pair; ok && u < p.num_units; u += npairs) {
+      for (int u = units.take(); ok && u >= 0; u = units.take()) {
         const int tile = u % p.num_tiles, run = u / p.num_tiles;
         const int kt_begin = run * p.kt_run, kt_end = min(p.k_tiles, kt_begin + p.kt_run);
         int mt, nt;
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) gemm_wide_kernel(const __grid_co
       constexpr uint32_t idesc = idesc_bf16_f32(2 * W_BM, W_BN / 2, false, B_MN);
       uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = pair; ok && u < p.num_units; u += npairs) {
+      for (int u = units.take(); ok && u >= 0; u = units.take()) {
         const int run = u / p.num_tiles;
         const int kt_begin = run * p.kt_run, kt_end = min(p.k_tiles, kt_begin + p.kt_run);
         if (!mbar_wait(&bars->tmem_empty, acc_phase ^ 1u, abort_flag, p.err)) break;
@@ -273,7 +287,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) gemm_wide_kernel(const __grid_co
     for (int i = 0; i < 4; ++i) rr[i] = ew * 16 + (lane >> 3) + 4 * i;
     uint32_t stage = 0, phase = 0, acc_phase = 0;
     bool ok = true;
-    for (int u = pair; ok && u < p.num_units; u += npairs) {
+    for (int u = units.take_warp(lane); ok && u >= 0; u = units.take_warp(lane)) {
       const int tile = u % p.num_tiles, run = u / p.num_tiles;
       const int kt_begin = run * p.kt_run, kt_end = min(p.k_tiles, kt_begin + p.kt_run);
       int mt, nt;
@@ -524,6 +538,7 @@ int launch_gemm_wide(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) 
   p.ksplit = 1;
   p.kflags = nullptr;
   if (g.ksplit > 1 && g.kflags != nullptr && p.k_tiles >= g.ksplit) p.ksplit = g.ksplit;
+  p.unit_counter = g.unit_counter;
   p.kt_run = (p.k_tiles + p.ksplit - 1) / p.ksplit;
   if (xf && (p.kt_run & 1) && p.ksplit > 1) ++p.kt_run;  // runs start on a statistics tile (two K tiles)
   p.ksplit = (p.k_tiles + p.kt_run - 1) / p.kt_run;     // every run holds at least one K tile

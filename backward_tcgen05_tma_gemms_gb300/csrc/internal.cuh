@@ -175,6 +175,10 @@ struct GemmDesc {
   // as the CE gradient (CeGradOperand), which needs the wide tiles.
   bool wide = false;
   CeGradOperand ce_grad;
+  // Wide tiles only: when set (a zeroed counter), the pairs take their work
+  // units in increasing order from this counter as they finish the previous
+  // one, instead of the static round-robin (pair p: units p, p + pairs, ...).
+  uint32_t* unit_counter = nullptr;
   const char* name = "gemm";  // label used by the launch profiler
 };
 // Pair tiles of a GEMM on the CTA-pair kernel (the size of GemmDesc::kflags).

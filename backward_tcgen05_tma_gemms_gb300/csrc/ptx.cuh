@@ -388,6 +388,9 @@ __device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t caddr) {
   return v;
 }
 
+__device__ __forceinline__ void st_cluster_u32(uint32_t caddr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_cluster_f32x2(uint32_t caddr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(caddr), "f"(a), "f"(b) : "memory");
 }

@@ -349,6 +349,84 @@ __device__ __forceinline__ void ce_stats_tile(const Epilogue& e, uint32_t t_col,
   if (row_ok) st.flush(e, row, tc0 / kStatsTileN);
 }
 
+// ---- work units of a CTA pair ---------------------------------------------
+// The units one role of a CTA pair processes, in order.  Static: pair p
+// takes units p, p + pairs, p + 2 pairs, ...  Dynamic (a zeroed global
+// counter given): the even CTA's producer takes each next unit from the
+// counter when it starts on it and publishes it through a ring of
+// kUnitRing slots in both CTAs' shared memory, where the other roles read
+// it; a unit past the end tells them to stop.  Units are taken in
+// increasing order and every pair works through its own in order, so a
+// K-split run only ever waits for a unit that a running pair took earlier.
+// Each slot's `empty` barrier (even CTA) counts `readers` arrivals.
+constexpr int kUnitRing = 4;
+struct PairUnits {
+  uint64_t* full;   // [kUnitRing], this CTA: the slot's unit has been written
+  uint64_t* empty;  // [kUnitRing], this CTA (used in the even CTA)
+  int32_t* unit;    // [kUnitRing], this CTA's copy
+  uint32_t empty0_leader, full0_peer, unit0_peer;  // cluster addresses
+  volatile uint32_t* abort_flag;
+  uint32_t* err;
+  uint32_t* counter;
+  uint32_t slot, phase;
+  int next, step, num_units;
+  bool writer;
+
+  __device__ __forceinline__ void init(uint64_t* full_, uint64_t* empty_, int32_t* unit_, volatile uint32_t* abort_,
+                                       uint32_t* err_, uint32_t* counter_, int pair, int npairs, int num_units_,
+                                       bool writer_) {
+    full = full_;
+    empty = empty_;
+    unit = unit_;
+    empty0_leader = cluster_map(smem_u32(empty_), 0);
+    full0_peer = cluster_map(smem_u32(full_), 1);
+    unit0_peer = cluster_map(smem_u32(unit_), 1);
+    abort_flag = abort_;
+    err = err_;
+    counter = counter_;
+    slot = 0;
+    phase = 0;
+    next = pair;
+    step = npairs;
+    num_units = num_units_;
+    writer = writer_;
+  }
+  // The next unit, or -1 when there is none left (or a wait timed out).
+  __device__ __forceinline__ int take() {
+    if (counter == nullptr) {
+      const int u = next;
+      next += step;
+      return u < num_units ? u : -1;
+    }
+    int u;
+    if (writer) {
+      // the odd CTA's readers released their copy of the slot from the other CTA
+      if (!mbar_wait_cluster(&empty[slot], phase ^ 1u, abort_flag, err)) return -1;
+      u = static_cast<int>(atomicAdd(counter, 1u));
+      unit[slot] = u;
+      st_cluster_u32(unit0_peer + slot * 4u, static_cast<uint32_t>(u));
+      mbar_arrive(&full[slot]);
+      mbar_arrive_cluster(full0_peer + slot * static_cast<uint32_t>(sizeof(uint64_t)));
+    } else {
+      if (!mbar_wait_cluster(&full[slot], phase, abort_flag, err)) return -1;
+      u = reinterpret_cast<volatile int32_t*>(unit)[slot];
+      mbar_arrive_cluster(empty0_leader + slot * static_cast<uint32_t>(sizeof(uint64_t)));
+    }
+    if (++slot == kUnitRing) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    return u < num_units ? u : -1;
+  }
+  // One reader per warp: lane 0 takes the unit and hands it to the warp.
+  __device__ __forceinline__ int take_warp(int lane) {
+    if (counter == nullptr) return take();
+    int u = 0;
+    if (lane == 0) u = take();
+    return __shfl_sync(0xffffffffu, u, 0);
+  }
+};
+
 // ---- tile raster and L2 policy -------------------------------------------
 // Tiles are walked in groups of `group` M-tiles, M fastest (raster_n = 0),
 // or groups of `group` N-tiles, N fastest (raster_n = 1).

@@ -129,3 +129,27 @@ def test_grad_in_gemm_llama_sampled(orc, monkeypatch):
     assert_close(dh[toks], rdh, True, "dHidden")
     assert np.array_equal(own[toks].numpy(), rown)
     assert torch.isfinite(loss).all()
+
+
+@pytest.mark.parametrize("wide", ["1", "0"])
+@pytest.mark.parametrize("ksplit", ["1", "2", "3"])
+@pytest.mark.parametrize("T,d,V,tp", [(600, 640, 5000, 4), (2048, 1024, 16032, 8)])
+def test_dynamic_schedule_bits(orc, wide, ksplit, T, d, V, tp, monkeypatch):
+    """TPS_CE_DYNAMIC=1 (the default): the pairs take their (tile, K run)
+    units in order from a counter instead of round-robin, on 256 x 512 and
+    on 256 x 256 tiles.  Each unit computes the same sums in the same order,
+    so every output is bit-identical to the static schedule, K split
+    included; and it matches the oracle."""
+    monkeypatch.setenv("TPS_CE_WIDE", wide)
+    monkeypatch.setenv("TPS_CE_KSPLIT", ksplit)
+    h, W, labels = inputs.ce_case(T + d + V, T, d, V, torch.bfloat16, w_std=0.2)
+    monkeypatch.setenv("TPS_CE_DYNAMIC", "0")
+    ref, rc0 = run(h, W, labels, tp)
+    monkeypatch.setenv("TPS_CE_DYNAMIC", "1")
+    got, rc1 = run(h, W, labels, tp)
+    assert rc0 == rc1 == 0
+    for x, y, name in zip(ref, got, ("loss", "dlogits", "dHidden", "owner")):
+        assert torch.equal(x, y), name
+    if T <= 600:
+        rl, rdl, rdh, rown = orc.ce_tokens(inputs.as_f64(h), inputs.as_f64(W), labels.numpy(), tp)
+        assert_close(got[2], rdh, True, "dHidden")
