@@ -175,9 +175,10 @@ struct GemmDesc {
   // as the CE gradient (CeGradOperand), which needs the wide tiles.
   bool wide = false;
   CeGradOperand ce_grad;
-  // Wide tiles only: when set (a zeroed counter), the pairs take their work
-  // units in increasing order from this counter as they finish the previous
-  // one, instead of the static round-robin (pair p: units p, p + pairs, ...).
+  // CTA-pair kernels (wide and 256 x 256 tiles): when set (a zeroed
+  // counter), the pairs take their work units in increasing order from this
+  // counter as they start on them, instead of the static round-robin (pair
+  // p: units p, p + pairs, ...).  Results are the same bits either way.
   uint32_t* unit_counter = nullptr;
   const char* name = "gemm";  // label used by the launch profiler
 };
