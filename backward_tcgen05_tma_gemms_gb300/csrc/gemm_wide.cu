@@ -525,14 +525,14 @@ int launch_gemm_wide(const GemmDesc& g, uint32_t* dev_err, cudaStream_t stream) 
   p.n_tiles = static_cast<int>((g.N + W_BN - 1) / W_BN);
   p.k_tiles = static_cast<int>((g.K + TC_BK - 1) / TC_BK);
   p.num_tiles = p.m_tiles * p.n_tiles;
-  // Groups of four pair rows (TPS_GEMM_GROUP counts 128-row tiles, as on
-  // the other kernels): on the dHidden GEMM of the Llama shapes they
-  // measured 1-2 % faster than eight (T = 8192: 4.27-4.36 against
-  // 4.34-4.40 ms), and a long K keeps no panel in L2 from one wave to the
-  // next anyway.
+  // Groups of eight pair rows (TPS_GEMM_GROUP counts 128-row tiles, as on
+  // the other kernels).  On the dHidden GEMM at T = 8192 with the units
+  // taken in order: 1, 2, 4, 8, 16 pair rows took 4.37-4.41, 4.30-4.32,
+  // 4.26-4.28, 4.24-4.25, 4.29-4.33 ms (with the static round-robin four
+  // had been 1-2 % faster than eight).
   int raster_n = 0, group = 0, pa = 0, pb = 0;
   tc_raster_choice(2 * p.m_tiles, &raster_n, &group, &pa, &pb);
-  p.group = getenv("TPS_GEMM_GROUP") != nullptr ? (group + 1) / 2 : 4;
+  p.group = getenv("TPS_GEMM_GROUP") != nullptr ? (group + 1) / 2 : 8;
   if (p.group < 1) p.group = 1;
   if (p.group > p.m_tiles) p.group = p.m_tiles;
   p.ksplit = 1;
