@@ -153,3 +153,43 @@ def test_dynamic_schedule_bits(orc, wide, ksplit, T, d, V, tp, monkeypatch):
     if T <= 600:
         rl, rdl, rdh, rown = orc.ce_tokens(inputs.as_f64(h), inputs.as_f64(W), labels.numpy(), tp)
         assert_close(got[2], rdh, True, "dHidden")
+
+
+def test_llama_out_in_head_sampled(orc):
+    """The Llama-3 vocabulary at full size with the head in (V, d) layout
+    (torch's lm_head weight): the logits GEMM reads the head K-major and the
+    wide dHidden GEMM reads it MN-major.  64 tokens with labels at both ends
+    of every shard, full dlogits and dHidden rows against the oracle."""
+    cfg = inputs.LLAMA_CE
+    T, V, tp = cfg["T"], cfg["V"], cfg["tp"]
+    h, W, labels = inputs.ce_case(0, T, cfg["d"], V, torch.bfloat16)
+    toks = spread_tokens(T, 64, 11)
+    labels[torch.from_numpy(toks)] = torch.from_numpy(boundary_labels(V, tp))
+    (loss, dlog, dh, own), rc = run(h, W.t().contiguous(), labels, tp, "out_in")
+    assert rc == 0
+    rl, rdl, rdh, rown = orc.ce_tokens(inputs.as_f64(h), inputs.as_f64(W), labels.numpy(), tp, toks)
+    assert_close(loss[toks], rl, True, "loss")
+    assert_close(dlog[toks], rdl, True, "dlogits")
+    assert_close(dh[toks], rdh, True, "dHidden")
+    assert np.array_equal(own[toks].numpy(), rown)
+
+
+@pytest.mark.parametrize("ksplit", [None, "3"])
+def test_ragged_multiwave_sampled(orc, ksplit, monkeypatch):
+    """T = 3000 (a partial pair of row tiles), d = 1536 (three 512-column
+    tiles), V = 32000 at tp = 8 (500 K steps): 36 wide tiles, which the
+    default K split turns into 72 (tile, run) units (one wave) and three
+    runs into 108 (1.4 waves), taken in order; 48 sampled tokens against
+    the oracle, including the last rows."""
+    if ksplit:
+        monkeypatch.setenv("TPS_CE_KSPLIT", ksplit)
+    T, d, V, tp = 3000, 1536, 32000, 8
+    h, W, labels = inputs.ce_case(17, T, d, V, torch.bfloat16, w_std=0.05)
+    toks = spread_tokens(T, 48, 13)
+    (loss, dlog, dh, own), rc = run(h, W, labels, tp)
+    assert rc == 0
+    rl, rdl, rdh, rown = orc.ce_tokens(inputs.as_f64(h), inputs.as_f64(W), labels.numpy(), tp, toks)
+    assert_close(loss[toks], rl, True, "loss")
+    assert_close(dlog[toks], rdl, True, "dlogits")
+    assert_close(dh[toks], rdh, True, "dHidden")
+    assert np.array_equal(own[toks].numpy(), rown)
